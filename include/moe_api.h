@@ -1,0 +1,186 @@
+/*
+ * moe_api.h -- C ABI of the GB300 (sm_103a) forward pass of one top-k-routed
+ * SwiGLU mixture-of-experts layer.
+ *
+ * The layer (page "Mixture of Experts in vLLM - From First Principles to
+ * fused_moe", below [vLLM]):
+ *   logits = x W_r^T (+ bias)                      "One token uses only 8 experts"
+ *   p = softmax(logits); keep top_k; renormalize   "One token uses only 8 experts"
+ *   group the M*top_k (token, expert) pairs by
+ *   expert, padded to BLOCK_SIZE_M blocks          "The two index lists"
+ *   a_p = SiLU(h_gate) * h_up, h = W13_e x_t       "An expert is a small SwiGLU MLP"
+ *   y_t = sum_j w_j W2_{e_j} a_{t*top_k+j}         "Put the results back, and combine
+ *                                                   them per token"
+ *
+ * Conventions shared by every entry point
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller; the
+ *     library never frees, keeps or reallocates it.  Tensors are dense and
+ *     row-major.  bf16 tensors hold raw bfloat16 bit patterns (moe_bf16_t).
+ *   - Every call is asynchronous on `stream`, allocates no memory and never
+ *     synchronises with the host (except moe_get_device_status).
+ *   - Pointers to bf16 matrices are 16-byte aligned; the workspace pointer is
+ *     256-byte aligned (MOE_ERR_INVALID_ARG otherwise).
+ *   - Weight layouts follow nn.Linear (the reduction dimension is
+ *     contiguous): W13 [E, 2I, H] with gate rows [0, I) above up rows
+ *     [I, 2I) ([vLLM] "An expert is a small SwiGLU MLP"); W2 [E, H, I];
+ *     W_r [E, H].
+ *   - Pair id p = t * top_k + j ([vLLM] "A batch: (token, expert) pairs").
+ *   - Limits: 1 <= E <= 1024; 1 <= top_k <= min(E, 32); H, I multiples of 16
+ *     with 16 <= H, I <= 65536; M >= 0 (M == 0 is a no-op returning MOE_OK);
+ *     1 <= block_size_m <= 256, or 0 for the automatic choice where the
+ *     entry point allows it.  M * top_k < 2^31 - 2^18.
+ *   - Rounding: bf16 round-to-nearest-even of fp32 values at the logits, the
+ *     GEMM-1 output h, the activation a and the output y; fp32 accumulation;
+ *     the GEMM-2 output is not rounded before the weighted combine.
+ *
+ * Errors: shape, pointer and size problems are found on the host before any
+ * launch and returned (nothing is launched).  A failed launch returns
+ * MOE_ERR_CUDA.  Data-dependent problems (an expert id outside [0, E) in a
+ * caller-given topk_ids) are written to a status word at the start of the
+ * workspace and read back by moe_get_device_status; kernels never trap.
+ */
+#ifndef MOE_API_H
+#define MOE_API_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t moe_bf16_t; /* raw bfloat16 bit pattern */
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,          /* null pointer, negative size, bad flag */
+    MOE_ERR_UNSUPPORTED_SHAPE = 2,    /* outside the limits above */
+    MOE_ERR_WORKSPACE_TOO_SMALL = 3,  /* ws_bytes < moe_workspace_size(...) */
+    MOE_ERR_CUDA = 4,                 /* a CUDA runtime call or launch failed */
+    MOE_ERR_DEVICE_BAD_EXPERT_ID = 5, /* device status: topk_ids entry outside [0, E) */
+    MOE_ERR_DEVICE_TIMEOUT = 6        /* device status: a bounded wait ran out */
+} moe_status_t;
+
+/* Bytes of workspace that moe_forward, moe_align_block_size and
+ * moe_grouped_gemm_w2_combine need for any M <= M_max with these shapes.
+ * block_size_m = 0 sizes for every block size the automatic choice may
+ * pick.  The workspace is the per-layer buffer set that the MoE execution
+ * analysis page ("Memory allocation per step") proposes to allocate once and
+ * reuse across layers: one buffer, reused by every layer and every call.
+ * Returns 0 when the arguments are outside the limits. */
+size_t moe_workspace_size(int M_max, int E, int top_k, int H, int I, int block_size_m);
+
+/* Entries of sorted_token_ids for M tokens: M*top_k + E*(B-1), rounded up to
+ * a multiple of B.  expert_ids has capacity / B entries.  [vLLM] "The two
+ * index lists": each expert's group is padded up to a multiple of B.
+ * Returns -1 when the arguments are outside the limits (B must be explicit). */
+long moe_align_capacity(int M, int top_k, int E, int block_size_m);
+
+/* The block size moe_forward uses when given block_size_m = 0. */
+int moe_pick_block_size(int M, int E, int top_k, int H, int I);
+
+/* S0. Router logits.  [vLLM] "One token uses only 8 experts": W_r [E, H]
+ * gives one score per expert.
+ *   logits[t, e] = bf16( sum_h x[t, h] * w_router[e, h] + router_bias[e] )
+ * x [M, H] bf16; w_router [E, H] bf16; router_bias [E] fp32 or NULL;
+ * logits [M, E] bf16 (output). */
+moe_status_t moe_router_logits(const moe_bf16_t *x, const moe_bf16_t *w_router,
+                               const float *router_bias, int M, int E, int H,
+                               moe_bf16_t *logits, cudaStream_t stream);
+
+/* S1. Softmax, top-k and renormalize.  [vLLM] "One token uses only 8
+ * experts", steps 1-3.  Slot j of token t holds the j-th largest logit; equal
+ * logits go to the lower expert id.  With renormalize != 0 the kept weights
+ * are rescaled to sum to 1, otherwise they are the softmax probabilities.
+ * logits [M, E] bf16; topk_ids [M, top_k] int32 (output); topk_weights
+ * [M, top_k] fp32 (output).  Logits must be finite. */
+moe_status_t moe_topk_softmax(const moe_bf16_t *logits, int M, int E, int top_k,
+                              int renormalize, int32_t *topk_ids, float *topk_weights,
+                              cudaStream_t stream);
+
+/* S2. Group the pairs by expert.  [vLLM] "The two index lists" and
+ * "Group by expert": sorted_token_ids lists the pair ids grouped by expert in
+ * ascending expert id, ascending pair id inside a group (a stable counting
+ * sort), each group padded with the id M*top_k up to a multiple of B;
+ * experts with no pair get no block.  expert_ids[b] is the expert of block b;
+ * expert_offsets[e] is where expert e's padded group starts
+ * (expert_offsets[E] = n_post); *num_tokens_post_padded = n_post.
+ * Entries of sorted_token_ids at and after n_post and of expert_ids at and
+ * after n_post / B are left unspecified.
+ * topk_ids [M*top_k] int32; sorted_token_ids [moe_align_capacity()] int32,
+ * expert_ids [capacity / B] int32, expert_offsets [E + 1] int32,
+ * num_tokens_post_padded [1] int32 (outputs).  block_size_m must be explicit.
+ * ws/ws_bytes: the workspace (status word and scratch counters).  An id
+ * outside [0, E) is left out of the grouping and reported as
+ * MOE_ERR_DEVICE_BAD_EXPERT_ID through moe_get_device_status. */
+moe_status_t moe_align_block_size(const int32_t *topk_ids, int M, int top_k, int E,
+                                  int block_size_m, int32_t *sorted_token_ids,
+                                  int32_t *expert_ids, int32_t *expert_offsets,
+                                  int32_t *num_tokens_post_padded, void *ws, size_t ws_bytes,
+                                  cudaStream_t stream);
+
+/* S3. Grouped GEMM 1 with SiLU-and-mul.  [vLLM] "One GEMM 1 program, step by
+ * step" and "The rest of the layer stays in pair order": for every real pair
+ * p in block b (p < M*top_k), with e = expert_ids[b] and t = p / top_k,
+ *   h = bf16(W13_e x_t)  [2I];   a[p, i] = bf16( SiLU(h[i]) * h[I + i] )
+ * Input rows are read in place through p / top_k (no permuted copy).
+ * x [M, H]; w13 [E, 2I, H]; sorted_token_ids / expert_ids /
+ * num_tokens_post_padded as produced by moe_align_block_size with the same
+ * M, top_k, E and block_size_m (explicit); a [M*top_k, I] bf16 (output, pair
+ * order).  Blocks whose expert id lies outside [0, E) are skipped. */
+moe_status_t moe_grouped_gemm_w13_act(const moe_bf16_t *x, const moe_bf16_t *w13,
+                                      const int32_t *sorted_token_ids, const int32_t *expert_ids,
+                                      const int32_t *num_tokens_post_padded, int M, int top_k,
+                                      int E, int H, int I, int block_size_m, moe_bf16_t *a,
+                                      cudaStream_t stream);
+
+/* S4. Grouped GEMM 2 with the router-weighted combine.  [vLLM] "The rest of
+ * the layer stays in pair order" and "Put the results back, and combine them
+ * per token":
+ *   o_p = W2_e a_p (fp32, not rounded);
+ *   y[t] = bf16( sum_j topk_weights[t, j] * o_{t*top_k + j} + residual[t] )
+ * a [M*top_k, I]; w2 [E, H, I]; topk_weights [M, top_k] fp32; residual
+ * [M, H] bf16 or NULL; y [M, H] bf16 (output).  Index lists as for S3.
+ * ws/ws_bytes: the workspace (holds the fp32 accumulator). */
+moe_status_t moe_grouped_gemm_w2_combine(const moe_bf16_t *a, const moe_bf16_t *w2,
+                                         const int32_t *sorted_token_ids,
+                                         const int32_t *expert_ids,
+                                         const int32_t *num_tokens_post_padded,
+                                         const float *topk_weights, const moe_bf16_t *residual,
+                                         int M, int top_k, int E, int H, int I, int block_size_m,
+                                         moe_bf16_t *y, void *ws, size_t ws_bytes,
+                                         cudaStream_t stream);
+
+/* The whole layer: S0 (skipped when router_logits is given) .. S4.
+ * Exactly one of w_router [E, H] and router_logits [M, E] is non-NULL.
+ * router_bias [E] fp32 or NULL (only with w_router); residual [M, H] or NULL.
+ * y [M, H] bf16 (output); topk_ids_out [M, top_k] int32 and
+ * topk_weights_out [M, top_k] fp32 are optional copies of the routing.
+ * block_size_m = 0 picks moe_pick_block_size(M, E, top_k, H, I).
+ * ws_bytes >= moe_workspace_size(M, E, top_k, H, I, block_size_m). */
+moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *w_router,
+                         const moe_bf16_t *router_logits, const float *router_bias,
+                         const moe_bf16_t *w13, const moe_bf16_t *w2,
+                         const moe_bf16_t *residual, int M, int E, int top_k, int H, int I,
+                         int renormalize, int block_size_m, moe_bf16_t *y,
+                         int32_t *topk_ids_out, float *topk_weights_out, void *ws,
+                         size_t ws_bytes, cudaStream_t stream);
+
+/* Clears the whole workspace (asynchronously on `stream`).  Call it once on a
+ * freshly allocated workspace before its first use: the status word at its
+ * start must begin at zero.  ws must be 256-byte aligned. */
+moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Synchronises `stream`, returns the device status word kept at the start of
+ * the workspace (MOE_OK if no kernel reported a problem) and clears it. */
+moe_status_t moe_get_device_status(void *ws, cudaStream_t stream);
+
+/* A static, human-readable name for a status code. */
+const char *moe_status_string(moe_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_API_H */

@@ -1,0 +1,259 @@
+"""Python binding of the GB300 MoE-layer CUDA library (``libmoe_gb300.so``).
+
+Argument marshalling only: every step of the layer runs in the library's CUDA
+kernels.  PyTorch supplies device memory and streams.  The functions keep the
+C ABI's names (``include/moe_api.h``); each takes preallocated torch tensors
+for its outputs and raises ``MoeError`` on a non-OK status.  There is no CPU
+fallback: if the library is missing or cannot be loaded, every call raises.
+
+The layer follows the page "Mixture of Experts in vLLM - From First
+Principles to fused_moe": router logits, softmax / top-k / renormalize,
+grouping of the (token, expert) pairs by expert into block-padded
+sorted_token_ids / expert_ids, grouped GEMM 1 with SiLU(gate) * up, grouped
+GEMM 2 with the router-weighted per-token combine.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import _build
+
+__all__ = [
+    "MoeError", "load_library", "library_path", "moe_workspace_size", "moe_align_capacity",
+    "moe_pick_block_size", "moe_workspace_init", "moe_router_logits", "moe_topk_softmax",
+    "moe_align_block_size", "moe_grouped_gemm_w13_act", "moe_grouped_gemm_w2_combine",
+    "moe_forward", "moe_get_device_status", "moe_status_string", "Workspace",
+]
+
+STATUS_NAMES = {
+    0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
+    3: "MOE_ERR_WORKSPACE_TOO_SMALL", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE_BAD_EXPERT_ID",
+    6: "MOE_ERR_DEVICE_TIMEOUT",
+}
+
+# Every symbol include/moe_api.h declares.
+EXPORTED = (
+    "moe_workspace_size", "moe_align_capacity", "moe_pick_block_size", "moe_router_logits",
+    "moe_topk_softmax", "moe_align_block_size", "moe_grouped_gemm_w13_act",
+    "moe_grouped_gemm_w2_combine", "moe_forward", "moe_workspace_init", "moe_get_device_status",
+    "moe_status_string",
+)
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__(f"{where}: {STATUS_NAMES.get(self.status, self.status)}")
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library(build_if_missing: bool = False):
+    """Load the CUDA library (optionally building it first)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        if not build_if_missing:
+            raise RuntimeError(f"CUDA library not built: {path} is missing "
+                               "(run `python -c 'import __graft_entry__ as g; g.build()'`)")
+        _build.build()
+    lib = ctypes.CDLL(path)
+    P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    sig = {
+        "moe_workspace_size": ([I, I, I, I, I, I], Z),
+        "moe_align_capacity": ([I, I, I, I], ctypes.c_long),
+        "moe_pick_block_size": ([I, I, I, I, I], I),
+        "moe_router_logits": ([P, P, P, I, I, I, P, P], I),
+        "moe_topk_softmax": ([P, I, I, I, I, P, P, P], I),
+        "moe_align_block_size": ([P, I, I, I, I, P, P, P, P, P, Z, P], I),
+        "moe_grouped_gemm_w13_act": ([P, P, P, P, P, I, I, I, I, I, I, P, P], I),
+        "moe_grouped_gemm_w2_combine": ([P, P, P, P, P, P, P, I, I, I, I, I, I, P, P, Z, P], I),
+        "moe_forward": ([P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, P, P, Z, P], I),
+        "moe_workspace_init": ([P, Z, P], I),
+        "moe_get_device_status": ([P, P], I),
+        "moe_status_string": ([I], ctypes.c_char_p),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = lib
+    return lib
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def _p(t):
+    """Device pointer of a tensor (None for None)."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _check_dtype(t, dtype, name):
+    if t is not None and t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ok(rc: int, where: str):
+    if rc != 0:
+        raise MoeError(rc, where)
+
+
+# ----------------------------------------------------------------------------- sizes
+
+def moe_workspace_size(M_max: int, E: int, top_k: int, H: int, I: int, block_size_m: int = 0) -> int:
+    n = load_library().moe_workspace_size(M_max, E, top_k, H, I, block_size_m)
+    if n == 0:
+        raise MoeError(2, "moe_workspace_size")
+    return int(n)
+
+
+def moe_align_capacity(M: int, top_k: int, E: int, block_size_m: int) -> int:
+    n = load_library().moe_align_capacity(M, top_k, E, block_size_m)
+    if n < 0:
+        raise MoeError(2, "moe_align_capacity")
+    return int(n)
+
+
+def moe_pick_block_size(M: int, E: int, top_k: int, H: int, I: int) -> int:
+    return int(load_library().moe_pick_block_size(M, E, top_k, H, I))
+
+
+def moe_status_string(status: int) -> str:
+    return load_library().moe_status_string(int(status)).decode()
+
+
+class Workspace:
+    """One caller-owned workspace buffer, sized once and reused by every call."""
+
+    def __init__(self, M_max: int, E: int, top_k: int, H: int, I: int, block_size_m: int = 0,
+                 device=None, stream=None):
+        self.nbytes = moe_workspace_size(M_max, E, top_k, H, I, block_size_m)
+        self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device or "cuda")
+        moe_workspace_init(self.buf, stream=stream)
+
+    @property
+    def ptr(self):
+        return ctypes.c_void_p(self.buf.data_ptr())
+
+
+def _ws(ws):
+    if isinstance(ws, Workspace):
+        return ws.ptr, ws.nbytes
+    return _p(ws), ws.numel() * ws.element_size()
+
+
+def moe_workspace_init(ws, stream=None) -> None:
+    ptr, n = _ws(ws)
+    _ok(load_library().moe_workspace_init(ptr, n, _stream(stream)), "moe_workspace_init")
+
+
+def moe_get_device_status(ws, stream=None) -> int:
+    """Synchronises the stream; returns and clears the device status word."""
+    ptr, _ = _ws(ws)
+    return int(load_library().moe_get_device_status(ptr, _stream(stream)))
+
+
+# ----------------------------------------------------------------------------- the steps
+
+def moe_router_logits(x, w_router, logits, router_bias=None, stream=None) -> None:
+    _check_dtype(x, torch.bfloat16, "x")
+    _check_dtype(w_router, torch.bfloat16, "w_router")
+    _check_dtype(logits, torch.bfloat16, "logits")
+    _check_dtype(router_bias, torch.float32, "router_bias")
+    M, H = x.shape
+    E = w_router.shape[0]
+    _ok(load_library().moe_router_logits(_p(x), _p(w_router), _p(router_bias), M, E, H, _p(logits),
+                                         _stream(stream)), "moe_router_logits")
+
+
+def moe_topk_softmax(logits, top_k: int, topk_ids, topk_weights, renormalize: bool = True,
+                     stream=None) -> None:
+    _check_dtype(logits, torch.bfloat16, "logits")
+    _check_dtype(topk_ids, torch.int32, "topk_ids")
+    _check_dtype(topk_weights, torch.float32, "topk_weights")
+    M, E = logits.shape
+    _ok(load_library().moe_topk_softmax(_p(logits), M, E, top_k, int(bool(renormalize)),
+                                        _p(topk_ids), _p(topk_weights), _stream(stream)),
+        "moe_topk_softmax")
+
+
+def moe_align_block_size(topk_ids, E: int, block_size_m: int, sorted_token_ids, expert_ids,
+                         expert_offsets, num_tokens_post_padded, ws, stream=None) -> None:
+    _check_dtype(topk_ids, torch.int32, "topk_ids")
+    M, top_k = topk_ids.shape
+    ptr, n = _ws(ws)
+    _ok(load_library().moe_align_block_size(_p(topk_ids), M, top_k, E, block_size_m,
+                                            _p(sorted_token_ids), _p(expert_ids),
+                                            _p(expert_offsets), _p(num_tokens_post_padded), ptr, n,
+                                            _stream(stream)), "moe_align_block_size")
+
+
+def moe_grouped_gemm_w13_act(x, w13, sorted_token_ids, expert_ids, num_tokens_post_padded,
+                             top_k: int, block_size_m: int, a, stream=None) -> None:
+    _check_dtype(x, torch.bfloat16, "x")
+    _check_dtype(w13, torch.bfloat16, "w13")
+    _check_dtype(a, torch.bfloat16, "a")
+    M, H = x.shape
+    E, twoI, _ = w13.shape
+    _ok(load_library().moe_grouped_gemm_w13_act(_p(x), _p(w13), _p(sorted_token_ids),
+                                                _p(expert_ids), _p(num_tokens_post_padded), M,
+                                                top_k, E, H, twoI // 2, block_size_m, _p(a),
+                                                _stream(stream)), "moe_grouped_gemm_w13_act")
+
+
+def moe_grouped_gemm_w2_combine(a, w2, sorted_token_ids, expert_ids, num_tokens_post_padded,
+                                topk_weights, top_k: int, block_size_m: int, y, ws,
+                                residual=None, stream=None) -> None:
+    _check_dtype(a, torch.bfloat16, "a")
+    _check_dtype(w2, torch.bfloat16, "w2")
+    _check_dtype(y, torch.bfloat16, "y")
+    _check_dtype(topk_weights, torch.float32, "topk_weights")
+    _check_dtype(residual, torch.bfloat16, "residual")
+    M, H = y.shape
+    E, _, I = w2.shape
+    ptr, n = _ws(ws)
+    _ok(load_library().moe_grouped_gemm_w2_combine(_p(a), _p(w2), _p(sorted_token_ids),
+                                                   _p(expert_ids), _p(num_tokens_post_padded),
+                                                   _p(topk_weights), _p(residual), M, top_k, E, H,
+                                                   I, block_size_m, _p(y), ptr, n, _stream(stream)),
+        "moe_grouped_gemm_w2_combine")
+
+
+def moe_forward(x, w13, w2, top_k: int, y, ws, *, w_router=None, router_logits=None,
+                router_bias=None, residual=None, renormalize: bool = True, block_size_m: int = 0,
+                topk_ids_out=None, topk_weights_out=None, stream=None) -> None:
+    for t, n in ((x, "x"), (w13, "w13"), (w2, "w2"), (y, "y"), (w_router, "w_router"),
+                 (router_logits, "router_logits"), (residual, "residual")):
+        _check_dtype(t, torch.bfloat16, n)
+    _check_dtype(router_bias, torch.float32, "router_bias")
+    _check_dtype(topk_ids_out, torch.int32, "topk_ids_out")
+    _check_dtype(topk_weights_out, torch.float32, "topk_weights_out")
+    M, H = x.shape
+    E, twoI, _ = w13.shape
+    ptr, n = _ws(ws)
+    _ok(load_library().moe_forward(_p(x), _p(w_router), _p(router_logits), _p(router_bias),
+                                   _p(w13), _p(w2), _p(residual), M, E, top_k, H, twoI // 2,
+                                   int(bool(renormalize)), block_size_m, _p(y), _p(topk_ids_out),
+                                   _p(topk_weights_out), ptr, n, _stream(stream)), "moe_forward")

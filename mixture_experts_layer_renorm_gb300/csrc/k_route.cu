@@ -1,0 +1,183 @@
+// k_route.cu -- S0 router logits (CUDA-core path) and S1 softmax / top-k /
+// renormalize.
+//
+// Page "Mixture of Experts in vLLM - From First Principles to fused_moe",
+// section "One token uses only 8 experts": the router is one linear layer
+// W_r [E, H]; softmax over the E scores; keep the top_k largest; rescale the
+// kept weights to sum to 1 (renormalize).
+#include "moe_internal.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kRouterTok = 8;        // tokens per CTA
+constexpr int kRouterWarps = 8;
+constexpr int kRouterExpPerCta = 16; // experts per CTA (2 per warp)
+constexpr int kRouterKChunk = 2048;  // x columns staged in shared memory at once
+
+// One CTA: kRouterTok tokens x kRouterExpPerCta experts.  x rows are staged in
+// shared memory chunk by chunk; each warp streams one router row with 16-byte
+// loads and accumulates all staged tokens against it in fp32.
+__global__ void __launch_bounds__(kRouterWarps * 32)
+k_router_logits(const uint16_t *__restrict__ x, const uint16_t *__restrict__ w_router,
+                const float *__restrict__ bias, int M, int E, int H, uint16_t *__restrict__ logits) {
+  __shared__ uint4 xs[kRouterTok * (kRouterKChunk / 8)];
+  const int t0 = blockIdx.x * kRouterTok;
+  const int nt = min(kRouterTok, M - t0);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e_begin = blockIdx.y * kRouterExpPerCta;
+  const int e_end = min(E, e_begin + kRouterExpPerCta);
+  constexpr int kPerWarp = kRouterExpPerCta / kRouterWarps;
+  float acc[kPerWarp][kRouterTok];
+#pragma unroll
+  for (int r = 0; r < kPerWarp; ++r)
+#pragma unroll
+    for (int j = 0; j < kRouterTok; ++j) acc[r][j] = 0.f;
+
+  for (int kc = 0; kc < H; kc += kRouterKChunk) {
+    const int kw = min(kRouterKChunk, H - kc);
+    const int vrow = kw / 8;
+    __syncthreads();
+    for (int v = threadIdx.x; v < kRouterTok * vrow; v += blockDim.x) {
+      const int r = v / vrow, c = v - r * vrow;
+      uint4 val = make_uint4(0, 0, 0, 0);
+      if (r < nt) val = *reinterpret_cast<const uint4 *>(x + (size_t)(t0 + r) * H + kc + c * 8);
+      xs[r * (kRouterKChunk / 8) + c] = val;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < kPerWarp; ++r) {
+      const int e = e_begin + warp + r * kRouterWarps;
+      if (e >= e_end) continue;
+      const uint16_t *wrow = w_router + (size_t)e * H + kc;
+      for (int c = lane; c < vrow; c += 32) {
+        float wf[8];
+        bf16x8_to_float(ld_stream_16(wrow + c * 8), wf);
+#pragma unroll
+        for (int j = 0; j < kRouterTok; ++j) {
+          float xf[8];
+          bf16x8_to_float(xs[j * (kRouterKChunk / 8) + c], xf);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc[r][j] = fmaf(xf[q], wf[q], acc[r][j]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < kPerWarp; ++r) {
+    const int e = e_begin + warp + r * kRouterWarps;
+    if (e >= e_end) continue;
+    float mine = 0.f;
+#pragma unroll
+    for (int j = 0; j < kRouterTok; ++j) {
+      float v = acc[r][j];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == j) mine = v;
+    }
+    if (lane < nt) {
+      if (bias != nullptr) mine += bias[e];
+      logits[(size_t)(t0 + lane) * E + e] = float_to_bf16_bits(mine);
+    }
+  }
+}
+
+// Order-preserving map of a bf16 pattern to 16 unsigned bits: larger value ->
+// larger key; -0 is folded onto +0 so that the two compare equal.
+__device__ __forceinline__ uint32_t bf16_order_key(uint16_t b) {
+  if (b == 0x8000u) b = 0;
+  return (b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u);
+}
+__device__ __forceinline__ uint16_t bf16_from_order_key(uint32_t k) {
+  return (k & 0x8000u) ? static_cast<uint16_t>(k & 0x7FFFu) : static_cast<uint16_t>(~k & 0xFFFFu);
+}
+
+// One warp per token.  Lane l holds logits l, l+32, ... as 32-bit keys
+// (order key << 16 | (0xFFFF - e)), so the largest key is the largest logit
+// and, among equal logits, the lowest expert id.  top_k rounds of a warp
+// max-reduction pick the slots in order; the winner's key is cleared.
+template <int VPL>
+__global__ void __launch_bounds__(256)
+k_topk_softmax(const uint16_t *__restrict__ logits, int M, int E, int top_k, int renormalize,
+               int32_t *__restrict__ topk_ids, float *__restrict__ topk_weights) {
+  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (t >= M) return;
+  const uint16_t *row = logits + (size_t)t * E;
+  uint32_t key[VPL];
+  float val[VPL];
+  float mx = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int e = lane + 32 * i;
+    key[i] = 0;
+    val[i] = -INFINITY;
+    if (e < E) {
+      const uint16_t b = row[e];
+      key[i] = (bf16_order_key(b) << 16) | (0xFFFFu - static_cast<uint32_t>(e));
+      val[i] = bf16_bits_to_float(b);
+      mx = fmaxf(mx, val[i]);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  float den = 0.f;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i)
+    if (lane + 32 * i < E) den += expf(val[i] - mx);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+
+  int my_id = 0;
+  float my_p = 0.f, kept = 0.f;
+  for (int j = 0; j < top_k; ++j) {
+    uint32_t best = 0;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) best = max(best, key[i]);
+    best = __reduce_max_sync(0xffffffffu, best);
+#pragma unroll
+    for (int i = 0; i < VPL; ++i)
+      if (key[i] == best) key[i] = 0;
+    const int e = static_cast<int>(0xFFFFu - (best & 0xFFFFu));
+    const float v = bf16_bits_to_float(bf16_from_order_key(best >> 16));
+    const float pj = expf(v - mx);
+    kept += pj;
+    if (lane == j) {
+      my_id = e;
+      my_p = pj;
+    }
+  }
+  if (lane < top_k) {
+    topk_ids[(size_t)t * top_k + lane] = my_id;
+    topk_weights[(size_t)t * top_k + lane] = renormalize ? my_p / kept : my_p / den;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_router_logits(const uint16_t *x, const uint16_t *w_router, const float *bias,
+                                 int M, int E, int H, uint16_t *logits, cudaStream_t s) {
+  dim3 grid((M + kRouterTok - 1) / kRouterTok, (E + kRouterExpPerCta - 1) / kRouterExpPerCta);
+  k_router_logits<<<grid, kRouterWarps * 32, 0, s>>>(x, w_router, bias, M, E, H, logits);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_topk_softmax(const uint16_t *logits, int M, int E, int top_k, int renormalize,
+                                int32_t *topk_ids, float *topk_weights, cudaStream_t s) {
+  const int threads = 256;
+  const int blocks = (M * 32 + threads - 1) / threads;
+#define MOE_TOPK_CASE(V)                                                                       \
+  k_topk_softmax<V><<<blocks, threads, 0, s>>>(logits, M, E, top_k, renormalize, topk_ids, \
+                                               topk_weights)
+  if (E <= 32) MOE_TOPK_CASE(1);
+  else if (E <= 64) MOE_TOPK_CASE(2);
+  else if (E <= 128) MOE_TOPK_CASE(4);
+  else if (E <= 256) MOE_TOPK_CASE(8);
+  else if (E <= 512) MOE_TOPK_CASE(16);
+  else MOE_TOPK_CASE(32);
+#undef MOE_TOPK_CASE
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,328 @@
+// moe_api.cu -- host side of the C ABI declared in include/moe_api.h:
+// argument checks, workspace layout, path choice and kernel launches.
+//
+// Nothing here allocates device memory or synchronises with the host (except
+// moe_get_device_status); every launch goes to the caller's stream, so the
+// calls can be captured in a CUDA graph.
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+
+#include "moe_api.h"
+#include "moe_internal.cuh"
+
+namespace {
+
+using moe::kMaxExperts;
+using moe::kMaxTopK;
+
+constexpr size_t kAlign = 256;
+constexpr int kMaxDim = 65536;
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool valid_block_size(int B) { return B >= 1 && B <= 256; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shapes shared by every entry point.
+moe_status_t check_shapes(int M, int E, int top_k, int H, int I) {
+  if (M < 0) return MOE_ERR_INVALID_ARG;
+  if (E < 1 || E > kMaxExperts) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (top_k < 1 || top_k > std::min(E, kMaxTopK)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (H < 16 || H > kMaxDim || H % 16 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (I < 16 || I > kMaxDim || I % 16 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (static_cast<long long>(M) * top_k >= (1LL << 31) - kMaxExperts * 256LL)
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  return MOE_OK;
+}
+
+long capacity(long P, int E, int B) {
+  const long cap = P + static_cast<long>(E) * (B - 1);
+  return (cap + B - 1) / B * B;
+}
+
+// Workspace regions, each 256-byte aligned.  The status word is always at
+// offset 0 so that moe_get_device_status can find it from the pointer alone.
+struct WsLayout {
+  size_t status, logits, ids, wts, sorted, eids, offsets, npost, hist, a, yacc, total;
+};
+
+WsLayout ws_layout(int M, int E, int top_k, int H, int I, int B) {
+  const long P = static_cast<long>(M) * top_k;
+  const long cap = capacity(P, E, B);
+  WsLayout w{};
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = round_up(o + bytes, kAlign);
+    return at;
+  };
+  w.status = take(moe::kStatusBytes);
+  w.logits = take(sizeof(uint16_t) * static_cast<size_t>(M) * E);
+  w.ids = take(sizeof(int32_t) * static_cast<size_t>(P));
+  w.wts = take(sizeof(float) * static_cast<size_t>(P));
+  w.sorted = take(sizeof(int32_t) * static_cast<size_t>(cap));
+  w.eids = take(sizeof(int32_t) * static_cast<size_t>(cap / B));
+  w.offsets = take(sizeof(int32_t) * static_cast<size_t>(E + 1));
+  w.npost = take(sizeof(int32_t));
+  w.hist = take(sizeof(int32_t) * static_cast<size_t>(moe::align_hist_entries(P, E)));
+  w.a = take(sizeof(uint16_t) * static_cast<size_t>(P) * I);
+  w.yacc = take(sizeof(float) * static_cast<size_t>(M) * H);
+  w.total = o;
+  return w;
+}
+
+template <typename T>
+T *at(void *ws, size_t off) {
+  return reinterpret_cast<T *>(static_cast<char *>(ws) + off);
+}
+
+moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// Which grouped-GEMM implementation runs for this shape.  The CUDA-core
+// weight-streaming kernels cover every shape.
+enum class GemmPath { kGemv };
+
+GemmPath pick_path(int M, int E, int top_k, int B) {
+  (void)M; (void)E; (void)top_k; (void)B;
+  return GemmPath::kGemv;
+}
+
+moe_status_t run_gemm1(const uint16_t *x, const uint16_t *w13, const int32_t *sorted,
+                       const int32_t *eids, const int32_t *npost, int M, int top_k, int E, int H,
+                       int I, int B, uint16_t *a, cudaStream_t s) {
+  const long P = static_cast<long>(M) * top_k;
+  const int cap = static_cast<int>(capacity(P, E, B));
+  switch (pick_path(M, E, top_k, B)) {
+    case GemmPath::kGemv:
+    default:
+      return cuda_status(moe::launch_gemv_w13_act(x, w13, sorted, eids, npost, static_cast<int>(P),
+                                                  top_k, E, H, I, B, cap, a, s));
+  }
+}
+
+moe_status_t run_gemm2(const uint16_t *a, const uint16_t *w2, const int32_t *sorted,
+                       const int32_t *eids, const int32_t *npost, const float *wts, int M,
+                       int top_k, int E, int H, int I, int B, float *yacc, cudaStream_t s) {
+  const long P = static_cast<long>(M) * top_k;
+  const int cap = static_cast<int>(capacity(P, E, B));
+  switch (pick_path(M, E, top_k, B)) {
+    case GemmPath::kGemv:
+    default:
+      return cuda_status(moe::launch_gemv_w2_combine(a, w2, sorted, eids, npost, wts,
+                                                     static_cast<int>(P), top_k, E, H, I, B, cap,
+                                                     yacc, s));
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *moe_status_string(moe_status_t st) {
+  switch (st) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "MOE_ERR_UNSUPPORTED_SHAPE";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "MOE_ERR_WORKSPACE_TOO_SMALL";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_DEVICE_BAD_EXPERT_ID: return "MOE_ERR_DEVICE_BAD_EXPERT_ID";
+    case MOE_ERR_DEVICE_TIMEOUT: return "MOE_ERR_DEVICE_TIMEOUT";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+int moe_pick_block_size(int M, int E, int top_k, int H, int I) {
+  (void)H; (void)I;
+  if (M <= 0 || E <= 0 || top_k <= 0) return 16;
+  const double mean = static_cast<double>(M) * top_k / E;  // mean pairs per expert
+  if (mean <= 24) return 16;
+  if (mean <= 48) return 32;
+  if (mean <= 96) return 64;
+  return 128;
+}
+
+long moe_align_capacity(int M, int top_k, int E, int block_size_m) {
+  if (M < 0 || E < 1 || E > kMaxExperts || top_k < 1 || top_k > std::min(E, kMaxTopK) ||
+      !valid_block_size(block_size_m))
+    return -1;
+  return capacity(static_cast<long>(M) * top_k, E, block_size_m);
+}
+
+size_t moe_workspace_size(int M_max, int E, int top_k, int H, int I, int block_size_m) {
+  if (check_shapes(M_max, E, top_k, H, I) != MOE_OK) return 0;
+  if (block_size_m != 0 && !valid_block_size(block_size_m)) return 0;
+  if (block_size_m != 0) return ws_layout(M_max, E, top_k, H, I, block_size_m).total;
+  size_t best = 0;
+  for (int B : {16, 32, 64, 128, 256}) best = std::max(best, ws_layout(M_max, E, top_k, H, I, B).total);
+  return best;
+}
+
+moe_status_t moe_router_logits(const moe_bf16_t *x, const moe_bf16_t *w_router,
+                               const float *router_bias, int M, int E, int H, moe_bf16_t *logits,
+                               cudaStream_t stream) {
+  if (M < 0 || E < 1 || E > kMaxExperts) return M < 0 ? MOE_ERR_INVALID_ARG : MOE_ERR_UNSUPPORTED_SHAPE;
+  if (H < 16 || H > kMaxDim || H % 16 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0) return MOE_OK;
+  if (!x || !w_router || !logits) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_router)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(moe::launch_router_logits(x, w_router, router_bias, M, E, H, logits, stream));
+}
+
+moe_status_t moe_topk_softmax(const moe_bf16_t *logits, int M, int E, int top_k, int renormalize,
+                              int32_t *topk_ids, float *topk_weights, cudaStream_t stream) {
+  if (M < 0) return MOE_ERR_INVALID_ARG;
+  if (E < 1 || E > kMaxExperts || top_k < 1 || top_k > std::min(E, kMaxTopK))
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0) return MOE_OK;
+  if (!logits || !topk_ids || !topk_weights) return MOE_ERR_INVALID_ARG;
+  return cuda_status(
+      moe::launch_topk_softmax(logits, M, E, top_k, renormalize, topk_ids, topk_weights, stream));
+}
+
+moe_status_t moe_align_block_size(const int32_t *topk_ids, int M, int top_k, int E,
+                                  int block_size_m, int32_t *sorted_token_ids, int32_t *expert_ids,
+                                  int32_t *expert_offsets, int32_t *num_tokens_post_padded,
+                                  void *ws, size_t ws_bytes, cudaStream_t stream) {
+  if (M < 0) return MOE_ERR_INVALID_ARG;
+  if (E < 1 || E > kMaxExperts || top_k < 1 || top_k > std::min(E, kMaxTopK) ||
+      !valid_block_size(block_size_m))
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (static_cast<long long>(M) * top_k >= (1LL << 31) - kMaxExperts * 256LL)
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  if ((M > 0 && !topk_ids) || !sorted_token_ids || !expert_ids || !expert_offsets ||
+      !num_tokens_post_padded || !ws)
+    return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return MOE_ERR_INVALID_ARG;
+  const long P = static_cast<long>(M) * top_k;
+  // the align needs only the status word and its histogram scratch
+  const size_t need = round_up(moe::kStatusBytes, kAlign) +
+                      sizeof(int32_t) * static_cast<size_t>(moe::align_hist_entries(P, E));
+  if (ws_bytes < need) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  int *status = at<int>(ws, 0);
+  int32_t *hist = at<int32_t>(ws, round_up(moe::kStatusBytes, kAlign));
+  const int cap = static_cast<int>(capacity(P, E, block_size_m));
+  return cuda_status(moe::launch_align(topk_ids, static_cast<int>(P), E, block_size_m, cap,
+                                       sorted_token_ids, expert_ids, expert_offsets,
+                                       num_tokens_post_padded, hist, status, stream));
+}
+
+moe_status_t moe_grouped_gemm_w13_act(const moe_bf16_t *x, const moe_bf16_t *w13,
+                                      const int32_t *sorted_token_ids, const int32_t *expert_ids,
+                                      const int32_t *num_tokens_post_padded, int M, int top_k,
+                                      int E, int H, int I, int block_size_m, moe_bf16_t *a,
+                                      cudaStream_t stream) {
+  moe_status_t st = check_shapes(M, E, top_k, H, I);
+  if (st != MOE_OK) return st;
+  if (!valid_block_size(block_size_m)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0) return MOE_OK;
+  if (!x || !w13 || !sorted_token_ids || !expert_ids || !num_tokens_post_padded || !a)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w13)) return MOE_ERR_INVALID_ARG;
+  return run_gemm1(x, w13, sorted_token_ids, expert_ids, num_tokens_post_padded, M, top_k, E, H, I,
+                   block_size_m, a, stream);
+}
+
+moe_status_t moe_grouped_gemm_w2_combine(const moe_bf16_t *a, const moe_bf16_t *w2,
+                                         const int32_t *sorted_token_ids,
+                                         const int32_t *expert_ids,
+                                         const int32_t *num_tokens_post_padded,
+                                         const float *topk_weights, const moe_bf16_t *residual,
+                                         int M, int top_k, int E, int H, int I, int block_size_m,
+                                         moe_bf16_t *y, void *ws, size_t ws_bytes,
+                                         cudaStream_t stream) {
+  moe_status_t st = check_shapes(M, E, top_k, H, I);
+  if (st != MOE_OK) return st;
+  if (!valid_block_size(block_size_m)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0) return MOE_OK;
+  if (!a || !w2 || !sorted_token_ids || !expert_ids || !num_tokens_post_padded || !topk_weights ||
+      !y || !ws)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(w2) || !aligned16(y) || (residual && !aligned16(residual)))
+    return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(M, E, top_k, H, I, block_size_m);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  float *yacc = at<float>(ws, L.yacc);
+  cudaError_t e = cudaMemsetAsync(yacc, 0, sizeof(float) * static_cast<size_t>(M) * H, stream);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  st = run_gemm2(a, w2, sorted_token_ids, expert_ids, num_tokens_post_padded, topk_weights, M,
+                 top_k, E, H, I, block_size_m, yacc, stream);
+  if (st != MOE_OK) return st;
+  return cuda_status(moe::launch_finalize(yacc, residual, M, H, y, stream));
+}
+
+moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *w_router,
+                         const moe_bf16_t *router_logits, const float *router_bias,
+                         const moe_bf16_t *w13, const moe_bf16_t *w2, const moe_bf16_t *residual,
+                         int M, int E, int top_k, int H, int I, int renormalize, int block_size_m,
+                         moe_bf16_t *y, int32_t *topk_ids_out, float *topk_weights_out, void *ws,
+                         size_t ws_bytes, cudaStream_t stream) {
+  moe_status_t st = check_shapes(M, E, top_k, H, I);
+  if (st != MOE_OK) return st;
+  if (block_size_m != 0 && !valid_block_size(block_size_m)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if ((w_router == nullptr) == (router_logits == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (router_bias && !w_router) return MOE_ERR_INVALID_ARG;
+  if (M == 0) return MOE_OK;
+  if (!x || !w13 || !w2 || !y || !ws) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w13) || !aligned16(w2) || !aligned16(y) ||
+      (residual && !aligned16(residual)) || (w_router && !aligned16(w_router)))
+    return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return MOE_ERR_INVALID_ARG;
+  const int B = block_size_m != 0 ? block_size_m : moe_pick_block_size(M, E, top_k, H, I);
+  const WsLayout L = ws_layout(M, E, top_k, H, I, B);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+
+  const long P = static_cast<long>(M) * top_k;
+  const int cap = static_cast<int>(capacity(P, E, B));
+  int *status = at<int>(ws, L.status);
+  const uint16_t *logits = router_logits;
+  if (w_router) {
+    uint16_t *lg = at<uint16_t>(ws, L.logits);
+    st = cuda_status(moe::launch_router_logits(x, w_router, router_bias, M, E, H, lg, stream));
+    if (st != MOE_OK) return st;
+    logits = lg;
+  }
+  int32_t *ids = topk_ids_out ? topk_ids_out : at<int32_t>(ws, L.ids);
+  float *wts = topk_weights_out ? topk_weights_out : at<float>(ws, L.wts);
+  st = cuda_status(moe::launch_topk_softmax(logits, M, E, top_k, renormalize, ids, wts, stream));
+  if (st != MOE_OK) return st;
+  int32_t *sorted = at<int32_t>(ws, L.sorted);
+  int32_t *eids = at<int32_t>(ws, L.eids);
+  int32_t *offs = at<int32_t>(ws, L.offsets);
+  int32_t *npost = at<int32_t>(ws, L.npost);
+  st = cuda_status(moe::launch_align(ids, static_cast<int>(P), E, B, cap, sorted, eids, offs, npost,
+                                     at<int32_t>(ws, L.hist), status, stream));
+  if (st != MOE_OK) return st;
+  uint16_t *a = at<uint16_t>(ws, L.a);
+  st = run_gemm1(x, w13, sorted, eids, npost, M, top_k, E, H, I, B, a, stream);
+  if (st != MOE_OK) return st;
+  float *yacc = at<float>(ws, L.yacc);
+  if (cudaMemsetAsync(yacc, 0, sizeof(float) * static_cast<size_t>(M) * H, stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  st = run_gemm2(a, w2, sorted, eids, npost, wts, M, top_k, E, H, I, B, yacc, stream);
+  if (st != MOE_OK) return st;
+  return cuda_status(moe::launch_finalize(yacc, residual, M, H, y, stream));
+}
+
+moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!ws || ws_bytes < static_cast<size_t>(moe::kStatusBytes)) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return MOE_ERR_INVALID_ARG;
+  return cuda_status(cudaMemsetAsync(ws, 0, ws_bytes, stream));
+}
+
+moe_status_t moe_get_device_status(void *ws, cudaStream_t stream) {
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  int host = 0;
+  if (cudaMemcpyAsync(&host, ws, sizeof(int), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
+  if (host != 0) {
+    if (cudaMemsetAsync(ws, 0, sizeof(int), stream) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  return static_cast<moe_status_t>(host);
+}
+
+}  // extern "C"

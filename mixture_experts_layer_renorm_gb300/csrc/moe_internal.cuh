@@ -1,0 +1,92 @@
+// moe_internal.cuh -- shared device helpers and the launch functions that
+// moe_api.cu calls.  Internal to the CUDA library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace moe {
+
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 32;
+constexpr int kStatusBytes = 256;  // the status word lives in the first 256 B of the workspace
+
+// Device status codes (same numbering as moe_status_t).
+constexpr int kStatusBadExpertId = 5;
+constexpr int kStatusTimeout = 6;
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// fp32 -> bf16 bits, round to nearest even (cvt.rn.bf16.f32).
+__device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+// Record the first problem a kernel meets; later ones keep the first code.
+__device__ __forceinline__ void report_status(int *status, int code) {
+  if (status != nullptr) atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+  uint32_t m;
+  asm volatile("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+// 8 bf16 in a uint4 -> 8 floats
+__device__ __forceinline__ void bf16x8_to_float(const uint4 &v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+// Streaming 16-byte load that skips L1 (weights are read once per use).
+__device__ __forceinline__ uint4 ld_stream_16(const void *p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// ----------------------------------------------------------------------------
+// Launch functions.  Each returns the cudaError_t of its launch(es).
+
+// S0: logits [M,E] = bf16(x [M,H] . w_router[E,H]^T + bias)
+cudaError_t launch_router_logits(const uint16_t *x, const uint16_t *w_router, const float *bias,
+                                 int M, int E, int H, uint16_t *logits, cudaStream_t s);
+
+// S1: warp-per-token softmax / top-k / renormalize
+cudaError_t launch_topk_softmax(const uint16_t *logits, int M, int E, int top_k, int renormalize,
+                                int32_t *topk_ids, float *topk_weights, cudaStream_t s);
+
+// S2: align.  hist: scratch int32 [align_hist_entries(P, E)] (may be null when
+// align_num_ctas(P) == 1).  status: device status word.
+int align_num_ctas(long P);
+long align_hist_entries(long P, int E);
+cudaError_t launch_align(const int32_t *topk_ids, int P, int E, int B, int cap,
+                         int32_t *sorted_ids, int32_t *expert_ids, int32_t *expert_offsets,
+                         int32_t *n_post, int32_t *hist, int *status, cudaStream_t s);
+
+// S3 / S4 on CUDA cores: weight-streaming grouped GEMV (decode-sized groups).
+cudaError_t launch_gemv_w13_act(const uint16_t *x, const uint16_t *w13, const int32_t *sorted_ids,
+                                const int32_t *expert_ids, const int32_t *n_post, int P, int top_k,
+                                int E, int H, int I, int B, int cap, uint16_t *a, cudaStream_t s);
+cudaError_t launch_gemv_w2_combine(const uint16_t *a, const uint16_t *w2, const int32_t *sorted_ids,
+                                   const int32_t *expert_ids, const int32_t *n_post,
+                                   const float *topk_weights, int P, int top_k, int E, int H, int I,
+                                   int B, int cap, float *y_acc, cudaStream_t s);
+
+// y = bf16(y_acc + residual)
+cudaError_t launch_finalize(const float *y_acc, const uint16_t *residual, int M, int H, uint16_t *y,
+                            cudaStream_t s);
+
+int num_sms();
+
+}  // namespace moe

@@ -1,0 +1,140 @@
+"""The C-ABI library loads, exports every symbol include/moe_api.h declares,
+and rejects bad arguments on the host before launching anything.
+
+No compute call is made here.  The argument-check cases run only where no
+GPU is visible: there an argument check that wrongly let a call through
+would end in a CUDA error code (no device), never in a kernel.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import mixture_experts_layer_renorm_gb300 as moe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_api.h")
+
+OK, INVALID, SHAPE, WS_SMALL = 0, 1, 2, 3
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mixture_experts_layer_renorm_gb300 import _build
+    _build.build()
+    return moe.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_bound_functions():
+    assert declared_functions() == sorted(moe.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code, name in moe.STATUS_NAMES.items():
+        assert moe.moe_status_string(code) == name
+    assert moe.moe_status_string(99) == "MOE_ERR_UNKNOWN"
+
+
+def test_sizes_and_capacity(lib):
+    assert moe.moe_align_capacity(3, 2, 4, 4) == 20           # 6 pairs + 4 experts * 3 = 18 -> 20
+    assert moe.moe_align_capacity(1, 8, 128, 16) == 1936       # 8 + 128*15 = 1928 -> 1936
+    assert moe.moe_align_capacity(16384, 8, 128, 128) == 147328
+    assert lib.moe_align_capacity(1, 8, 128, 0) == -1          # B must be explicit
+    assert lib.moe_align_capacity(1, 9, 8, 16) == -1           # top_k > E
+    n = moe.moe_workspace_size(64, 128, 8, 2048, 768, 16)
+    assert n >= 64 * 8 * 768 * 2 + 64 * 2048 * 4
+    assert moe.moe_workspace_size(64, 128, 8, 2048, 768, 0) >= n
+    assert lib.moe_workspace_size(64, 128, 8, 2047, 768, 16) == 0   # H not a multiple of 16
+    assert lib.moe_workspace_size(64, 2000, 8, 2048, 768, 16) == 0  # E > 1024
+    assert lib.moe_workspace_size(64, 128, 8, 2048, 768, 257) == 0  # block size > 256
+    for M in (1, 8, 64, 512, 4096, 16384):
+        assert moe.moe_pick_block_size(M, 128, 8, 2048, 768) in (16, 32, 64, 128, 256)
+
+
+needs_no_gpu = pytest.mark.skipif(torch.cuda.is_available(),
+                                  reason="host-only argument checks use fake device pointers")
+
+FAKE = ctypes.c_void_p(1 << 20)     # 16- and 256-byte aligned, never dereferenced
+FAKE_MIS = ctypes.c_void_p((1 << 20) + 8)
+NULL = None
+S = None  # default stream
+
+
+@needs_no_gpu
+def test_forward_argument_checks(lib):
+    f = lib.moe_forward
+    big = 1 << 40
+    args = dict(x=FAKE, wr=FAKE, lg=NULL, bias=NULL, w13=FAKE, w2=FAKE, res=NULL, M=4, E=8, k=2,
+                H=64, I=32, renorm=1, B=16, y=FAKE, ids=NULL, wts=NULL, ws=FAKE, wsb=big)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return f(a["x"], a["wr"], a["lg"], a["bias"], a["w13"], a["w2"], a["res"], a["M"], a["E"],
+                 a["k"], a["H"], a["I"], a["renorm"], a["B"], a["y"], a["ids"], a["wts"], a["ws"],
+                 a["wsb"], S)
+
+    assert call(M=0) == OK                      # M == 0 is a no-op
+    assert call(M=-1) == INVALID
+    assert call(E=0) == SHAPE
+    assert call(E=1025) == SHAPE
+    assert call(k=9) == SHAPE                   # top_k > E
+    assert call(k=0) == SHAPE
+    assert call(E=64, k=33) == SHAPE            # top_k > 32
+    assert call(H=60) == SHAPE                  # not a multiple of 16
+    assert call(I=8) == SHAPE
+    assert call(B=257) == SHAPE
+    assert call(B=-3) == SHAPE
+    assert call(lg=FAKE) == INVALID             # both router weights and logits
+    assert call(wr=NULL) == INVALID             # neither
+    assert call(wr=NULL, lg=FAKE, bias=FAKE) == INVALID  # a bias without router weights
+    assert call(x=NULL) == INVALID
+    assert call(w13=NULL) == INVALID
+    assert call(y=NULL) == INVALID
+    assert call(ws=NULL) == INVALID
+    assert call(x=FAKE_MIS) == INVALID          # misaligned matrix
+    assert call(ws=FAKE_MIS) == INVALID         # misaligned workspace
+    need = moe.moe_workspace_size(4, 8, 2, 64, 32, 16)
+    assert call(wsb=need - 1) == WS_SMALL
+
+
+@needs_no_gpu
+def test_step_argument_checks(lib):
+    assert lib.moe_topk_softmax(FAKE, 4, 8, 9, 1, FAKE, FAKE, S) == SHAPE
+    assert lib.moe_topk_softmax(FAKE, -1, 8, 2, 1, FAKE, FAKE, S) == INVALID
+    assert lib.moe_topk_softmax(NULL, 4, 8, 2, 1, FAKE, FAKE, S) == INVALID
+    assert lib.moe_topk_softmax(FAKE, 0, 8, 2, 1, FAKE, FAKE, S) == OK
+    assert lib.moe_router_logits(FAKE, FAKE, NULL, 4, 8, 63, FAKE, S) == SHAPE
+    assert lib.moe_router_logits(NULL, FAKE, NULL, 4, 8, 64, FAKE, S) == INVALID
+    assert lib.moe_align_block_size(FAKE, 4, 2, 8, 0, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 20, S) == SHAPE
+    assert lib.moe_align_block_size(FAKE, 4, 2, 8, 16, FAKE, FAKE, FAKE, FAKE, NULL, 1 << 20, S) == INVALID
+    assert lib.moe_align_block_size(FAKE, 4, 2, 8, 16, FAKE, FAKE, FAKE, FAKE, FAKE, 16, S) == WS_SMALL
+    assert lib.moe_grouped_gemm_w13_act(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2, 8, 64, 32, 0, FAKE, S) == SHAPE
+    assert lib.moe_grouped_gemm_w13_act(FAKE, NULL, FAKE, FAKE, FAKE, 4, 2, 8, 64, 32, 16, FAKE, S) == INVALID
+    assert lib.moe_grouped_gemm_w2_combine(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, NULL, 4, 2, 8, 64, 32,
+                                           16, FAKE, FAKE, 64, S) == WS_SMALL
+    assert lib.moe_grouped_gemm_w2_combine(FAKE, FAKE, FAKE, FAKE, FAKE, NULL, NULL, 4, 2, 8, 64, 32,
+                                           16, FAKE, FAKE, 1 << 30, S) == INVALID
+    assert lib.moe_workspace_init(NULL, 1024, S) == INVALID
+    assert lib.moe_workspace_init(FAKE_MIS, 1024, S) == INVALID
+    assert lib.moe_get_device_status(NULL, S) == INVALID
+
+
+def test_product_path_fails_loudly_without_the_library(monkeypatch, tmp_path):
+    from mixture_experts_layer_renorm_gb300 import _build
+    monkeypatch.setattr(_build, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(moe, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        moe.load_library()

@@ -1,0 +1,312 @@
+"""Parity of every C-ABI entry point against the CPU oracle, on the GPU.
+
+The CUDA path and the oracle get the same seeded inputs (module `synth`);
+nothing the CUDA path produces is fed to the oracle.  Routing outputs must
+match bit for bit; y (and the activation a) within the output tolerance
+(tests/_util.py); router weights within 1e-6.
+
+Where the two sides round a router logit differently (fp32 vs fp64 sums can
+land on either side of a bf16 rounding midpoint), the test checks that the
+exact value lies within the fp32 summation error bound of that midpoint, and
+then compares the layer outputs only on tokens whose routing agrees.
+"""
+import numpy as np
+import pytest
+import torch
+
+import mixture_experts_layer_renorm_gb300 as moe
+import oracle
+import synth
+from _util import (W_ABS, assert_close_bf16, bits, f64_of_bits, fp32_dot_error_bound,
+                   tensor_of_bits)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from mixture_experts_layer_renorm_gb300 import _build
+    _build.build()
+    moe.load_library()
+    oracle.build()
+    oracle.set_threads(max(1, len(__import__("os").sched_getaffinity(0))))
+
+
+def rand_bf16(shape, std, seed, device=DEV):
+    return synth.normal_bf16(shape, std, seed, device)
+
+
+def tie_heavy_logits(M, E, seed):
+    g = torch.Generator().manual_seed(seed)
+    levels = torch.tensor([-1.0, -0.0, 0.0, 0.25, 0.5, 0.5078125, 1.0])
+    return levels[torch.randint(0, len(levels), (M, E), generator=g)].to(torch.bfloat16)
+
+
+# ----------------------------------------------------------------------------- S0 router
+
+def check_logits(got_bits, x, wr, bias):
+    """Equal to the oracle, or both neighbours of a midpoint within fp32 error of the exact value."""
+    xb, wb = bits(x), bits(wr)
+    want = oracle.router_logits(xb, wb, None if bias is None else bias.cpu().numpy())
+    diff = got_bits != want
+    if not diff.any():
+        return 0
+    xf, wf = f64_of_bits(xb), f64_of_bits(wb)
+    exact = xf @ wf.T
+    if bias is not None:
+        exact = exact + bias.cpu().numpy().astype(np.float64)
+    bound = fp32_dot_error_bound(xf, wf) + 1e-30
+    mid = (f64_of_bits(got_bits) + f64_of_bits(want)) / 2
+    ulp_gap = np.abs(got_bits.astype(np.int32) - want.astype(np.int32))
+    assert (ulp_gap[diff] == 1).all(), "logits differ by more than one bf16 step"
+    assert (np.abs(exact - mid)[diff] <= bound[diff]).all(), "a logit differs without a rounding tie"
+    return int(diff.sum())
+
+
+@pytest.mark.parametrize("M,E,H,with_bias", [(3, 4, 128, False), (64, 128, 2048, False),
+                                             (37, 256, 2048, False), (200, 33, 160, True),
+                                             (1, 128, 2048, True), (515, 128, 2048, True)])
+def test_router_logits(M, E, H, with_bias):
+    x = rand_bf16((M, H), 1.0, 11 + M)
+    wr = rand_bf16((E, H), 0.02, 12 + E)
+    bias = synth.zipf_router_bias(E, 1.1).to(DEV) if with_bias else None
+    lg = torch.empty((M, E), dtype=torch.bfloat16, device=DEV)
+    moe.moe_router_logits(x, wr, lg, router_bias=bias)
+    torch.cuda.synchronize()
+    n = check_logits(bits(lg), x, wr, bias)
+    assert n <= max(2, 0.01 * M * E)
+
+
+# ----------------------------------------------------------------------------- S1 top-k
+
+@pytest.mark.parametrize("M,E,k", [(3, 4, 2), (64, 128, 8), (1000, 60, 4), (129, 256, 8),
+                                   (50, 1024, 32), (77, 33, 33), (40, 7, 1), (300, 128, 1)])
+@pytest.mark.parametrize("kind", ["normal", "ties"])
+@pytest.mark.parametrize("renorm", [True, False])
+def test_topk_softmax(M, E, k, kind, renorm):
+    lg = (rand_bf16((M, E), 1.0, 1000 + M + E, "cpu") if kind == "normal"
+          else tie_heavy_logits(M, E, 2000 + M + E))
+    ids = torch.empty((M, k), dtype=torch.int32, device=DEV)
+    w = torch.empty((M, k), dtype=torch.float32, device=DEV)
+    moe.moe_topk_softmax(lg.to(DEV), k, ids, w, renormalize=renorm)
+    torch.cuda.synchronize()
+    rid, rw = oracle.topk_softmax(bits(lg), k, renormalize=renorm)
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    assert np.abs(w.cpu().numpy().astype(np.float64) - rw).max() <= W_ABS
+
+
+# ----------------------------------------------------------------------------- S2 align
+
+def skewed_ids(M, E, k, seed, s=1.1):
+    """topk_ids with Zipf-skewed expert loads (some experts empty, some heavy)."""
+    g = torch.Generator().manual_seed(seed)
+    bias = synth.zipf_router_bias(E, s, seed=seed)
+    lg = (torch.randn((M, E), generator=g) + bias).to(torch.bfloat16)
+    return oracle.topk_softmax(bits(lg), k)[0]
+
+
+def run_align(ids_np, E, B):
+    M, k = ids_np.shape
+    cap = moe.moe_align_capacity(M, k, E, B)
+    sorted_ids = torch.full((cap,), -7, dtype=torch.int32, device=DEV)
+    eids = torch.full((cap // B,), -7, dtype=torch.int32, device=DEV)
+    offs = torch.empty((E + 1,), dtype=torch.int32, device=DEV)
+    npost = torch.empty((1,), dtype=torch.int32, device=DEV)
+    ws = moe.Workspace(M, E, k, 16, 16, B)
+    moe.moe_align_block_size(torch.from_numpy(ids_np).to(DEV), E, B, sorted_ids, eids, offs, npost, ws)
+    torch.cuda.synchronize()
+    return sorted_ids.cpu().numpy(), eids.cpu().numpy(), offs.cpu().numpy(), int(npost.item()), ws
+
+
+def assert_align_equal(ids_np, E, B):
+    s, e, o, n, ws = run_align(ids_np, E, B)
+    rs, re_, ro, rn = oracle.align_block_size(ids_np, E, B)
+    assert n == rn
+    assert np.array_equal(s[:n], rs[:n])
+    assert np.array_equal(e[: n // B], re_[: n // B])
+    assert np.array_equal(o, ro)
+    assert moe.moe_get_device_status(ws) == 0
+    return s, e, o, n
+
+
+@pytest.mark.parametrize("M,E,k,B", [(3, 4, 2, 4), (3, 4, 2, 16), (1, 128, 8, 16), (64, 128, 8, 16),
+                                     (128, 256, 8, 16), (64, 60, 4, 16), (512, 128, 8, 32),
+                                     (2047, 128, 8, 64), (4096, 128, 8, 128), (16384, 128, 8, 128),
+                                     (8192, 60, 4, 128), (100, 1024, 32, 256), (5000, 7, 3, 1),
+                                     (3000, 128, 8, 256), (2049, 1, 1, 64)])
+def test_align_block_size(M, E, k, B):
+    assert_align_equal(skewed_ids(M, E, k, seed=M * 31 + E), E, B)
+
+
+def test_align_pages_worked_example():
+    import json
+    import os
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "toy_align.json")))
+    ids = np.array(g["our_choice"]["topk_ids"], np.int32)
+    s, e, o, n = assert_align_equal(ids, 4, 4)
+    assert list(s[:4]) == g["printed_on_page"]["block0_sorted_token_ids"]
+    assert e[0] == g["printed_on_page"]["block0_expert"]
+
+
+def test_align_is_deterministic_and_all_on_one_expert():
+    ids = skewed_ids(16384, 128, 8, seed=5)
+    first = run_align(ids, 128, 128)[:4]
+    for _ in range(3):
+        again = run_align(ids, 128, 128)[:4]
+        assert all(np.array_equal(a, b) for a, b in zip(first[:3], again[:3])) and first[3] == again[3]
+    same = np.zeros((40000, 1), np.int32) + 3
+    assert_align_equal(same, 8, 64)
+
+
+def test_align_reports_a_bad_expert_id():
+    ids = skewed_ids(64, 16, 2, seed=9)
+    ids[5, 1] = 16
+    ids[7, 0] = -2
+    s, e, o, n, ws = run_align(ids, 16, 16)
+    assert moe.moe_get_device_status(ws) == 5       # MOE_ERR_DEVICE_BAD_EXPERT_ID
+    assert moe.moe_get_device_status(ws) == 0       # read clears it
+    body = s[:n]
+    real = body[body < ids.size]
+    assert sorted(real) == sorted(set(range(ids.size)) - {5 * 2 + 1, 7 * 2 + 0})
+
+
+# ----------------------------------------------------------------------------- S3 / S4
+
+def layer_case(M, E, k, H, I, seed, dev=DEV):
+    x = rand_bf16((M, H), 1.0, seed, dev)
+    w13 = rand_bf16((E, 2 * I, H), 0.02, seed + 1, dev)
+    w2 = rand_bf16((E, H, I), 0.02, seed + 2, dev)
+    lg = rand_bf16((M, E), 1.0, seed + 3, "cpu")
+    return x, w13, w2, lg
+
+
+def align_on_device(ids_np, E, B):
+    """The oracle's align lists as device tensors (oracle -> CUDA inputs only)."""
+    rs, re_, _, rn = oracle.align_block_size(ids_np, E, B)
+    return (torch.from_numpy(rs).to(DEV), torch.from_numpy(re_).to(DEV),
+            torch.tensor([rn], dtype=torch.int32, device=DEV))
+
+
+GEMM_SHAPES = [(3, 4, 2, 128, 64, 16), (64, 128, 8, 2048, 768, 16), (64, 60, 4, 2048, 1408, 16),
+               (33, 16, 3, 256, 160, 4), (200, 32, 4, 512, 96, 32), (128, 256, 8, 2048, 512, 16),
+               (512, 128, 8, 2048, 768, 32), (1, 128, 8, 2048, 768, 16)]
+
+
+@pytest.mark.parametrize("M,E,k,H,I,B", GEMM_SHAPES)
+def test_grouped_gemm_w13_act(M, E, k, H, I, B):
+    x, w13, w2, lg = layer_case(M, E, k, H, I, seed=M + E + H)
+    ids, _ = oracle.topk_softmax(bits(lg), k)
+    s, e, n = align_on_device(ids, E, B)
+    a = torch.full((M * k, I), float("nan"), dtype=torch.bfloat16, device=DEV)
+    moe.moe_grouped_gemm_w13_act(x, w13, s, e, n, k, B, a)
+    torch.cuda.synchronize()
+    ref = oracle.expert_act(bits(x), bits(w13), ids)
+    assert_close_bf16(bits(a), ref, "a")
+
+
+@pytest.mark.parametrize("M,E,k,H,I,B", GEMM_SHAPES)
+@pytest.mark.parametrize("with_residual", [False, True])
+def test_grouped_gemm_w2_combine(M, E, k, H, I, B, with_residual):
+    x, w13, w2, lg = layer_case(M, E, k, H, I, seed=2 * M + E + I)
+    ids, w = oracle.topk_softmax(bits(lg), k)
+    a_bits = oracle.expert_act(bits(x), bits(w13), ids)     # oracle activation as the input
+    res = rand_bf16((M, H), 1.0, 77) if with_residual else None
+    s, e, n = align_on_device(ids, E, B)
+    y = torch.empty((M, H), dtype=torch.bfloat16, device=DEV)
+    ws = moe.Workspace(M, E, k, H, I, B)
+    moe.moe_grouped_gemm_w2_combine(tensor_of_bits(a_bits, DEV), w2, s, e, n,
+                                    torch.from_numpy(w).to(DEV), k, B, y, ws, residual=res)
+    torch.cuda.synchronize()
+    ref = oracle.expert_down_combine(a_bits, bits(w2), ids, w, None if res is None else bits(res))
+    assert_close_bf16(bits(y), ref, "y")
+
+
+# ----------------------------------------------------------------------------- the layer
+
+def run_forward(x, w13, w2, k, *, lg=None, wr=None, bias=None, res=None, B=0, renorm=True):
+    M, H = x.shape
+    E, twoI, _ = w13.shape
+    y = torch.empty((M, H), dtype=torch.bfloat16, device=DEV)
+    ids = torch.empty((M, k), dtype=torch.int32, device=DEV)
+    wts = torch.empty((M, k), dtype=torch.float32, device=DEV)
+    ws = moe.Workspace(M, E, k, H, twoI // 2, B)
+    moe.moe_forward(x, w13, w2, k, y, ws, w_router=wr, router_logits=lg, router_bias=bias,
+                    residual=res, renormalize=renorm, block_size_m=B, topk_ids_out=ids,
+                    topk_weights_out=wts)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status(ws) == 0
+    return bits(y), ids.cpu().numpy(), wts.cpu().numpy()
+
+
+@pytest.mark.parametrize("M,E,k,H,I,B", [(3, 4, 2, 128, 64, 16), (1, 60, 4, 2048, 1408, 0),
+                                         (64, 60, 4, 2048, 1408, 0), (21, 9, 9, 64, 48, 0),
+                                         (50, 24, 5, 96, 32, 8), (300, 64, 6, 256, 128, 0)])
+@pytest.mark.parametrize("renorm", [True, False])
+def test_forward_given_logits(M, E, k, H, I, B, renorm):
+    x, w13, w2, lg = layer_case(M, E, k, H, I, seed=3 * M + E)
+    yb, ids, wts = run_forward(x, w13, w2, k, lg=lg.to(DEV), B=B, renorm=renorm)
+    ref = oracle.moe_forward(bits(x), bits(w13), bits(w2), k, router_logits=bits(lg), renormalize=renorm)
+    assert np.array_equal(ids, ref["topk_ids"])
+    assert np.abs(wts.astype(np.float64) - ref["topk_weights"]).max() <= W_ABS
+    assert_close_bf16(yb, ref["y"], "y")
+
+
+def compare_routed_layer(yb, ids, ref, x, wr, bias):
+    """y compared on tokens whose routing agrees; disagreeing tokens must have a
+    logit that the two sides round differently."""
+    agree = (ids == ref["topk_ids"]).all(axis=1)
+    if not agree.all():
+        lg = torch.empty((x.shape[0], wr.shape[0]), dtype=torch.bfloat16, device=DEV)
+        moe.moe_router_logits(x, wr, lg, router_bias=bias)
+        torch.cuda.synchronize()
+        lgb = bits(lg)
+        check_logits(lgb, x, wr, bias)
+        for t in np.nonzero(~agree)[0]:
+            assert (lgb[t] != ref["logits"][t]).any(), f"token {t}: routing differs, logits equal"
+        assert (~agree).sum() <= max(1, 0.02 * len(agree))
+    assert_close_bf16(yb[agree], ref["y"][agree], "y")
+
+
+@pytest.mark.parametrize("cfg,M", [(1, 3), (2, 1), (2, 8), (2, 32), (2, 64), (4, 16), (4, 128)])
+def test_forward_with_router_on_workloads(cfg, M):
+    w = synth.WORKLOADS[cfg]
+    wt = synth.layer_weights(w, device=DEV)
+    inp = synth.layer_input(w, M, device=DEV)
+    x = inp["x"]
+    res = x if w.residual else None
+    yb, ids, _ = run_forward(x, wt["w13"], wt["w2"], w.top_k, wr=wt["w_router"], res=res,
+                             B=w.block_size_m)
+    ref = oracle.moe_forward(bits(x), bits(wt["w13"]), bits(wt["w2"]), w.top_k,
+                             w_router=bits(wt["w_router"]),
+                             residual=None if res is None else bits(res))
+    compare_routed_layer(yb, ids, ref, x, wt["w_router"], None)
+
+
+@pytest.mark.parametrize("cfg,M", [(3, 512), (3, 4096), (3, 16384), (5, 8192), (5, 1)])
+def test_forward_full_size_sampled(cfg, M):
+    """The full workload on the GPU; the oracle recomputes a sample of tokens."""
+    w = synth.WORKLOADS[cfg]
+    wt = synth.layer_weights(w, device=DEV)
+    inp = synth.layer_input(w, M, device=DEV)
+    x = inp["x"]
+    lg = inp["router_logits"]
+    yb, ids, _ = run_forward(x, wt["w13"], wt["w2"], w.top_k, wr=wt["w_router"], lg=lg,
+                             bias=wt["router_bias"])
+    g = torch.Generator().manual_seed(M)
+    sample = torch.randperm(M, generator=g)[: min(M, 48)].sort().values.numpy()
+    ref = oracle.moe_forward(
+        bits(x)[sample], bits(wt["w13"]), bits(wt["w2"]), w.top_k,
+        w_router=None if wt["w_router"] is None else bits(wt["w_router"]),
+        router_logits=None if lg is None else bits(lg)[sample],
+        router_bias=None if wt["router_bias"] is None else wt["router_bias"].cpu().numpy())
+    if wt["w_router"] is None:
+        assert np.array_equal(ids[sample], ref["topk_ids"])
+        assert_close_bf16(yb[sample], ref["y"], "y")
+    else:
+        compare_routed_layer(yb[sample], ids[sample], ref, x[torch.from_numpy(sample).to(DEV)],
+                             wt["w_router"], wt["router_bias"])
+    # routing is complete: every token has top_k distinct experts
+    assert (np.sort(ids, axis=1)[:, 1:] != np.sort(ids, axis=1)[:, :-1]).all()

@@ -1,0 +1,478 @@
+#!/usr/bin/env python
+"""Throughput of the MoE layer forward on one GB300 (or N replicas).
+
+Default workload: the Qwen3-30B-A3B-shaped decode layer (E=128, top_k=8,
+H=2048, I=768, bf16) at M=64 tokens, seeded synthetic weights and inputs
+already resident in HBM.  A step is one pass of the whole layer (router
+logits, softmax/top-k/renormalize, align, grouped GEMM 1 + SiLU-and-mul,
+grouped GEMM 2 + weighted combine) over one batch, timed with CUDA events on
+the launching stream; the L2 is flushed (a 512 MB write) between steps,
+outside the events, and each step routes a different x.
+
+Printed (rank 0, one JSON line): tokens/s, the roofline of the dominant
+kernel (grouped GEMM 1, HBM-bound in decode) measured live with CUDA events,
+the end-to-end figure through moe_forward with host buffers (copies inside
+the timed region), the CPU oracle timed on a bounded sample, SM clocks
+sampled during the timed region, and the other decode batch sizes.
+
+`--impl reference` times the CPU oracle instead (the slow reference arm).
+Under torchrun every rank runs its own replica (no collective on the data
+path); the reported time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "MoE-layer tokens/s; % HBM roofline (decode), % bf16 TC peak (prefill)"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+WORKLOAD_CFG = {"toy": 1, "decode": 2, "prefill": 3, "stack": 4, "tail": 5}
+
+
+# ----------------------------------------------------------------------------- accounting
+
+def layer_bytes(w, M, D):
+    """Algorithmic bytes of one layer: the D touched experts' W13 and W2, the
+    router (or the given logits), x and y (and the residual), ids and weights."""
+    b = D * 3 * w.H * w.I * 2 + 2 * M * w.H * 2 + M * w.top_k * 8
+    b += M * w.E * 2 if w.logits_given else w.E * w.H * 2
+    if w.residual:
+        b += M * w.H * 2
+    return b
+
+
+def gemm1_bytes(w, M, D):
+    """Algorithmic bytes of grouped GEMM 1: each touched expert's W13 [2I, H]
+    once, the M input rows once, the M*top_k activation rows written once."""
+    return D * 2 * w.I * w.H * 2 + M * w.H * 2 + M * w.top_k * w.I * 2
+
+
+def layer_flops(w, M):
+    return M * w.top_k * 6 * w.H * w.I + (0 if w.logits_given else 2 * M * w.H * w.E)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS, source="fallback")
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        self.gpu = str(device.index or 0)
+        try:
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            self.gpu = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except (AttributeError, RuntimeError):
+            pass
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self._t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- ranks
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(value: float, world: int, device) -> float:
+    """Max of a per-rank float over all ranks (identity for one rank)."""
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- our arm
+
+class Layer:
+    """Device-resident weights, inputs and buffers of one workload point."""
+
+    def __init__(self, moe, w, M, n_inputs, device, layer=0):
+        self.w, self.M = w, M
+        wt = synth.layer_weights(w, layer=layer, device=device)
+        self.wr, self.bias, self.w13, self.w2 = wt["w_router"], wt["router_bias"], wt["w13"], wt["w2"]
+        self.inputs = [synth.layer_input(w, M, rep=r, device=device) for r in range(n_inputs)]
+        self.B = w.block_size_m or moe.moe_pick_block_size(M, w.E, w.top_k, w.H, w.I)
+        P = M * w.top_k
+        cap = moe.moe_align_capacity(M, w.top_k, w.E, self.B)
+        i32 = dict(dtype=torch.int32, device=device)
+        self.logits = torch.empty((M, w.E), dtype=torch.bfloat16, device=device)
+        self.ids = torch.empty((M, w.top_k), **i32)
+        self.wts = torch.empty((M, w.top_k), dtype=torch.float32, device=device)
+        self.sorted = torch.empty((cap,), **i32)
+        self.eids = torch.empty((cap // self.B,), **i32)
+        self.offs = torch.empty((w.E + 1,), **i32)
+        self.npost = torch.empty((1,), **i32)
+        self.a = torch.empty((P, w.I), dtype=torch.bfloat16, device=device)
+        self.y = torch.empty((M, w.H), dtype=torch.bfloat16, device=device)
+        self.ws = moe.Workspace(M, w.E, w.top_k, w.H, w.I, 0, device=device)
+
+    def kernels_per_step(self):
+        align = 1 if self.M * self.w.top_k <= 16384 else 2
+        router = 0 if self.w.logits_given else 1
+        return router + 1 + align + 1 + 2  # + topk, GEMM 1, GEMM 2 and the output pass
+
+    def step(self, moe, i, stream, ev):
+        """One pass of the layer through the step entry points; ev[0..5] bracket the steps."""
+        w, inp = self.w, self.inputs[i]
+        x = inp["x"]
+        ev[0].record(stream)
+        if w.logits_given:
+            logits = inp["router_logits"]
+        else:
+            moe.moe_router_logits(x, self.wr, self.logits, router_bias=self.bias, stream=stream)
+            logits = self.logits
+        ev[1].record(stream)
+        moe.moe_topk_softmax(logits, w.top_k, self.ids, self.wts, renormalize=w.renormalize,
+                             stream=stream)
+        ev[2].record(stream)
+        moe.moe_align_block_size(self.ids, w.E, self.B, self.sorted, self.eids, self.offs,
+                                 self.npost, self.ws, stream=stream)
+        ev[3].record(stream)
+        moe.moe_grouped_gemm_w13_act(x, self.w13, self.sorted, self.eids, self.npost, w.top_k,
+                                     self.B, self.a, stream=stream)
+        ev[4].record(stream)
+        moe.moe_grouped_gemm_w2_combine(self.a, self.w2, self.sorted, self.eids, self.npost,
+                                        self.wts, w.top_k, self.B, self.y, self.ws,
+                                        residual=x if w.residual else None, stream=stream)
+        ev[5].record(stream)
+
+    def distinct_experts(self, moe, i, stream):
+        inp = self.inputs[i]
+        logits = inp["router_logits"]
+        if logits is None:
+            moe.moe_router_logits(inp["x"], self.wr, self.logits, router_bias=self.bias, stream=stream)
+            logits = self.logits
+        moe.moe_topk_softmax(logits, self.w.top_k, self.ids, self.wts,
+                             renormalize=self.w.renormalize, stream=stream)
+        stream.synchronize()
+        return int(torch.unique(self.ids).numel())
+
+
+def run_point(moe, w, M, steps, warmup, device, stream, flush):
+    L = Layer(moe, w, M, warmup + steps, device)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(warmup + steps)]
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            flush.zero_()
+            L.step(moe, i, stream, evs[i])
+        stream.synchronize()
+        for i in range(warmup, warmup + steps):
+            flush.zero_()
+            L.step(moe, i, stream, evs[i])
+        stream.synchronize()
+    per = [[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(5)] for i in range(warmup, warmup + steps)]
+    step_ms = [evs[i][0].elapsed_time(evs[i][5]) for i in range(warmup, warmup + steps)]
+    D = [L.distinct_experts(moe, i, stream) for i in range(warmup, warmup + steps)]
+    return L, per, step_ms, D
+
+
+def e2e_point(moe, L, steps, warmup, device, stream, flush):
+    """Through moe_forward with pinned host buffers: H2D of x (and logits), the
+    layer, D2H of y, all inside the events of each step."""
+    w, M = L.w, L.M
+    hx = [inp["x"].cpu().pin_memory() for inp in L.inputs]
+    hl = [inp["router_logits"].cpu().pin_memory() if inp["router_logits"] is not None else None
+          for inp in L.inputs]
+    hy = torch.empty((M, w.H), dtype=torch.bfloat16).pin_memory()
+    dx = torch.empty((M, w.H), dtype=torch.bfloat16, device=device)
+    dl = torch.empty((M, w.E), dtype=torch.bfloat16, device=device) if w.logits_given else None
+    times = []
+    with torch.cuda.stream(stream):
+        for i in range(warmup + steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            dx.copy_(hx[i], non_blocking=True)
+            if dl is not None:
+                dl.copy_(hl[i], non_blocking=True)
+            moe.moe_forward(dx, L.w13, L.w2, w.top_k, L.y, L.ws, w_router=L.wr, router_logits=dl,
+                            router_bias=L.bias, residual=dx if w.residual else None,
+                            renormalize=w.renormalize, block_size_m=L.B, stream=stream)
+            hy.copy_(L.y, non_blocking=True)
+            e1.record(stream)
+            stream.synchronize()
+            if i >= warmup:
+                times.append(e0.elapsed_time(e1))
+    h2d = M * w.H * 2 + (M * w.E * 2 if w.logits_given else 0)
+    return times, h2d, M * w.H * 2
+
+
+def cpu_baseline(w, L, budget_s=12.0):
+    """The oracle, as it stands, on the host cores: repeated whole-batch layers
+    of this workload until about budget_s seconds have passed."""
+    import oracle
+    oracle.build()
+    cores = len(os.sched_getaffinity(0))
+    oracle.set_threads(cores)
+    inp = L.inputs[0]
+    M = L.M
+    sample_tokens = min(M, 64)
+    x = synth.bf16_bits(inp["x"])[:sample_tokens]
+    lg = None if inp["router_logits"] is None else synth.bf16_bits(inp["router_logits"])[:sample_tokens]
+    w13, w2 = synth.bf16_bits(L.w13), synth.bf16_bits(L.w2)
+    wr = None if L.wr is None else synth.bf16_bits(L.wr)
+    bias = None if L.bias is None else L.bias.cpu().numpy()
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        oracle.moe_forward(x, w13, w2, w.top_k, w_router=wr, router_logits=lg, router_bias=bias,
+                           residual=x if w.residual else None, renormalize=w.renormalize)
+        n += 1
+        if time.perf_counter() - t0 >= budget_s or n >= 50:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(n * sample_tokens / dt, 3), "unit": UNIT, "cores": oracle.get_threads(),
+            "kind": "oracle",
+            "sample": f"{n} x {w.name} layer on {sample_tokens} tokens (full expert weights), {dt:.1f} s"}
+
+
+def ours(args):
+    import mixture_experts_layer_renorm_gb300 as moe
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    moe.load_library(build_if_missing=True)
+    w = synth.WORKLOADS[WORKLOAD_CFG[args.workload]]
+    M = args.M or max(w.Ms)
+    peaks = load_peaks()
+    stream = torch.cuda.Stream(device=device)
+    flush = torch.empty(args.flush_mb << 20, dtype=torch.uint8, device=device)
+
+    # the timed region: K steps, barrier + synchronize on both sides
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(device) as clk:
+        L, per, step_ms, D = run_point(moe, w, M, args.steps, args.warmup, device, stream, flush)
+    torch.cuda.synchronize()
+    barrier(world)
+    local_total_ms = sum(step_ms)
+    total_ms = max_over_ranks(local_total_ms, world, device)
+    ms_per_step = total_ms / args.steps
+    value = world * M * args.steps / (total_ms / 1e3)
+
+    gemm1_ms = statistics.mean(p[3] for p in per)
+    D_mean = statistics.mean(D)
+    g1_bytes = statistics.mean(gemm1_bytes(w, M, d) for d in D)
+    achieved = g1_bytes / (gemm1_ms / 1e3) / 1e9
+    lay_bytes = statistics.mean(layer_bytes(w, M, d) for d in D)
+    lay_gbs = lay_bytes / (ms_per_step / 1e3) / 1e9
+    flops = layer_flops(w, M)
+    lay_tflops = flops / (ms_per_step / 1e3) / 1e12
+
+    e2e_times, h2d, d2h = e2e_point(moe, L, args.steps, args.warmup, device, stream, flush)
+    e2e_total = max_over_ranks(sum(e2e_times), world, device)
+    e2e_value = world * M * args.steps / (e2e_total / 1e3)
+
+    points = []
+    if not args.no_points and args.workload == "decode":
+        for m in w.Ms:
+            if m == M:
+                continue
+            _, p_per, p_ms, p_D = run_point(moe, w, m, max(5, args.steps // 2), args.warmup, device,
+                                            stream, flush)
+            ms = statistics.mean(p_ms)
+            bpl = statistics.mean(layer_bytes(w, m, d) for d in p_D)
+            points.append({"M": m, "tokens_per_s": round(m / (ms / 1e3), 1), "ms_per_layer": round(ms, 5),
+                           "hbm_frac_layer": round(bpl / (ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+                           "distinct_experts": round(statistics.mean(p_D), 2)})
+
+    if rank != 0:
+        return
+    cpu = None if (world > 1 or args.no_cpu_baseline) else cpu_baseline(w, L)
+    kernels = L.kernels_per_step()
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: seeded x ~ N(0,1), weights ~ N(0,0.02), bf16; new x every step",
+        "config": {"workload": f"{w.name}_m{M}", "M": M, "E": w.E, "top_k": w.top_k, "H": w.H,
+                   "I": w.I, "block_size_m": L.B, "renormalize": w.renormalize,
+                   "l2": f"flushed between steps ({args.flush_mb} MB write, outside the events)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"kernel": "grouped GEMM 1 + SiLU-and-mul", "bound": "hbm",
+                     "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                     "peak_source": peaks["source"],
+                     "algorithmic_bytes": int(g1_bytes), "ms": round(gemm1_ms, 5)},
+        "layer_roofline": {"achieved_gbs": round(lay_gbs, 1),
+                           "hbm_frac": round(lay_gbs / peaks["hbm_gbs"], 4),
+                           "achieved_tflops": round(lay_tflops, 3),
+                           "tc_frac": round(lay_tflops / peaks["bf16_tflops"], 5),
+                           "algorithmic_bytes": int(lay_bytes), "flops": int(flops),
+                           "distinct_experts": round(D_mean, 2)},
+        "step_breakdown_ms": {k: round(statistics.mean(p[j] for p in per), 5) for j, k in
+                              enumerate(["router", "topk", "align", "gemm1_act", "gemm2_combine"])},
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_total / args.steps, 5)},
+        "cpu_baseline": cpu,
+        "gpu_launches": kernels * args.steps,
+        "clocks": clk.summary(),
+        "points": points,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+def reference(args):
+    """The CPU oracle as the reference arm: each step is the layer on a bounded
+    sample of the workload's tokens, on this host's cores."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    oracle.build()
+    cores = len(os.sched_getaffinity(0))
+    oracle.set_threads(cores)
+    w = synth.WORKLOADS[WORKLOAD_CFG[args.workload]]
+    M = args.M or max(w.Ms)
+    sample = min(M, args.ref_tokens)
+    wt = synth.layer_weights(w, device="cuda" if torch.cuda.is_available() else "cpu")
+    w13, w2 = synth.bf16_bits(wt["w13"]), synth.bf16_bits(wt["w2"])
+    wr = None if wt["w_router"] is None else synth.bf16_bits(wt["w_router"])
+    bias = None if wt["router_bias"] is None else wt["router_bias"].cpu().numpy()
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    times = []
+    for i in range(args.warmup + args.steps):
+        inp = synth.layer_input(w, M, rep=i, device=dev)
+        x = synth.bf16_bits(inp["x"])[:sample]
+        lg = None if inp["router_logits"] is None else synth.bf16_bits(inp["router_logits"])[:sample]
+        t0 = time.perf_counter()
+        oracle.moe_forward(np.ascontiguousarray(x), w13, w2, w.top_k, w_router=wr,
+                           router_logits=lg, router_bias=bias,
+                           residual=x if w.residual else None, renormalize=w.renormalize)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+    total = sum(times)
+    value = sample * args.steps / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic: seeded x ~ N(0,1), weights ~ N(0,0.02), bf16",
+        "config": {"workload": f"{w.name}_m{M}", "M": M, "E": w.E, "top_k": w.top_k, "H": w.H,
+                   "I": w.I, "sampled_tokens_per_step": sample},
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": oracle.get_threads(),
+                         "kind": "oracle",
+                         "sample": f"{sample} of {M} tokens per step, full expert weights"},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOAD_CFG), default="decode")
+    ap.add_argument("--M", type=int, default=0, help="tokens per step (default: the largest of the workload)")
+    ap.add_argument("--flush-mb", type=int, default=512)
+    ap.add_argument("--no-points", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-tokens", type=int, default=64)
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        reference(args)
+    else:
+        ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -49,7 +49,3 @@ def fp32_dot_error_bound(x_f64, w_f64):
     product of two bf16 values is exact in fp32)."""
     K = x_f64.shape[1]
     return K * 2.0 ** -24 * (np.abs(x_f64) @ np.abs(w_f64).T)
-
-
-def bf16_neighbours_midpoint(a_bits, b_bits):
-    return (f64_of_bits(a_bits) + f64_of_bits(b_bits)) / 2

@@ -152,6 +152,31 @@ moe_status_t moe_grouped_gemm_w2_combine(const moe_bf16_t *a, const moe_bf16_t *
                                          moe_bf16_t *y, void *ws, size_t ws_bytes,
                                          cudaStream_t stream);
 
+/* moe_grouped_gemm_w2_combine for callers that cannot provide a workspace.
+ * The pages this library follows have no counterpart of this entry point.
+ * It serves callers that cannot allocate device memory: plugin code inside a
+ * host application that owns every device allocation and offers the plugin no
+ * allocator, and latency-critical code that may not call cudaMalloc (which can
+ * synchronise the device and takes unbounded time).  Same arguments and result
+ * as moe_grouped_gemm_w2_combine, without ws / ws_bytes.
+ * The fp32 accumulator is a fixed array of 2,097,152 floats (8 MiB) compiled
+ * into the library; every GPU that loads the library holds it until the
+ * process exits.  M * H above 2,097,152 returns MOE_ERR_UNSUPPORTED_SHAPE
+ * (nothing is launched).  No memory is allocated: the first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress) and keeps it, so
+ * make that first call on each device before capturing a stream.  All calls
+ * share the one array, which keeps the last call's contents (each call clears
+ * the part it uses first): calls that may overlap on the GPU (different
+ * streams, or different host threads) race on it and give wrong results. */
+moe_status_t moe_grouped_gemm_w2_combine_noalloc(const moe_bf16_t *a, const moe_bf16_t *w2,
+                                                 const int32_t *sorted_token_ids,
+                                                 const int32_t *expert_ids,
+                                                 const int32_t *num_tokens_post_padded,
+                                                 const float *topk_weights,
+                                                 const moe_bf16_t *residual, int M, int top_k,
+                                                 int E, int H, int I, int block_size_m,
+                                                 moe_bf16_t *y, cudaStream_t stream);
+
 /* The whole layer: S0 (skipped when router_logits is given) .. S4.
  * Exactly one of w_router [E, H] and router_logits [M, E] is non-NULL.
  * router_bias [E] fp32 or NULL (only with w_router); residual [M, H] or NULL.

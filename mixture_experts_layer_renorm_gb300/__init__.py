@@ -26,6 +26,7 @@ __all__ = [
     "moe_pick_block_size", "moe_workspace_init", "moe_router_logits", "moe_topk_softmax",
     "moe_align_block_size", "moe_grouped_gemm_w13_act", "moe_grouped_gemm_w2_combine",
     "moe_forward", "moe_get_device_status", "moe_status_string", "Workspace",
+    "moe_grouped_gemm_w2_combine_noalloc",
 ]
 
 STATUS_NAMES = {
@@ -39,7 +40,7 @@ EXPORTED = (
     "moe_workspace_size", "moe_align_capacity", "moe_pick_block_size", "moe_router_logits",
     "moe_topk_softmax", "moe_align_block_size", "moe_grouped_gemm_w13_act",
     "moe_grouped_gemm_w2_combine", "moe_forward", "moe_workspace_init", "moe_get_device_status",
-    "moe_status_string",
+    "moe_status_string", "moe_grouped_gemm_w2_combine_noalloc",
 )
 
 
@@ -78,6 +79,7 @@ def load_library(build_if_missing: bool = False):
         "moe_align_block_size": ([P, I, I, I, I, P, P, P, P, P, Z, P], I),
         "moe_grouped_gemm_w13_act": ([P, P, P, P, P, I, I, I, I, I, I, P, P], I),
         "moe_grouped_gemm_w2_combine": ([P, P, P, P, P, P, P, I, I, I, I, I, I, P, P, Z, P], I),
+        "moe_grouped_gemm_w2_combine_noalloc": ([P, P, P, P, P, P, P, I, I, I, I, I, I, P, P], I),
         "moe_forward": ([P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, P, P, Z, P], I),
         "moe_workspace_init": ([P, Z, P], I),
         "moe_get_device_status": ([P, P], I),
@@ -239,6 +241,26 @@ def moe_grouped_gemm_w2_combine(a, w2, sorted_token_ids, expert_ids, num_tokens_
                                                    _p(topk_weights), _p(residual), M, top_k, E, H,
                                                    I, block_size_m, _p(y), ptr, n, _stream(stream)),
         "moe_grouped_gemm_w2_combine")
+
+
+def moe_grouped_gemm_w2_combine_noalloc(a, w2, sorted_token_ids, expert_ids,
+                                        num_tokens_post_padded, topk_weights, top_k: int,
+                                        block_size_m: int, y, residual=None, stream=None) -> None:
+    """GEMM 2 + combine with the library's built-in accumulator (no workspace).
+
+    For callers that cannot allocate device memory.  M * H must not exceed
+    2,097,152; calls that overlap on the GPU share the accumulator and race."""
+    _check_dtype(a, torch.bfloat16, "a")
+    _check_dtype(w2, torch.bfloat16, "w2")
+    _check_dtype(y, torch.bfloat16, "y")
+    _check_dtype(topk_weights, torch.float32, "topk_weights")
+    _check_dtype(residual, torch.bfloat16, "residual")
+    M, H = y.shape
+    E, _, I = w2.shape
+    _ok(load_library().moe_grouped_gemm_w2_combine_noalloc(
+        _p(a), _p(w2), _p(sorted_token_ids), _p(expert_ids), _p(num_tokens_post_padded),
+        _p(topk_weights), _p(residual), M, top_k, E, H, I, block_size_m, _p(y), _stream(stream)),
+        "moe_grouped_gemm_w2_combine_noalloc")
 
 
 def moe_forward(x, w13, w2, top_k: int, y, ws, *, w_router=None, router_logits=None,

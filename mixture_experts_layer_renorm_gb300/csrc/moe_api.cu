@@ -7,6 +7,7 @@
 #include <algorithm>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "moe_api.h"
 #include "moe_internal.cuh"
@@ -326,3 +327,67 @@ moe_status_t moe_get_device_status(void *ws, cudaStream_t stream) {
 }
 
 }  // extern "C"
+
+// ----------------------------------------------------------------------------
+// GEMM 2 + combine without a caller workspace.
+//
+// Some callers cannot hand the library a workspace: plugin code running inside
+// a host application that owns every device allocation and gives the plugin no
+// allocator, or latency-critical code that may not call cudaMalloc (it can
+// synchronise the device and its latency is unbounded).  For them the fp32
+// accumulator of the combine lives in a fixed array compiled into this file.
+// Every GPU that loads the library holds the array until the process exits.
+
+namespace {
+
+constexpr long kNoAllocAccElems = 1L << 21;  // 8 MiB of fp32: M * H <= 2,097,152
+
+static __device__ __align__(256) float g_noalloc_acc[kNoAllocAccElems];
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+float *g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+// Device address of g_noalloc_acc on the current device, looked up once per
+// device.  In host code the array's name is only a host-side stand-in, so the
+// kernels must be given this address instead.
+moe_status_t noalloc_scratch(float **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_acc) != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
+    g_noalloc_ptr[dev] = static_cast<float *>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" moe_status_t moe_grouped_gemm_w2_combine_noalloc(
+    const moe_bf16_t *a, const moe_bf16_t *w2, const int32_t *sorted_token_ids,
+    const int32_t *expert_ids, const int32_t *num_tokens_post_padded, const float *topk_weights,
+    const moe_bf16_t *residual, int M, int top_k, int E, int H, int I, int block_size_m,
+    moe_bf16_t *y, cudaStream_t stream) {
+  moe_status_t st = check_shapes(M, E, top_k, H, I);
+  if (st != MOE_OK) return st;
+  if (!valid_block_size(block_size_m)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (static_cast<long>(M) * H > kNoAllocAccElems) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0) return MOE_OK;
+  if (!a || !w2 || !sorted_token_ids || !expert_ids || !num_tokens_post_padded || !topk_weights || !y)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(w2) || !aligned16(y) || (residual && !aligned16(residual)))
+    return MOE_ERR_INVALID_ARG;
+  float *acc = nullptr;
+  st = noalloc_scratch(&acc);
+  if (st != MOE_OK) return st;
+  // the array keeps the previous call's sums: clear the part this call uses
+  if (cudaMemsetAsync(acc, 0, sizeof(float) * static_cast<size_t>(M) * H, stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  st = run_gemm2(a, w2, sorted_token_ids, expert_ids, num_tokens_post_padded, topk_weights, M,
+                 top_k, E, H, I, block_size_m, acc, stream);
+  if (st != MOE_OK) return st;
+  return cuda_status(moe::launch_finalize(acc, residual, M, H, y, stream));
+}

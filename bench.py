@@ -66,6 +66,11 @@ def layer_flops(w, M):
     return M * w.top_k * 6 * w.H * w.I + (0 if w.logits_given else 2 * M * w.H * w.E)
 
 
+def gemm1_flops(w, M):
+    """GEMM 1 multiply-adds (2 flops each): every pair against the 2I rows of W13."""
+    return M * w.top_k * 2 * (2 * w.I) * w.H
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -343,18 +348,28 @@ def ours(args):
     gemm1_ms = statistics.mean(p[3] for p in per)
     D_mean = statistics.mean(D)
     g1_bytes = statistics.mean(gemm1_bytes(w, M, d) for d in D)
-    achieved = g1_bytes / (gemm1_ms / 1e3) / 1e9
+    g1_flops = gemm1_flops(w, M)
     lay_bytes = statistics.mean(layer_bytes(w, M, d) for d in D)
     lay_gbs = lay_bytes / (ms_per_step / 1e3) / 1e9
     flops = layer_flops(w, M)
     lay_tflops = flops / (ms_per_step / 1e3) / 1e12
+    # which roof binds GEMM 1: its arithmetic intensity against the ridge of the measured peaks
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if g1_flops / g1_bytes > ridge:
+        roof = {"bound": "tensor", "achieved": round(g1_flops / (gemm1_ms / 1e3) / 1e12, 2),
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "algorithmic_flops": int(g1_flops)}
+    else:
+        roof = {"bound": "hbm", "achieved": round(g1_bytes / (gemm1_ms / 1e3) / 1e9, 1),
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "algorithmic_bytes": int(g1_bytes)}
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
 
     e2e_times, h2d, d2h = e2e_point(moe, L, args.steps, args.warmup, device, stream, flush)
     e2e_total = max_over_ranks(sum(e2e_times), world, device)
     e2e_value = world * M * args.steps / (e2e_total / 1e3)
 
     points = []
-    if not args.no_points and args.workload == "decode":
+    if not args.no_points:
         for m in w.Ms:
             if m == M:
                 continue
@@ -364,6 +379,10 @@ def ours(args):
             bpl = statistics.mean(layer_bytes(w, m, d) for d in p_D)
             points.append({"M": m, "tokens_per_s": round(m / (ms / 1e3), 1), "ms_per_layer": round(ms, 5),
                            "hbm_frac_layer": round(bpl / (ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+                           "tc_frac_layer": round(layer_flops(w, m) / (ms / 1e3) / 1e12
+                                                  / peaks["bf16_tflops"], 4),
+                           "gemm1_ms": round(statistics.mean(p[3] for p in p_per), 5),
+                           "gemm2_ms": round(statistics.mean(p[4] for p in p_per), 5),
                            "distinct_experts": round(statistics.mean(p_D), 2)})
 
     if rank != 0:
@@ -379,11 +398,8 @@ def ours(args):
                    "I": w.I, "block_size_m": L.B, "renormalize": w.renormalize,
                    "l2": f"flushed between steps ({args.flush_mb} MB write, outside the events)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "roofline": {"kernel": "grouped GEMM 1 + SiLU-and-mul", "bound": "hbm",
-                     "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
-                     "peak_source": peaks["source"],
-                     "algorithmic_bytes": int(g1_bytes), "ms": round(gemm1_ms, 5)},
+        "roofline": dict({"kernel": "grouped GEMM 1 + SiLU-and-mul"}, **roof,
+                         traffic=None, peak_source=peaks["source"], ms=round(gemm1_ms, 5)),
         "layer_roofline": {"achieved_gbs": round(lay_gbs, 1),
                            "hbm_frac": round(lay_gbs / peaks["hbm_gbs"], 4),
                            "achieved_tflops": round(lay_tflops, 3),

@@ -1,0 +1,496 @@
+// k_gemm_tc.cu -- S3 / S4 on the 5th-generation tensor cores (tcgen05): the
+// grouped GEMMs of the layer with their fused epilogues.
+//
+// Page "Mixture of Experts in vLLM - From First Principles to fused_moe",
+// sections "Each expert is now an ordinary GEMM", "One GEMM 1 program, step
+// by step" and "The rest of the layer stays in pair order": every block of
+// B = block_size_m entries of sorted_token_ids belongs to one expert; its
+// rows are read in place through the pair id (GEMM 1: row p / top_k of x;
+// GEMM 2: row p of the activation) and its results go straight to the pair's
+// or token's final place.
+//
+// One CTA computes one block against a tile of weight rows, with the operands
+// swapped so that the weight rows fill the MMA's M = 128 dimension and the
+// block's B gathered rows are its N dimension (N = B in {16, ..., 256}):
+//
+//   GEMM 1: D_gate[128, B] = W13_e[i0 .. i0+127, :] . X_b^T
+//           D_up  [128, B] = W13_e[I+i0 .. I+i0+127, :] . X_b^T
+//           epilogue: a[p, i] = bf16(SiLU(bf16(gate)) * bf16(up)) -- the gate
+//           row and its up row share a TMEM lane, so one thread forms a.
+//   GEMM 2: D_0/1 [128, B] = W2_e[n0 .. n0+255, :] . A_b^T
+//           epilogue: y_acc[t, n] += topk_weight[p] * D (fp32 red.add)
+//
+// Warp roles (192 threads): warp 0 loads -- one lane issues the TMA copies
+// of the two 128 x 64 weight tiles (128-byte swizzle), all lanes gather the
+// block's rows with 16-byte cp.async into the same swizzled K-major layout;
+// warp 1 allocates TMEM and one lane issues tcgen05.mma (accumulators in
+// TMEM, 2 x B fp32 columns); warps 2-5 are the epilogue, one TMEM lane
+// quarter each (tcgen05.ld 32x32b).  A ring of shared-memory stages with
+// full/empty mbarriers connects the roles.  Every wait is bounded: after 2 s
+// the kernel records MOE_ERR_DEVICE_TIMEOUT in the status word, drains its
+// own copies and returns; it never traps.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kTcThreads = 192;
+constexpr int kBK = 64;                              // K per stage: one 128-byte swizzle row
+constexpr int kTileM = 128;                          // weight rows per MMA
+constexpr uint32_t kATileBytes = kTileM * kBK * 2;   // 16 KB
+constexpr int kSmemBudget = 220 * 1024;
+constexpr int kMaxStages = 6;
+constexpr int kCpAsyncLag = 1;                       // stages a row gather may trail its TMA
+constexpr uint64_t kWaitLimitNs = 2000000000ull;     // 2 s
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---------------------------------------------------------------- mbarrier
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for phase `parity` of the barrier; gives up after kWaitLimitNs (or
+// when another role already gave up), recording the timeout.
+__device__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort, int *status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort = 1;
+      report_status(status, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- copies
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                            int c2, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// Makes this thread's completed generic-proxy writes to shared memory visible
+// to the async proxy (the tensor core reads operands through it).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- tcgen05
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] . B[smem]^T, bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrives once on the barrier when every MMA this thread issued has completed.
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes, 8-row core groups 1024 bytes apart (stride byte offset).
+__device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
+  uint64_t d = static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(1) << 16;            // leading byte offset (unused with this swizzle)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;    // stride byte offset
+  d |= static_cast<uint64_t>(1) << 46;            // descriptor version (tcgen05)
+  d |= static_cast<uint64_t>(2) << 61;            // layout: 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor of kind::f16: bf16 A and B (K-major), fp32 D, M x N.
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+template <int N>
+struct TcConfig {
+  static constexpr uint32_t kBStageBytes = N * kBK * 2;
+  static constexpr uint32_t kStageBytes = 2 * kATileBytes + kBStageBytes;
+  static constexpr int kStages =
+      (kSmemBudget / static_cast<int>(kStageBytes)) < kMaxStages ? kSmemBudget / static_cast<int>(kStageBytes)
+                                                                 : kMaxStages;
+  static constexpr uint32_t kTmemCols = (2 * N <= 32) ? 32 : (2 * N <= 64) ? 64 : (2 * N <= 128) ? 128
+                                        : (2 * N <= 256) ? 256 : 512;
+  // barriers: full[S], empty[S], tmem_full; then tmem address, abort flag, rows, pairs
+  static constexpr uint32_t kCtlBytes = 8 * (2 * kStages + 1) + 16 + 8 * N;
+  static constexpr uint32_t kSmemBytes = 1024 + kStages * kStageBytes + kCtlBytes;
+  static_assert(kStages >= 3, "pipeline needs at least three stages");
+};
+
+// MODE 0: GEMM 1 + SiLU-and-mul; MODE 1: GEMM 2 + weighted combine.
+template <int N, int MODE>
+__global__ void __launch_bounds__(kTcThreads, 1)
+k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict__ src,
+          const int32_t *__restrict__ sorted_ids, const int32_t *__restrict__ expert_ids,
+          const int32_t *__restrict__ n_post_ptr, const float *__restrict__ topk_w, int P,
+          int top_k, int E, int K, int R_out, int B, int cap, uint16_t *__restrict__ a_out,
+          float *__restrict__ y_acc, int H_out, int *status) {
+  using Cfg = TcConfig<N>;
+  constexpr int S = Cfg::kStages;
+  const int b = blockIdx.x;
+  const int tile = blockIdx.y;
+  const int n_post = min(max(*n_post_ptr, 0), cap);
+  if (b >= n_post / B) return;
+  const int e = expert_ids[b];
+  if (e < 0 || e >= E) return;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t *a_tiles = smem;                                   // [S][2][16 KB]
+  uint8_t *b_tiles = smem + S * 2 * kATileBytes;             // [S][N * 128 B]
+  uint64_t *bars = reinterpret_cast<uint64_t *>(b_tiles + S * Cfg::kBStageBytes);
+  uint64_t *full = bars;
+  uint64_t *empty = bars + S;
+  uint64_t *tmem_full = bars + 2 * S;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 1);
+  volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  int *rows = reinterpret_cast<int *>(tmem_slot + 4);
+  int *pairs = rows + N;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&full[s]), 1 + 32);  // the TMA lane's expect_tx + 32 gather lanes
+      mbar_init(smem_u32(&empty[s]), 1);      // one tcgen05.commit
+    }
+    mbar_init(smem_u32(tmem_full), 1);
+    *abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  for (int j = threadIdx.x; j < N; j += blockDim.x) {
+    int p = -1;
+    if (j < B) {
+      const int v = sorted_ids[(size_t)b * B + j];
+      if (v >= 0 && v < P) p = v;
+    }
+    pairs[j] = p;
+    rows[j] = p < 0 ? -1 : (MODE == 0 ? p / top_k : p);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int nk = (K + kBK - 1) / kBK;
+  // weight rows of the two MMA tiles
+  const int row0 = MODE == 0 ? tile * kTileM : tile * 2 * kTileM;
+  const int row1 = MODE == 0 ? R_out + tile * kTileM : tile * 2 * kTileM + kTileM;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ loads
+    int kb = 0;
+    for (; kb < nk; ++kb) {
+      const int s = kb % S;
+      const uint32_t ph = (kb / S) & 1;
+      if (!wait_bounded(smem_u32(&empty[s]), ph ^ 1, abort, status)) break;
+      const uint32_t a_s = smem_u32(a_tiles + s * 2 * kATileBytes);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(smem_u32(&full[s]), 2 * kATileBytes);
+        tma_load_3d(a_s, &tmap_w, kb * kBK, row0, e, smem_u32(&full[s]));
+        tma_load_3d(a_s + kATileBytes, &tmap_w, kb * kBK, row1, e, smem_u32(&full[s]));
+      }
+      const uint32_t b_s = smem_u32(b_tiles + s * Cfg::kBStageBytes);
+      for (int idx = lane; idx < N * 8; idx += 32) {
+        const int r = idx >> 3, ch = idx & 7;
+        const int row = rows[r];
+        const int kel = kb * kBK + ch * 8;
+        const bool ok = row >= 0 && kel < K;
+        const uint16_t *gp = ok ? src + (size_t)row * K + kel : src;
+        const uint32_t dst = b_s + (r >> 3) * 1024 + (r & 7) * 128 + ((ch ^ (r & 7)) << 4);
+        cp_async_16(dst, gp, ok ? 16u : 0u);
+      }
+      cp_async_commit();
+      if (kb >= kCpAsyncLag) {
+        cp_async_wait<kCpAsyncLag>();
+        fence_proxy_async_smem();
+        mbar_arrive(smem_u32(&full[(kb - kCpAsyncLag) % S]));
+      }
+    }
+    // the last gathers (and, after an abort, every gather still in flight)
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    for (int k2 = (kb > kCpAsyncLag ? kb - kCpAsyncLag : 0); k2 < kb; ++k2)
+      mbar_arrive(smem_u32(&full[k2 % S]));
+    // after an abort: let the weight copies already issued land before exit
+    if (*abort && lane == 0) {
+      for (int k2 = (kb > S ? kb - S : 0); k2 < kb; ++k2) {
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(smem_u32(&full[k2 % S]), (k2 / S) & 1) &&
+               globaltimer_ns() - t0 < kWaitLimitNs) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA
+    if (lane == 0) {
+      constexpr uint32_t idesc = umma_idesc_bf16(kTileM, N);
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % S;
+        const uint32_t ph = (kb / S) & 1;
+        if (!wait_bounded(smem_u32(&full[s]), ph, abort, status)) break;
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(a_tiles + s * 2 * kATileBytes);
+        const uint32_t a1 = a0 + kATileBytes;
+        const uint32_t bt = smem_u32(b_tiles + s * Cfg::kBStageBytes);
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk) {
+          const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+          const uint64_t bd = sw128_kmajor_desc(bt + kk * 32);
+          umma_bf16(tmem, sw128_kmajor_desc(a0 + kk * 32), bd, idesc, acc);
+          umma_bf16(tmem + N, sw128_kmajor_desc(a1 + kk * 32), bd, idesc, acc);
+        }
+        umma_commit(smem_u32(&empty[s]));
+      }
+      umma_commit(smem_u32(tmem_full));
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    bool ok = wait_bounded(smem_u32(tmem_full), 0, abort, status);
+    tc_fence_after();
+    ok = __all_sync(0xffffffffu, ok && !*abort);  // tcgen05.ld needs the whole warp
+    if (ok) {
+      const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+      if (MODE == 0) {
+        const int i = tile * kTileM + q * 32 + lane;
+        const bool valid = i < R_out;
+#pragma unroll 1
+        for (int j0 = 0; j0 < N; j0 += 16) {
+          uint32_t g[16], u[16];
+          tmem_ld_32x32b_x16(tmem + lane_base + j0, g);
+          tmem_ld_32x32b_x16(tmem + lane_base + N + j0, u);
+          tmem_ld_wait();
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            const int p = pairs[j0 + jj];
+            if (valid && p >= 0) {
+              const float gb = bf16_bits_to_float(float_to_bf16_bits(__uint_as_float(g[jj])));
+              const float ub = bf16_bits_to_float(float_to_bf16_bits(__uint_as_float(u[jj])));
+              const float silu = gb / (1.0f + expf(-gb));
+              a_out[(size_t)p * R_out + i] = float_to_bf16_bits(silu * ub);
+            }
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int t = 0; t < 2; ++t) {
+          const int n = tile * 2 * kTileM + t * kTileM + q * 32 + lane;
+          const bool valid = n < H_out;
+#pragma unroll 1
+          for (int j0 = 0; j0 < N; j0 += 16) {
+            uint32_t o[16];
+            tmem_ld_32x32b_x16(tmem + lane_base + t * N + j0, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+              const int p = pairs[j0 + jj];
+              if (valid && p >= 0)
+                atomicAdd(y_acc + (size_t)(p / top_k) * H_out + n, topk_w[p] * __uint_as_float(o[jj]));
+            }
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, Cfg::kTmemCols);
+}
+
+// ---------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void *p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 3-D map over weights [E][rows][K] (bf16, K contiguous), box 64 x 128 x 1,
+// 128-byte swizzle; out-of-range rows and columns read as zero.
+cudaError_t make_weight_map(CUtensorMap *map, const uint16_t *w, int K, int rows, int E) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode_fn();
+  if (encode == nullptr) return cudaErrorNotSupported;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(E)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2,
+                                 static_cast<cuuint64_t>(K) * 2 * rows};
+  const cuuint32_t box[3] = {kBK, kTileM, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t *>(w),
+                            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int N, int MODE>
+cudaError_t launch_tc_n(const CUtensorMap &map, const uint16_t *src, const int32_t *sorted_ids,
+                        const int32_t *expert_ids, const int32_t *n_post, const float *topk_w, int P,
+                        int top_k, int E, int K, int R_out, int B, int cap, uint16_t *a_out,
+                        float *y_acc, int H_out, int *status, int tiles, cudaStream_t s) {
+  using Cfg = TcConfig<N>;
+  auto kern = k_gemm_tc<N, MODE>;
+  cudaError_t err = cudaFuncSetAttribute(reinterpret_cast<const void *>(kern),
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(Cfg::kSmemBytes));
+  if (err != cudaSuccess) return err;
+  const dim3 grid(cap / B, tiles);
+  kern<<<grid, kTcThreads, Cfg::kSmemBytes, s>>>(map, src, sorted_ids, expert_ids, n_post, topk_w, P,
+                                                 top_k, E, K, R_out, B, cap, a_out, y_acc, H_out,
+                                                 status);
+  return cudaGetLastError();
+}
+
+template <int MODE>
+cudaError_t launch_tc(const CUtensorMap &map, const uint16_t *src, const int32_t *sorted_ids,
+                      const int32_t *expert_ids, const int32_t *n_post, const float *topk_w, int P,
+                      int top_k, int E, int K, int R_out, int B, int cap, uint16_t *a_out,
+                      float *y_acc, int H_out, int *status, int tiles, cudaStream_t s) {
+#define MOE_TC_CASE(NN)                                                                         \
+  case NN:                                                                                      \
+    return launch_tc_n<NN, MODE>(map, src, sorted_ids, expert_ids, n_post, topk_w, P, top_k, E, \
+                                 K, R_out, B, cap, a_out, y_acc, H_out, status, tiles, s)
+  switch (B) {
+    MOE_TC_CASE(16);
+    MOE_TC_CASE(32);
+    MOE_TC_CASE(64);
+    MOE_TC_CASE(128);
+    MOE_TC_CASE(256);
+    default:
+      return cudaErrorInvalidValue;
+  }
+#undef MOE_TC_CASE
+}
+
+}  // namespace
+
+bool tc_supports_block(int B) { return B == 16 || B == 32 || B == 64 || B == 128 || B == 256; }
+
+cudaError_t launch_tc_w13_act(const uint16_t *x, const uint16_t *w13, const int32_t *sorted_ids,
+                              const int32_t *expert_ids, const int32_t *n_post, int P, int top_k,
+                              int E, int H, int I, int B, int cap, uint16_t *a, int *status,
+                              cudaStream_t s) {
+  CUtensorMap map;
+  cudaError_t err = make_weight_map(&map, w13, H, 2 * I, E);
+  if (err != cudaSuccess) return err;
+  const int tiles = (I + kTileM - 1) / kTileM;
+  return launch_tc<0>(map, x, sorted_ids, expert_ids, n_post, nullptr, P, top_k, E, H, I, B, cap,
+                      a, nullptr, 0, status, tiles, s);
+}
+
+cudaError_t launch_tc_w2_combine(const uint16_t *a, const uint16_t *w2, const int32_t *sorted_ids,
+                                 const int32_t *expert_ids, const int32_t *n_post,
+                                 const float *topk_weights, int P, int top_k, int E, int H, int I,
+                                 int B, int cap, float *y_acc, int *status, cudaStream_t s) {
+  CUtensorMap map;
+  cudaError_t err = make_weight_map(&map, w2, I, H, E);
+  if (err != cudaSuccess) return err;
+  const int tiles = (H + 2 * kTileM - 1) / (2 * kTileM);
+  return launch_tc<1>(map, a, sorted_ids, expert_ids, n_post, topk_weights, P, top_k, E, I, H, B,
+                      cap, nullptr, y_acc, H, status, tiles, s);
+}
+
+}  // namespace moe

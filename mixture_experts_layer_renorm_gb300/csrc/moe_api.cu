@@ -6,6 +6,7 @@
 // calls can be captured in a CUDA graph.
 #include <algorithm>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -81,21 +82,53 @@ T *at(void *ws, size_t off) {
 
 moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
-// Which grouped-GEMM implementation runs for this shape.  The CUDA-core
-// weight-streaming kernels cover every shape.
-enum class GemmPath { kGemv };
+// Which grouped-GEMM implementation runs: the tcgen05 kernels for block sizes
+// they tile (16, 32, 64, 128, 256), the CUDA-core weight-streaming kernels for
+// any other block size.  MOE_FORCE_PATH=gemv|tc overrides the choice (for
+// measurements); "tc" falls back to gemv where the block size is not tiled.
+enum class GemmPath { kGemv, kTensorCore };
+
+int forced_path() {
+  const char *v = std::getenv("MOE_FORCE_PATH");
+  if (v == nullptr) return 0;
+  if (std::strcmp(v, "gemv") == 0) return 1;
+  if (std::strcmp(v, "tc") == 0) return 2;
+  return 0;
+}
 
 GemmPath pick_path(int M, int E, int top_k, int B) {
-  (void)M; (void)E; (void)top_k; (void)B;
-  return GemmPath::kGemv;
+  (void)M; (void)E; (void)top_k;
+  if (!moe::tc_supports_block(B)) return GemmPath::kGemv;
+  if (forced_path() == 1) return GemmPath::kGemv;
+  return GemmPath::kTensorCore;
+}
+
+// A library-wide status word (one per device) for entry points without a
+// workspace; moe_get_device_status reports it together with the workspace's.
+static __device__ int g_lib_status;
+std::mutex g_lib_status_mutex;
+int *g_lib_status_ptr[64] = {};
+
+int *lib_status() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(g_lib_status_mutex);
+  if (g_lib_status_ptr[dev] == nullptr) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_lib_status) == cudaSuccess) g_lib_status_ptr[dev] = static_cast<int *>(p);
+  }
+  return g_lib_status_ptr[dev];
 }
 
 moe_status_t run_gemm1(const uint16_t *x, const uint16_t *w13, const int32_t *sorted,
                        const int32_t *eids, const int32_t *npost, int M, int top_k, int E, int H,
-                       int I, int B, uint16_t *a, cudaStream_t s) {
+                       int I, int B, uint16_t *a, int *status, cudaStream_t s) {
   const long P = static_cast<long>(M) * top_k;
   const int cap = static_cast<int>(capacity(P, E, B));
   switch (pick_path(M, E, top_k, B)) {
+    case GemmPath::kTensorCore:
+      return cuda_status(moe::launch_tc_w13_act(x, w13, sorted, eids, npost, static_cast<int>(P),
+                                                top_k, E, H, I, B, cap, a, status, s));
     case GemmPath::kGemv:
     default:
       return cuda_status(moe::launch_gemv_w13_act(x, w13, sorted, eids, npost, static_cast<int>(P),
@@ -105,10 +138,15 @@ moe_status_t run_gemm1(const uint16_t *x, const uint16_t *w13, const int32_t *so
 
 moe_status_t run_gemm2(const uint16_t *a, const uint16_t *w2, const int32_t *sorted,
                        const int32_t *eids, const int32_t *npost, const float *wts, int M,
-                       int top_k, int E, int H, int I, int B, float *yacc, cudaStream_t s) {
+                       int top_k, int E, int H, int I, int B, float *yacc, int *status,
+                       cudaStream_t s) {
   const long P = static_cast<long>(M) * top_k;
   const int cap = static_cast<int>(capacity(P, E, B));
   switch (pick_path(M, E, top_k, B)) {
+    case GemmPath::kTensorCore:
+      return cuda_status(moe::launch_tc_w2_combine(a, w2, sorted, eids, npost, wts,
+                                                   static_cast<int>(P), top_k, E, H, I, B, cap,
+                                                   yacc, status, s));
     case GemmPath::kGemv:
     default:
       return cuda_status(moe::launch_gemv_w2_combine(a, w2, sorted, eids, npost, wts,
@@ -222,7 +260,7 @@ moe_status_t moe_grouped_gemm_w13_act(const moe_bf16_t *x, const moe_bf16_t *w13
     return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w13)) return MOE_ERR_INVALID_ARG;
   return run_gemm1(x, w13, sorted_token_ids, expert_ids, num_tokens_post_padded, M, top_k, E, H, I,
-                   block_size_m, a, stream);
+                   block_size_m, a, lib_status(), stream);
 }
 
 moe_status_t moe_grouped_gemm_w2_combine(const moe_bf16_t *a, const moe_bf16_t *w2,
@@ -249,7 +287,7 @@ moe_status_t moe_grouped_gemm_w2_combine(const moe_bf16_t *a, const moe_bf16_t *
   cudaError_t e = cudaMemsetAsync(yacc, 0, sizeof(float) * static_cast<size_t>(M) * H, stream);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   st = run_gemm2(a, w2, sorted_token_ids, expert_ids, num_tokens_post_padded, topk_weights, M,
-                 top_k, E, H, I, block_size_m, yacc, stream);
+                 top_k, E, H, I, block_size_m, yacc, at<int>(ws, 0), stream);
   if (st != MOE_OK) return st;
   return cuda_status(moe::launch_finalize(yacc, residual, M, H, y, stream));
 }
@@ -297,12 +335,12 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *w_router,
                                      at<int32_t>(ws, L.hist), status, stream));
   if (st != MOE_OK) return st;
   uint16_t *a = at<uint16_t>(ws, L.a);
-  st = run_gemm1(x, w13, sorted, eids, npost, M, top_k, E, H, I, B, a, stream);
+  st = run_gemm1(x, w13, sorted, eids, npost, M, top_k, E, H, I, B, a, status, stream);
   if (st != MOE_OK) return st;
   float *yacc = at<float>(ws, L.yacc);
   if (cudaMemsetAsync(yacc, 0, sizeof(float) * static_cast<size_t>(M) * H, stream) != cudaSuccess)
     return MOE_ERR_CUDA;
-  st = run_gemm2(a, w2, sorted, eids, npost, wts, M, top_k, E, H, I, B, yacc, stream);
+  st = run_gemm2(a, w2, sorted, eids, npost, wts, M, top_k, E, H, I, B, yacc, status, stream);
   if (st != MOE_OK) return st;
   return cuda_status(moe::launch_finalize(yacc, residual, M, H, y, stream));
 }
@@ -315,15 +353,17 @@ moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream) 
 
 moe_status_t moe_get_device_status(void *ws, cudaStream_t stream) {
   if (!ws) return MOE_ERR_INVALID_ARG;
-  int host = 0;
-  if (cudaMemcpyAsync(&host, ws, sizeof(int), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+  int host[2] = {0, 0};
+  int *lib = lib_status();
+  if (cudaMemcpyAsync(&host[0], ws, sizeof(int), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (lib && cudaMemcpyAsync(&host[1], lib, sizeof(int), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
-  if (host != 0) {
-    if (cudaMemsetAsync(ws, 0, sizeof(int), stream) != cudaSuccess) return MOE_ERR_CUDA;
-    if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
-  }
-  return static_cast<moe_status_t>(host);
+  if (host[0] != 0 && cudaMemsetAsync(ws, 0, sizeof(int), stream) != cudaSuccess) return MOE_ERR_CUDA;
+  if (host[1] != 0 && cudaMemsetAsync(lib, 0, sizeof(int), stream) != cudaSuccess) return MOE_ERR_CUDA;
+  if ((host[0] | host[1]) != 0 && cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
+  return static_cast<moe_status_t>(host[0] != 0 ? host[0] : host[1]);
 }
 
 }  // extern "C"
@@ -387,7 +427,7 @@ extern "C" moe_status_t moe_grouped_gemm_w2_combine_noalloc(
   if (cudaMemsetAsync(acc, 0, sizeof(float) * static_cast<size_t>(M) * H, stream) != cudaSuccess)
     return MOE_ERR_CUDA;
   st = run_gemm2(a, w2, sorted_token_ids, expert_ids, num_tokens_post_padded, topk_weights, M,
-                 top_k, E, H, I, block_size_m, acc, stream);
+                 top_k, E, H, I, block_size_m, acc, lib_status(), stream);
   if (st != MOE_OK) return st;
   return cuda_status(moe::launch_finalize(acc, residual, M, H, y, stream));
 }

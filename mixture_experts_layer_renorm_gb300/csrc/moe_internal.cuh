@@ -83,6 +83,18 @@ cudaError_t launch_gemv_w2_combine(const uint16_t *a, const uint16_t *w2, const 
                                    const float *topk_weights, int P, int top_k, int E, int H, int I,
                                    int B, int cap, float *y_acc, cudaStream_t s);
 
+// S3 / S4 on the tensor cores (tcgen05 + TMEM + TMA), block sizes 16..256 (multiples of 16
+// that are powers of two).  status: device status word for bounded-wait timeouts (nullable).
+bool tc_supports_block(int B);
+cudaError_t launch_tc_w13_act(const uint16_t *x, const uint16_t *w13, const int32_t *sorted_ids,
+                              const int32_t *expert_ids, const int32_t *n_post, int P, int top_k,
+                              int E, int H, int I, int B, int cap, uint16_t *a, int *status,
+                              cudaStream_t s);
+cudaError_t launch_tc_w2_combine(const uint16_t *a, const uint16_t *w2, const int32_t *sorted_ids,
+                                 const int32_t *expert_ids, const int32_t *n_post,
+                                 const float *topk_weights, int P, int top_k, int E, int H, int I,
+                                 int B, int cap, float *y_acc, int *status, cudaStream_t s);
+
 // y = bf16(y_acc + residual)
 cudaError_t launch_finalize(const float *y_acc, const uint16_t *residual, int M, int H, uint16_t *y,
                             cudaStream_t s);

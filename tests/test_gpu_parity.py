@@ -198,11 +198,20 @@ def align_on_device(ids_np, E, B):
 
 GEMM_SHAPES = [(3, 4, 2, 128, 64, 16), (64, 128, 8, 2048, 768, 16), (64, 60, 4, 2048, 1408, 16),
                (33, 16, 3, 256, 160, 4), (200, 32, 4, 512, 96, 32), (128, 256, 8, 2048, 512, 16),
-               (512, 128, 8, 2048, 768, 32), (1, 128, 8, 2048, 768, 16)]
+               (512, 128, 8, 2048, 768, 32), (1, 128, 8, 2048, 768, 16), (300, 8, 2, 192, 48, 64),
+               (1000, 16, 4, 320, 208, 128), (700, 4, 2, 256, 128, 256), (40, 3, 3, 80, 16, 16)]
+
+
+@pytest.fixture(params=["tc", "gemv"])
+def gemm_path(request, monkeypatch):
+    """Runs a test once per grouped-GEMM implementation (tensor-core kernels for
+    block sizes 16..256, CUDA-core weight-streaming kernels otherwise)."""
+    monkeypatch.setenv("MOE_FORCE_PATH", request.param)
+    return request.param
 
 
 @pytest.mark.parametrize("M,E,k,H,I,B", GEMM_SHAPES)
-def test_grouped_gemm_w13_act(M, E, k, H, I, B):
+def test_grouped_gemm_w13_act(M, E, k, H, I, B, gemm_path):
     x, w13, w2, lg = layer_case(M, E, k, H, I, seed=M + E + H)
     ids, _ = oracle.topk_softmax(bits(lg), k)
     s, e, n = align_on_device(ids, E, B)
@@ -215,7 +224,7 @@ def test_grouped_gemm_w13_act(M, E, k, H, I, B):
 
 @pytest.mark.parametrize("M,E,k,H,I,B", GEMM_SHAPES)
 @pytest.mark.parametrize("with_residual", [False, True])
-def test_grouped_gemm_w2_combine(M, E, k, H, I, B, with_residual):
+def test_grouped_gemm_w2_combine(M, E, k, H, I, B, with_residual, gemm_path):
     x, w13, w2, lg = layer_case(M, E, k, H, I, seed=2 * M + E + I)
     ids, w = oracle.topk_softmax(bits(lg), k)
     a_bits = oracle.expert_act(bits(x), bits(w13), ids)     # oracle activation as the input

@@ -240,8 +240,11 @@ class Layer:
         return int(torch.unique(self.ids).numel())
 
 
-def run_point(moe, w, M, steps, warmup, device, stream, flush):
-    L = Layer(moe, w, M, warmup + steps, device)
+def run_point(moe, w, M, steps, warmup, device, stream, flush, L=None):
+    if L is None:
+        L = Layer(moe, w, M, warmup + steps, device)
+    # inputs are drawn on the default stream; the steps run on `stream`
+    torch.cuda.synchronize()
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(warmup + steps)]
     with torch.cuda.stream(stream):
         for i in range(warmup):
@@ -269,6 +272,7 @@ def e2e_point(moe, L, steps, warmup, device, stream, flush):
     dx = torch.empty((M, w.H), dtype=torch.bfloat16, device=device)
     dl = torch.empty((M, w.E), dtype=torch.bfloat16, device=device) if w.logits_given else None
     times = []
+    torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         for i in range(warmup + steps):
             flush.zero_()
@@ -333,11 +337,12 @@ def ours(args):
     stream = torch.cuda.Stream(device=device)
     flush = torch.empty(args.flush_mb << 20, dtype=torch.uint8, device=device)
 
+    L = Layer(moe, w, M, args.warmup + args.steps, device)
     # the timed region: K steps, barrier + synchronize on both sides
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(device) as clk:
-        L, per, step_ms, D = run_point(moe, w, M, args.steps, args.warmup, device, stream, flush)
+        L, per, step_ms, D = run_point(moe, w, M, args.steps, args.warmup, device, stream, flush, L)
     torch.cuda.synchronize()
     barrier(world)
     local_total_ms = sum(step_ms)

@@ -32,6 +32,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "moe_internal.cuh"
@@ -200,30 +201,40 @@ struct TcConfig {
   static constexpr int kStages =
       (kSmemBudget / static_cast<int>(kStageBytes)) < kMaxStages ? kSmemBudget / static_cast<int>(kStageBytes)
                                                                  : kMaxStages;
-  static constexpr uint32_t kTmemCols = (2 * N <= 32) ? 32 : (2 * N <= 64) ? 64 : (2 * N <= 128) ? 128
-                                        : (2 * N <= 256) ? 256 : 512;
-  // barriers: full[S], empty[S], tmem_full; then tmem address, abort flag, rows, pairs
-  static constexpr uint32_t kCtlBytes = 8 * (2 * kStages + 1) + 16 + 8 * N;
+  // accumulator buffers in TMEM: two (epilogue of one tile overlaps the
+  // mainloop of the next) while 2 x 2N fp32 columns fit the 512 columns
+  static constexpr int kAccBufs = (4 * N <= 512) ? 2 : 1;
+  static constexpr uint32_t kAccCols = 2 * N;
+  static constexpr uint32_t kTmemCols = (kAccBufs * kAccCols <= 32) ? 32
+                                        : (kAccBufs * kAccCols <= 64) ? 64
+                                        : (kAccBufs * kAccCols <= 128) ? 128
+                                        : (kAccBufs * kAccCols <= 256) ? 256 : 512;
+  // gathers may trail their stage's TMA by this many stages
+  static constexpr int kLag = kStages - 1 < 3 ? kStages - 1 : 3;
+  // barriers: full[S], empty[S], acc_full[2], acc_empty[2]; tmem address, abort flag; rows[N]
+  static constexpr uint32_t kCtlBytes = 8 * (2 * kStages + 4) + 16 + 4 * N;
   static constexpr uint32_t kSmemBytes = 1024 + kStages * kStageBytes + kCtlBytes;
   static_assert(kStages >= 3, "pipeline needs at least three stages");
 };
 
+// Tile t of the persistent schedule: block t / n_ctiles, channel tile t % n_ctiles
+// (channel tiles of one block are neighbours, so concurrently running CTAs
+// share the block's gathered rows and the expert's weights in L2).
+//
 // MODE 0: GEMM 1 + SiLU-and-mul; MODE 1: GEMM 2 + weighted combine.
 template <int N, int MODE>
 __global__ void __launch_bounds__(kTcThreads, 1)
 k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict__ src,
           const int32_t *__restrict__ sorted_ids, const int32_t *__restrict__ expert_ids,
           const int32_t *__restrict__ n_post_ptr, const float *__restrict__ topk_w, int P,
-          int top_k, int E, int K, int R_out, int B, int cap, uint16_t *__restrict__ a_out,
-          float *__restrict__ y_acc, int H_out, int *status) {
+          int top_k, int E, int K, int R_out, int B, int cap, int n_ctiles,
+          uint16_t *__restrict__ a_out, float *__restrict__ y_acc, int H_out, int *status) {
   using Cfg = TcConfig<N>;
   constexpr int S = Cfg::kStages;
-  const int b = blockIdx.x;
-  const int tile = blockIdx.y;
+  constexpr int LAG = Cfg::kLag;
   const int n_post = min(max(*n_post_ptr, 0), cap);
-  if (b >= n_post / B) return;
-  const int e = expert_ids[b];
-  if (e < 0 || e >= E) return;
+  const int n_tiles = (n_post / B) * n_ctiles;
+  if (static_cast<int>(blockIdx.x) >= n_tiles) return;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -232,11 +243,11 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
   uint64_t *bars = reinterpret_cast<uint64_t *>(b_tiles + S * Cfg::kBStageBytes);
   uint64_t *full = bars;
   uint64_t *empty = bars + S;
-  uint64_t *tmem_full = bars + 2 * S;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 1);
+  uint64_t *acc_full = bars + 2 * S;
+  uint64_t *acc_empty = bars + 2 * S + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 4);
   volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
-  int *rows = reinterpret_cast<int *>(tmem_slot + 4);
-  int *pairs = rows + N;
+  int *rows = reinterpret_cast<int *>(tmem_slot + 4);       // producer's current block
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -244,18 +255,12 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
       mbar_init(smem_u32(&full[s]), 1 + 32);  // the TMA lane's expect_tx + 32 gather lanes
       mbar_init(smem_u32(&empty[s]), 1);      // one tcgen05.commit
     }
-    mbar_init(smem_u32(tmem_full), 1);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(smem_u32(&acc_full[a]), 1);   // one tcgen05.commit
+      mbar_init(smem_u32(&acc_empty[a]), 4);  // one arrive per epilogue warp
+    }
     *abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  for (int j = threadIdx.x; j < N; j += blockDim.x) {
-    int p = -1;
-    if (j < B) {
-      const int v = sorted_ids[(size_t)b * B + j];
-      if (v >= 0 && v < P) p = v;
-    }
-    pairs[j] = p;
-    rows[j] = p < 0 ? -1 : (MODE == 0 ? p / top_k : p);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
@@ -266,50 +271,68 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int nk = (K + kBK - 1) / kBK;
-  // weight rows of the two MMA tiles
-  const int row0 = MODE == 0 ? tile * kTileM : tile * 2 * kTileM;
-  const int row1 = MODE == 0 ? R_out + tile * kTileM : tile * 2 * kTileM + kTileM;
 
   if (warp == 0) {
     // ------------------------------------------------------------ loads
-    int kb = 0;
-    for (; kb < nk; ++kb) {
-      const int s = kb % S;
-      const uint32_t ph = (kb / S) & 1;
-      if (!wait_bounded(smem_u32(&empty[s]), ph ^ 1, abort, status)) break;
-      const uint32_t a_s = smem_u32(a_tiles + s * 2 * kATileBytes);
-      if (lane == 0) {
-        mbar_arrive_expect_tx(smem_u32(&full[s]), 2 * kATileBytes);
-        tma_load_3d(a_s, &tmap_w, kb * kBK, row0, e, smem_u32(&full[s]));
-        tma_load_3d(a_s + kATileBytes, &tmap_w, kb * kBK, row1, e, smem_u32(&full[s]));
+    int g = 0;  // stages issued by this CTA so far
+    bool stop = false;
+    for (int t = blockIdx.x; t < n_tiles && !stop; t += gridDim.x) {
+      const int b = t / n_ctiles, c = t - b * n_ctiles;
+      const int e = expert_ids[b];
+      if (e < 0 || e >= E) continue;  // the MMA and epilogue skip this tile too
+      __syncwarp();
+      for (int j = lane; j < N; j += 32) {
+        int row = -1;
+        if (j < B) {
+          const int p = sorted_ids[(size_t)b * B + j];
+          if (p >= 0 && p < P) row = MODE == 0 ? p / top_k : p;
+        }
+        rows[j] = row;
       }
-      const uint32_t b_s = smem_u32(b_tiles + s * Cfg::kBStageBytes);
-      for (int idx = lane; idx < N * 8; idx += 32) {
-        const int r = idx >> 3, ch = idx & 7;
-        const int row = rows[r];
-        const int kel = kb * kBK + ch * 8;
-        const bool ok = row >= 0 && kel < K;
-        const uint16_t *gp = ok ? src + (size_t)row * K + kel : src;
-        const uint32_t dst = b_s + (r >> 3) * 1024 + (r & 7) * 128 + ((ch ^ (r & 7)) << 4);
-        cp_async_16(dst, gp, ok ? 16u : 0u);
-      }
-      cp_async_commit();
-      if (kb >= kCpAsyncLag) {
-        cp_async_wait<kCpAsyncLag>();
-        fence_proxy_async_smem();
-        mbar_arrive(smem_u32(&full[(kb - kCpAsyncLag) % S]));
+      __syncwarp();
+      const int row0 = MODE == 0 ? c * kTileM : c * 2 * kTileM;
+      const int row1 = MODE == 0 ? R_out + c * kTileM : c * 2 * kTileM + kTileM;
+      for (int kb = 0; kb < nk; ++kb, ++g) {
+        const int s = g % S;
+        const uint32_t ph = (g / S) & 1;
+        if (!wait_bounded(smem_u32(&empty[s]), ph ^ 1, abort, status)) {
+          stop = true;
+          break;
+        }
+        const uint32_t a_s = smem_u32(a_tiles + s * 2 * kATileBytes);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(smem_u32(&full[s]), 2 * kATileBytes);
+          tma_load_3d(a_s, &tmap_w, kb * kBK, row0, e, smem_u32(&full[s]));
+          tma_load_3d(a_s + kATileBytes, &tmap_w, kb * kBK, row1, e, smem_u32(&full[s]));
+        }
+        const uint32_t b_s = smem_u32(b_tiles + s * Cfg::kBStageBytes);
+#pragma unroll 4
+        for (int idx = lane; idx < N * 8; idx += 32) {
+          const int r = idx >> 3, ch = idx & 7;
+          const int row = rows[r];
+          const int kel = kb * kBK + ch * 8;
+          const bool ok = row >= 0 && kel < K;
+          const uint16_t *gp = ok ? src + (size_t)row * K + kel : src;
+          const uint32_t dst = b_s + (r >> 3) * 1024 + (r & 7) * 128 + ((ch ^ (r & 7)) << 4);
+          cp_async_16(dst, gp, ok ? 16u : 0u);
+        }
+        cp_async_commit();
+        if (g >= LAG) {
+          cp_async_wait<LAG>();
+          fence_proxy_async_smem();
+          mbar_arrive(smem_u32(&full[(g - LAG) % S]));
+        }
       }
     }
     // the last gathers (and, after an abort, every gather still in flight)
     cp_async_wait<0>();
     fence_proxy_async_smem();
-    for (int k2 = (kb > kCpAsyncLag ? kb - kCpAsyncLag : 0); k2 < kb; ++k2)
-      mbar_arrive(smem_u32(&full[k2 % S]));
+    for (int g2 = (g > LAG ? g - LAG : 0); g2 < g; ++g2) mbar_arrive(smem_u32(&full[g2 % S]));
     // after an abort: let the weight copies already issued land before exit
     if (*abort && lane == 0) {
-      for (int k2 = (kb > S ? kb - S : 0); k2 < kb; ++k2) {
+      for (int g2 = (g > S ? g - S : 0); g2 < g; ++g2) {
         const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(smem_u32(&full[k2 % S]), (k2 / S) & 1) &&
+        while (!mbar_try_wait(smem_u32(&full[g2 % S]), (g2 / S) & 1) &&
                globaltimer_ns() - t0 < kWaitLimitNs) {
         }
       }
@@ -318,73 +341,104 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
     // ------------------------------------------------------------ MMA
     if (lane == 0) {
       constexpr uint32_t idesc = umma_idesc_bf16(kTileM, N);
-      for (int kb = 0; kb < nk; ++kb) {
-        const int s = kb % S;
-        const uint32_t ph = (kb / S) & 1;
-        if (!wait_bounded(smem_u32(&full[s]), ph, abort, status)) break;
+      int g = 0, i = 0;
+      bool stop = false;
+      for (int t = blockIdx.x; t < n_tiles && !stop; t += gridDim.x) {
+        const int b = t / n_ctiles;
+        const int e = expert_ids[b];
+        if (e < 0 || e >= E) continue;
+        const int acc = i % Cfg::kAccBufs;
+        const uint32_t use = i / Cfg::kAccBufs;
+        ++i;
+        if (!wait_bounded(smem_u32(&acc_empty[acc]), (use & 1) ^ 1, abort, status)) break;
         tc_fence_after();
-        const uint32_t a0 = smem_u32(a_tiles + s * 2 * kATileBytes);
-        const uint32_t a1 = a0 + kATileBytes;
-        const uint32_t bt = smem_u32(b_tiles + s * Cfg::kBStageBytes);
+        const uint32_t d0 = tmem + acc * Cfg::kAccCols;
+        for (int kb = 0; kb < nk; ++kb, ++g) {
+          const int s = g % S;
+          if (!wait_bounded(smem_u32(&full[s]), (g / S) & 1, abort, status)) {
+            stop = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(a_tiles + s * 2 * kATileBytes);
+          const uint32_t a1 = a0 + kATileBytes;
+          const uint32_t bt = smem_u32(b_tiles + s * Cfg::kBStageBytes);
 #pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk) {
-          const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
-          const uint64_t bd = sw128_kmajor_desc(bt + kk * 32);
-          umma_bf16(tmem, sw128_kmajor_desc(a0 + kk * 32), bd, idesc, acc);
-          umma_bf16(tmem + N, sw128_kmajor_desc(a1 + kk * 32), bd, idesc, acc);
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint32_t accumulate = (kb > 0 || kk > 0) ? 1u : 0u;
+            const uint64_t bd = sw128_kmajor_desc(bt + kk * 32);
+            umma_bf16(d0, sw128_kmajor_desc(a0 + kk * 32), bd, idesc, accumulate);
+            umma_bf16(d0 + N, sw128_kmajor_desc(a1 + kk * 32), bd, idesc, accumulate);
+          }
+          umma_commit(smem_u32(&empty[s]));
         }
-        umma_commit(smem_u32(&empty[s]));
+        umma_commit(smem_u32(&acc_full[acc]));
       }
-      umma_commit(smem_u32(tmem_full));
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
-    bool ok = wait_bounded(smem_u32(tmem_full), 0, abort, status);
-    tc_fence_after();
-    ok = __all_sync(0xffffffffu, ok && !*abort);  // tcgen05.ld needs the whole warp
-    if (ok) {
-      const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    int i = 0;
+    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+      const int b = t / n_ctiles, c = t - b * n_ctiles;
+      const int e = expert_ids[b];
+      if (e < 0 || e >= E) continue;
+      const int acc = i % Cfg::kAccBufs;
+      const uint32_t use = i / Cfg::kAccBufs;
+      ++i;
+      bool ok = wait_bounded(smem_u32(&acc_full[acc]), use & 1, abort, status);
+      tc_fence_after();
+      ok = __all_sync(0xffffffffu, ok && !*abort);  // tcgen05.ld needs the whole warp
+      if (!ok) break;
+      const uint32_t d0 = tmem + lane_base + acc * Cfg::kAccCols;
+      const int32_t *blk = sorted_ids + (size_t)b * B;
       if (MODE == 0) {
-        const int i = tile * kTileM + q * 32 + lane;
-        const bool valid = i < R_out;
+        const int ch = c * kTileM + q * 32 + lane;
+        const bool valid = ch < R_out;
 #pragma unroll 1
         for (int j0 = 0; j0 < N; j0 += 16) {
-          uint32_t g[16], u[16];
-          tmem_ld_32x32b_x16(tmem + lane_base + j0, g);
-          tmem_ld_32x32b_x16(tmem + lane_base + N + j0, u);
+          uint32_t gt[16], up[16];
+          tmem_ld_32x32b_x16(d0 + j0, gt);
+          tmem_ld_32x32b_x16(d0 + N + j0, up);
           tmem_ld_wait();
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) {
-            const int p = pairs[j0 + jj];
-            if (valid && p >= 0) {
-              const float gb = bf16_bits_to_float(float_to_bf16_bits(__uint_as_float(g[jj])));
-              const float ub = bf16_bits_to_float(float_to_bf16_bits(__uint_as_float(u[jj])));
+            const int j = j0 + jj;
+            const int p = j < B ? blk[j] : -1;
+            if (valid && p >= 0 && p < P) {
+              const float gb = bf16_bits_to_float(float_to_bf16_bits(__uint_as_float(gt[jj])));
+              const float ub = bf16_bits_to_float(float_to_bf16_bits(__uint_as_float(up[jj])));
               const float silu = gb / (1.0f + expf(-gb));
-              a_out[(size_t)p * R_out + i] = float_to_bf16_bits(silu * ub);
+              a_out[(size_t)p * R_out + ch] = float_to_bf16_bits(silu * ub);
             }
           }
         }
       } else {
 #pragma unroll 1
-        for (int t = 0; t < 2; ++t) {
-          const int n = tile * 2 * kTileM + t * kTileM + q * 32 + lane;
+        for (int h = 0; h < 2; ++h) {
+          const int n = c * 2 * kTileM + h * kTileM + q * 32 + lane;
           const bool valid = n < H_out;
 #pragma unroll 1
           for (int j0 = 0; j0 < N; j0 += 16) {
             uint32_t o[16];
-            tmem_ld_32x32b_x16(tmem + lane_base + t * N + j0, o);
+            tmem_ld_32x32b_x16(d0 + h * N + j0, o);
             tmem_ld_wait();
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
-              const int p = pairs[j0 + jj];
-              if (valid && p >= 0)
+              const int j = j0 + jj;
+              const int p = j < B ? blk[j] : -1;
+              if (valid && p >= 0 && p < P)
                 atomicAdd(y_acc + (size_t)(p / top_k) * H_out + n, topk_w[p] * __uint_as_float(o[jj]));
             }
           }
         }
       }
+      // this accumulator buffer may be overwritten once all four warps are done with it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&acc_empty[acc]));
     }
   }
   tc_fence_before();
@@ -437,10 +491,13 @@ cudaError_t launch_tc_n(const CUtensorMap &map, const uint16_t *src, const int32
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(Cfg::kSmemBytes));
   if (err != cudaSuccess) return err;
-  const dim3 grid(cap / B, tiles);
+  // persistent: one CTA per SM at most, each walking the tile list with stride gridDim.x
+  const long max_tiles = static_cast<long>(cap / B) * tiles;
+  const int grid = static_cast<int>(std::min<long>(max_tiles, num_sms()));
+  if (grid <= 0) return cudaSuccess;
   kern<<<grid, kTcThreads, Cfg::kSmemBytes, s>>>(map, src, sorted_ids, expert_ids, n_post, topk_w, P,
-                                                 top_k, E, K, R_out, B, cap, a_out, y_acc, H_out,
-                                                 status);
+                                                 top_k, E, K, R_out, B, cap, tiles, a_out, y_acc,
+                                                 H_out, status);
   return cudaGetLastError();
 }
 

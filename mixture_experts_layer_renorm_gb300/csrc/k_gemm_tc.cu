@@ -20,15 +20,17 @@
 //   GEMM 2: D_0/1 [128, B] = W2_e[n0 .. n0+255, :] . A_b^T
 //           epilogue: y_acc[t, n] += topk_weight[p] * D (fp32 red.add)
 //
+// Persistent CTAs (one per SM) walk the list of (block, weight tile) tiles.
 // Warp roles (192 threads): warp 0 loads -- one lane issues the TMA copies
-// of the two 128 x 64 weight tiles (128-byte swizzle), all lanes gather the
-// block's rows with 16-byte cp.async into the same swizzled K-major layout;
-// warp 1 allocates TMEM and one lane issues tcgen05.mma (accumulators in
-// TMEM, 2 x B fp32 columns); warps 2-5 are the epilogue, one TMEM lane
-// quarter each (tcgen05.ld 32x32b).  A ring of shared-memory stages with
-// full/empty mbarriers connects the roles.  Every wait is bounded: after 2 s
-// the kernel records MOE_ERR_DEVICE_TIMEOUT in the status word, drains its
-// own copies and returns; it never traps.
+// of the two 128 x 64 weight tiles (128-byte swizzle) and each lane gathers
+// four of the block's rows with TMA tile::gather4 into the same swizzled
+// K-major layout; warp 1 allocates TMEM and one lane issues tcgen05.mma;
+// warps 2-5 are the epilogue, one TMEM lane quarter each (tcgen05.ld
+// 32x32b).  Two accumulator buffers in TMEM (while 4B fp32 columns fit) let
+// the epilogue of one tile overlap the mainloop of the next.  A ring of
+// shared-memory stages with full/empty mbarriers connects the roles.  Every
+// wait is bounded: after 2 s the kernel records MOE_ERR_DEVICE_TIMEOUT in the
+// status word, lets its own copies land and returns; it never traps.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -47,7 +49,6 @@ constexpr int kTileM = 128;                          // weight rows per MMA
 constexpr uint32_t kATileBytes = kTileM * kBK * 2;   // 16 KB
 constexpr int kSmemBudget = 220 * 1024;
 constexpr int kMaxStages = 6;
-constexpr int kCpAsyncLag = 1;                       // stages a row gather may trail its TMA
 constexpr uint64_t kWaitLimitNs = 2000000000ull;     // 2 s
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -111,19 +112,16 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-// Makes this thread's completed generic-proxy writes to shared memory visible
-// to the async proxy (the tensor core reads operands through it).
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+// Gathers four 128-byte rows (rows r0..r3, columns c0..c0+63 of a 2-D map
+// whose box is 64 x 1) into 512 consecutive bytes of shared memory, applying
+// the map's 128-byte swizzle; rows outside the tensor read as zero.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *map, int c0, int r0,
+                                            int r1, int r2, int r3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
+      : "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05
@@ -209,8 +207,6 @@ struct TcConfig {
                                         : (kAccBufs * kAccCols <= 64) ? 64
                                         : (kAccBufs * kAccCols <= 128) ? 128
                                         : (kAccBufs * kAccCols <= 256) ? 256 : 512;
-  // gathers may trail their stage's TMA by this many stages
-  static constexpr int kLag = kStages - 1 < 3 ? kStages - 1 : 3;
   // barriers: full[S], empty[S], acc_full[2], acc_empty[2]; tmem address, abort flag; rows[N]
   static constexpr uint32_t kCtlBytes = 8 * (2 * kStages + 4) + 16 + 4 * N;
   static constexpr uint32_t kSmemBytes = 1024 + kStages * kStageBytes + kCtlBytes;
@@ -224,14 +220,13 @@ struct TcConfig {
 // MODE 0: GEMM 1 + SiLU-and-mul; MODE 1: GEMM 2 + weighted combine.
 template <int N, int MODE>
 __global__ void __launch_bounds__(kTcThreads, 1)
-k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict__ src,
-          const int32_t *__restrict__ sorted_ids, const int32_t *__restrict__ expert_ids,
+k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_src,
+          int src_rows, const int32_t *__restrict__ sorted_ids, const int32_t *__restrict__ expert_ids,
           const int32_t *__restrict__ n_post_ptr, const float *__restrict__ topk_w, int P,
           int top_k, int E, int K, int R_out, int B, int cap, int n_ctiles,
           uint16_t *__restrict__ a_out, float *__restrict__ y_acc, int H_out, int *status) {
   using Cfg = TcConfig<N>;
   constexpr int S = Cfg::kStages;
-  constexpr int LAG = Cfg::kLag;
   const int n_post = min(max(*n_post_ptr, 0), cap);
   const int n_tiles = (n_post / B) * n_ctiles;
   if (static_cast<int>(blockIdx.x) >= n_tiles) return;
@@ -252,7 +247,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(smem_u32(&full[s]), 1 + 32);  // the TMA lane's expect_tx + 32 gather lanes
+      mbar_init(smem_u32(&full[s]), 1);       // lane 0's expect_tx; the bytes complete it
       mbar_init(smem_u32(&empty[s]), 1);      // one tcgen05.commit
     }
     for (int a = 0; a < 2; ++a) {
@@ -274,6 +269,10 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
 
   if (warp == 0) {
     // ------------------------------------------------------------ loads
+    // Lane 0 issues the two weight tiles; lane L gathers rows 4q..4q+3 of the
+    // block for q = L, L+32, ... (tile::gather4), straight into the swizzled
+    // K-major layout.
+    constexpr uint32_t kStageTx = 2 * kATileBytes + Cfg::kBStageBytes;
     int g = 0;  // stages issued by this CTA so far
     bool stop = false;
     for (int t = blockIdx.x; t < n_tiles && !stop; t += gridDim.x) {
@@ -282,7 +281,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
       if (e < 0 || e >= E) continue;  // the MMA and epilogue skip this tile too
       __syncwarp();
       for (int j = lane; j < N; j += 32) {
-        int row = -1;
+        int row = src_rows;  // past the end: reads as zero
         if (j < B) {
           const int p = sorted_ids[(size_t)b * B + j];
           if (p >= 0 && p < P) row = MODE == 0 ? p / top_k : p;
@@ -299,36 +298,22 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
           stop = true;
           break;
         }
+        const uint32_t fb = smem_u32(&full[s]);
         const uint32_t a_s = smem_u32(a_tiles + s * 2 * kATileBytes);
         if (lane == 0) {
-          mbar_arrive_expect_tx(smem_u32(&full[s]), 2 * kATileBytes);
-          tma_load_3d(a_s, &tmap_w, kb * kBK, row0, e, smem_u32(&full[s]));
-          tma_load_3d(a_s + kATileBytes, &tmap_w, kb * kBK, row1, e, smem_u32(&full[s]));
+          mbar_arrive_expect_tx(fb, kStageTx);
+          tma_load_3d(a_s, &tmap_w, kb * kBK, row0, e, fb);
+          tma_load_3d(a_s + kATileBytes, &tmap_w, kb * kBK, row1, e, fb);
         }
+        __syncwarp();
         const uint32_t b_s = smem_u32(b_tiles + s * Cfg::kBStageBytes);
-#pragma unroll 4
-        for (int idx = lane; idx < N * 8; idx += 32) {
-          const int r = idx >> 3, ch = idx & 7;
-          const int row = rows[r];
-          const int kel = kb * kBK + ch * 8;
-          const bool ok = row >= 0 && kel < K;
-          const uint16_t *gp = ok ? src + (size_t)row * K + kel : src;
-          const uint32_t dst = b_s + (r >> 3) * 1024 + (r & 7) * 128 + ((ch ^ (r & 7)) << 4);
-          cp_async_16(dst, gp, ok ? 16u : 0u);
-        }
-        cp_async_commit();
-        if (g >= LAG) {
-          cp_async_wait<LAG>();
-          fence_proxy_async_smem();
-          mbar_arrive(smem_u32(&full[(g - LAG) % S]));
-        }
+#pragma unroll
+        for (int q4 = lane; q4 < N / 4; q4 += 32)
+          tma_gather4(b_s + q4 * 512, &tmap_src, kb * kBK, rows[4 * q4], rows[4 * q4 + 1],
+                      rows[4 * q4 + 2], rows[4 * q4 + 3], fb);
       }
     }
-    // the last gathers (and, after an abort, every gather still in flight)
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
-    for (int g2 = (g > LAG ? g - LAG : 0); g2 < g; ++g2) mbar_arrive(smem_u32(&full[g2 % S]));
-    // after an abort: let the weight copies already issued land before exit
+    // after an abort: let the copies already issued land before exit
     if (*abort && lane == 0) {
       for (int g2 = (g > S ? g - S : 0); g2 < g; ++g2) {
         const uint64_t t0 = globaltimer_ns();
@@ -480,11 +465,28 @@ cudaError_t make_weight_map(CUtensorMap *map, const uint16_t *w, int K, int rows
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// 2-D map over gathered rows [rows][K] (bf16, K contiguous), box 64 x 1 (one
+// row high, as tile::gather4 requires), 128-byte swizzle.
+cudaError_t make_row_map(CUtensorMap *map, const uint16_t *base, int K, int rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode_fn();
+  if (encode == nullptr) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+  const cuuint32_t box[2] = {kBK, 1};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(base),
+                            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int N, int MODE>
-cudaError_t launch_tc_n(const CUtensorMap &map, const uint16_t *src, const int32_t *sorted_ids,
-                        const int32_t *expert_ids, const int32_t *n_post, const float *topk_w, int P,
-                        int top_k, int E, int K, int R_out, int B, int cap, uint16_t *a_out,
-                        float *y_acc, int H_out, int *status, int tiles, cudaStream_t s) {
+cudaError_t launch_tc_n(const CUtensorMap &map_w, const CUtensorMap &map_src, int src_rows,
+                        const int32_t *sorted_ids, const int32_t *expert_ids, const int32_t *n_post,
+                        const float *topk_w, int P, int top_k, int E, int K, int R_out, int B,
+                        int cap, uint16_t *a_out, float *y_acc, int H_out, int *status, int tiles,
+                        cudaStream_t s) {
   using Cfg = TcConfig<N>;
   auto kern = k_gemm_tc<N, MODE>;
   cudaError_t err = cudaFuncSetAttribute(reinterpret_cast<const void *>(kern),
@@ -495,21 +497,23 @@ cudaError_t launch_tc_n(const CUtensorMap &map, const uint16_t *src, const int32
   const long max_tiles = static_cast<long>(cap / B) * tiles;
   const int grid = static_cast<int>(std::min<long>(max_tiles, num_sms()));
   if (grid <= 0) return cudaSuccess;
-  kern<<<grid, kTcThreads, Cfg::kSmemBytes, s>>>(map, src, sorted_ids, expert_ids, n_post, topk_w, P,
-                                                 top_k, E, K, R_out, B, cap, tiles, a_out, y_acc,
-                                                 H_out, status);
+  kern<<<grid, kTcThreads, Cfg::kSmemBytes, s>>>(map_w, map_src, src_rows, sorted_ids, expert_ids,
+                                                 n_post, topk_w, P, top_k, E, K, R_out, B, cap,
+                                                 tiles, a_out, y_acc, H_out, status);
   return cudaGetLastError();
 }
 
 template <int MODE>
-cudaError_t launch_tc(const CUtensorMap &map, const uint16_t *src, const int32_t *sorted_ids,
-                      const int32_t *expert_ids, const int32_t *n_post, const float *topk_w, int P,
-                      int top_k, int E, int K, int R_out, int B, int cap, uint16_t *a_out,
-                      float *y_acc, int H_out, int *status, int tiles, cudaStream_t s) {
-#define MOE_TC_CASE(NN)                                                                         \
-  case NN:                                                                                      \
-    return launch_tc_n<NN, MODE>(map, src, sorted_ids, expert_ids, n_post, topk_w, P, top_k, E, \
-                                 K, R_out, B, cap, a_out, y_acc, H_out, status, tiles, s)
+cudaError_t launch_tc(const CUtensorMap &map_w, const CUtensorMap &map_src, int src_rows,
+                      const int32_t *sorted_ids, const int32_t *expert_ids, const int32_t *n_post,
+                      const float *topk_w, int P, int top_k, int E, int K, int R_out, int B,
+                      int cap, uint16_t *a_out, float *y_acc, int H_out, int *status, int tiles,
+                      cudaStream_t s) {
+#define MOE_TC_CASE(NN)                                                                            \
+  case NN:                                                                                         \
+    return launch_tc_n<NN, MODE>(map_w, map_src, src_rows, sorted_ids, expert_ids, n_post, topk_w, \
+                                 P, top_k, E, K, R_out, B, cap, a_out, y_acc, H_out, status,      \
+                                 tiles, s)
   switch (B) {
     MOE_TC_CASE(16);
     MOE_TC_CASE(32);
@@ -530,24 +534,29 @@ cudaError_t launch_tc_w13_act(const uint16_t *x, const uint16_t *w13, const int3
                               const int32_t *expert_ids, const int32_t *n_post, int P, int top_k,
                               int E, int H, int I, int B, int cap, uint16_t *a, int *status,
                               cudaStream_t s) {
-  CUtensorMap map;
-  cudaError_t err = make_weight_map(&map, w13, H, 2 * I, E);
+  CUtensorMap map_w, map_x;
+  cudaError_t err = make_weight_map(&map_w, w13, H, 2 * I, E);
+  if (err != cudaSuccess) return err;
+  const int M = (P + top_k - 1) / top_k;
+  err = make_row_map(&map_x, x, H, M);
   if (err != cudaSuccess) return err;
   const int tiles = (I + kTileM - 1) / kTileM;
-  return launch_tc<0>(map, x, sorted_ids, expert_ids, n_post, nullptr, P, top_k, E, H, I, B, cap,
-                      a, nullptr, 0, status, tiles, s);
+  return launch_tc<0>(map_w, map_x, M, sorted_ids, expert_ids, n_post, nullptr, P, top_k, E, H, I,
+                      B, cap, a, nullptr, 0, status, tiles, s);
 }
 
 cudaError_t launch_tc_w2_combine(const uint16_t *a, const uint16_t *w2, const int32_t *sorted_ids,
                                  const int32_t *expert_ids, const int32_t *n_post,
                                  const float *topk_weights, int P, int top_k, int E, int H, int I,
                                  int B, int cap, float *y_acc, int *status, cudaStream_t s) {
-  CUtensorMap map;
-  cudaError_t err = make_weight_map(&map, w2, I, H, E);
+  CUtensorMap map_w, map_a;
+  cudaError_t err = make_weight_map(&map_w, w2, I, H, E);
+  if (err != cudaSuccess) return err;
+  err = make_row_map(&map_a, a, I, P);
   if (err != cudaSuccess) return err;
   const int tiles = (H + 2 * kTileM - 1) / (2 * kTileM);
-  return launch_tc<1>(map, a, sorted_ids, expert_ids, n_post, topk_weights, P, top_k, E, I, H, B,
-                      cap, nullptr, y_acc, H, status, tiles, s);
+  return launch_tc<1>(map_w, map_a, P, sorted_ids, expert_ids, n_post, topk_weights, P, top_k, E,
+                      I, H, B, cap, nullptr, y_acc, H, status, tiles, s);
 }
 
 }  // namespace moe

@@ -207,28 +207,44 @@ struct TcConfig {
                                         : (kAccBufs * kAccCols <= 64) ? 64
                                         : (kAccBufs * kAccCols <= 128) ? 128
                                         : (kAccBufs * kAccCols <= 256) ? 256 : 512;
-  // barriers: full[S], empty[S], acc_full[2], acc_empty[2]; tmem address, abort flag; rows[N]
-  static constexpr uint32_t kCtlBytes = 8 * (2 * kStages + 4) + 16 + 4 * N;
+  // barriers: full[S], empty[S], acc_full[2], acc_empty[2]; tmem address,
+  // abort flag; producer rows[N]; epilogue destination rows[N], weights[N]
+  static constexpr uint32_t kCtlBytes = 8 * (2 * kStages + 4) + 16 + 12 * N;
   static constexpr uint32_t kSmemBytes = 1024 + kStages * kStageBytes + kCtlBytes;
   static_assert(kStages >= 3, "pipeline needs at least three stages");
 };
 
-// Tile t of the persistent schedule: block t / n_ctiles, channel tile t % n_ctiles
-// (channel tiles of one block are neighbours, so concurrently running CTAs
-// share the block's gathered rows and the expert's weights in L2).
+__device__ __forceinline__ void epilogue_bar_sync() {
+  asm volatile("bar.sync 1, 128;" ::: "memory");  // the four epilogue warps only
+}
+
+// Persistent tiles: tile t = (block t / n_ctiles, weight tile t % n_ctiles);
+// the weight tiles of one block are neighbours, so concurrently running CTAs
+// share the block's gathered rows and the expert's weights in L2.
 //
-// MODE 0: GEMM 1 + SiLU-and-mul; MODE 1: GEMM 2 + weighted combine.
+// MODE 0: GEMM 1 + SiLU-and-mul   rows = x[p / top_k], A = W13_e gate | up tiles,
+//                                 a[p, i] = bf16(SiLU(bf16 gate) * bf16 up)
+// MODE 1: GEMM 2 + combine        rows = a[p],         A = W2_e rows n0..n0+255,
+//                                 y_acc[p / top_k, n] += topk_w[p] * o
+// MODE 2: router logits           rows = x[t] (blocks of N consecutive tokens),
+//                                 A = W_r rows e0..e0+255, logits[t, e] = bf16(D + bias[e])
 template <int N, int MODE>
 __global__ void __launch_bounds__(kTcThreads, 1)
 k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_src,
           int src_rows, const int32_t *__restrict__ sorted_ids, const int32_t *__restrict__ expert_ids,
-          const int32_t *__restrict__ n_post_ptr, const float *__restrict__ topk_w, int P,
-          int top_k, int E, int K, int R_out, int B, int cap, int n_ctiles,
-          uint16_t *__restrict__ a_out, float *__restrict__ y_acc, int H_out, int *status) {
+          const int32_t *__restrict__ n_post_ptr, const float *__restrict__ vec, int P, int top_k,
+          int E, int K, int R_out, int a_rows, int B, int cap, int n_ctiles,
+          uint16_t *__restrict__ out16, float *__restrict__ y_acc, int H_out, int *status) {
   using Cfg = TcConfig<N>;
   constexpr int S = Cfg::kStages;
-  const int n_post = min(max(*n_post_ptr, 0), cap);
-  const int n_tiles = (n_post / B) * n_ctiles;
+  int n_blocks;
+  if (MODE == 2) {
+    n_blocks = (src_rows + N - 1) / N;
+  } else {
+    const int n_post = min(max(*n_post_ptr, 0), cap);
+    n_blocks = n_post / B;
+  }
+  const int n_tiles = n_blocks * n_ctiles;
   if (static_cast<int>(blockIdx.x) >= n_tiles) return;
 
   extern __shared__ uint8_t smem_raw[];
@@ -242,7 +258,9 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CU
   uint64_t *acc_empty = bars + 2 * S + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 4);
   volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
-  int *rows = reinterpret_cast<int *>(tmem_slot + 4);       // producer's current block
+  int *rows = reinterpret_cast<int *>(tmem_slot + 4);        // producer's current block
+  int *dst_row = rows + N;                                   // epilogue's current block
+  float *dst_w = reinterpret_cast<float *>(dst_row + N);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -269,20 +287,21 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CU
 
   if (warp == 0) {
     // ------------------------------------------------------------ loads
-    // Lane 0 issues the two weight tiles; lane L gathers rows 4q..4q+3 of the
+    // Lane 0 issues the weight tiles; lane L gathers rows 4q..4q+3 of the
     // block for q = L, L+32, ... (tile::gather4), straight into the swizzled
     // K-major layout.
-    constexpr uint32_t kStageTx = 2 * kATileBytes + Cfg::kBStageBytes;
     int g = 0;  // stages issued by this CTA so far
     bool stop = false;
     for (int t = blockIdx.x; t < n_tiles && !stop; t += gridDim.x) {
       const int b = t / n_ctiles, c = t - b * n_ctiles;
-      const int e = expert_ids[b];
+      const int e = MODE == 2 ? 0 : expert_ids[b];
       if (e < 0 || e >= E) continue;  // the MMA and epilogue skip this tile too
       __syncwarp();
       for (int j = lane; j < N; j += 32) {
         int row = src_rows;  // past the end: reads as zero
-        if (j < B) {
+        if (MODE == 2) {
+          if (b * N + j < src_rows) row = b * N + j;
+        } else if (j < B) {
           const int p = sorted_ids[(size_t)b * B + j];
           if (p >= 0 && p < P) row = MODE == 0 ? p / top_k : p;
         }
@@ -291,6 +310,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CU
       __syncwarp();
       const int row0 = MODE == 0 ? c * kTileM : c * 2 * kTileM;
       const int row1 = MODE == 0 ? R_out + c * kTileM : c * 2 * kTileM + kTileM;
+      const bool two = MODE == 0 || row1 < a_rows;
+      const uint32_t stage_tx = (two ? 2 : 1) * kATileBytes + Cfg::kBStageBytes;
       for (int kb = 0; kb < nk; ++kb, ++g) {
         const int s = g % S;
         const uint32_t ph = (g / S) & 1;
@@ -301,9 +322,9 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CU
         const uint32_t fb = smem_u32(&full[s]);
         const uint32_t a_s = smem_u32(a_tiles + s * 2 * kATileBytes);
         if (lane == 0) {
-          mbar_arrive_expect_tx(fb, kStageTx);
+          mbar_arrive_expect_tx(fb, stage_tx);
           tma_load_3d(a_s, &tmap_w, kb * kBK, row0, e, fb);
-          tma_load_3d(a_s + kATileBytes, &tmap_w, kb * kBK, row1, e, fb);
+          if (two) tma_load_3d(a_s + kATileBytes, &tmap_w, kb * kBK, row1, e, fb);
         }
         __syncwarp();
         const uint32_t b_s = smem_u32(b_tiles + s * Cfg::kBStageBytes);
@@ -329,9 +350,10 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CU
       int g = 0, i = 0;
       bool stop = false;
       for (int t = blockIdx.x; t < n_tiles && !stop; t += gridDim.x) {
-        const int b = t / n_ctiles;
-        const int e = expert_ids[b];
+        const int b = t / n_ctiles, c = t - b * n_ctiles;
+        const int e = MODE == 2 ? 0 : expert_ids[b];
         if (e < 0 || e >= E) continue;
+        const bool two = MODE == 0 || c * 2 * kTileM + kTileM < a_rows;
         const int acc = i % Cfg::kAccBufs;
         const uint32_t use = i / Cfg::kAccBufs;
         ++i;
@@ -353,7 +375,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CU
             const uint32_t accumulate = (kb > 0 || kk > 0) ? 1u : 0u;
             const uint64_t bd = sw128_kmajor_desc(bt + kk * 32);
             umma_bf16(d0, sw128_kmajor_desc(a0 + kk * 32), bd, idesc, accumulate);
-            umma_bf16(d0 + N, sw128_kmajor_desc(a1 + kk * 32), bd, idesc, accumulate);
+            if (two) umma_bf16(d0 + N, sw128_kmajor_desc(a1 + kk * 32), bd, idesc, accumulate);
           }
           umma_commit(smem_u32(&empty[s]));
         }
@@ -364,21 +386,40 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CU
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int et = threadIdx.x - 64;  // 0..127 over the four epilogue warps
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     int i = 0;
     for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
       const int b = t / n_ctiles, c = t - b * n_ctiles;
-      const int e = expert_ids[b];
+      const int e = MODE == 2 ? 0 : expert_ids[b];
       if (e < 0 || e >= E) continue;
+      const bool two = MODE == 0 || c * 2 * kTileM + kTileM < a_rows;
       const int acc = i % Cfg::kAccBufs;
       const uint32_t use = i / Cfg::kAccBufs;
       ++i;
+      // the block's destinations (and router weights), staged while the MMAs run
+      epilogue_bar_sync();  // the previous tile's readers are done
+      for (int j = et; j < N; j += 128) {
+        int d = -1;
+        float wgt = 0.f;
+        if (MODE == 2) {
+          if (b * N + j < src_rows) d = b * N + j;
+        } else if (j < B) {
+          const int p = sorted_ids[(size_t)b * B + j];
+          if (p >= 0 && p < P) {
+            d = MODE == 0 ? p : p / top_k;
+            if (MODE == 1) wgt = vec[p];
+          }
+        }
+        dst_row[j] = d;
+        dst_w[j] = wgt;
+      }
+      epilogue_bar_sync();
       bool ok = wait_bounded(smem_u32(&acc_full[acc]), use & 1, abort, status);
       tc_fence_after();
       ok = __all_sync(0xffffffffu, ok && !*abort);  // tcgen05.ld needs the whole warp
       if (!ok) break;
       const uint32_t d0 = tmem + lane_base + acc * Cfg::kAccCols;
-      const int32_t *blk = sorted_ids + (size_t)b * B;
       if (MODE == 0) {
         const int ch = c * kTileM + q * 32 + lane;
         const bool valid = ch < R_out;
@@ -390,21 +431,21 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CU
           tmem_ld_wait();
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) {
-            const int j = j0 + jj;
-            const int p = j < B ? blk[j] : -1;
-            if (valid && p >= 0 && p < P) {
+            const int p = dst_row[j0 + jj];
+            if (valid && p >= 0) {
               const float gb = bf16_bits_to_float(float_to_bf16_bits(__uint_as_float(gt[jj])));
               const float ub = bf16_bits_to_float(float_to_bf16_bits(__uint_as_float(up[jj])));
               const float silu = gb / (1.0f + expf(-gb));
-              a_out[(size_t)p * R_out + ch] = float_to_bf16_bits(silu * ub);
+              out16[(size_t)p * R_out + ch] = float_to_bf16_bits(silu * ub);
             }
           }
         }
       } else {
 #pragma unroll 1
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < (two ? 2 : 1); ++h) {
           const int n = c * 2 * kTileM + h * kTileM + q * 32 + lane;
-          const bool valid = n < H_out;
+          const bool valid = n < (MODE == 1 ? H_out : a_rows);
+          const float bias = (MODE == 2 && valid && vec != nullptr) ? vec[n] : 0.f;
 #pragma unroll 1
           for (int j0 = 0; j0 < N; j0 += 16) {
             uint32_t o[16];
@@ -412,10 +453,13 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CU
             tmem_ld_wait();
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
-              const int j = j0 + jj;
-              const int p = j < B ? blk[j] : -1;
-              if (valid && p >= 0 && p < P)
-                atomicAdd(y_acc + (size_t)(p / top_k) * H_out + n, topk_w[p] * __uint_as_float(o[jj]));
+              const int d = dst_row[j0 + jj];
+              if (valid && d >= 0) {
+                if (MODE == 1)
+                  atomicAdd(y_acc + (size_t)d * H_out + n, dst_w[j0 + jj] * __uint_as_float(o[jj]));
+                else
+                  out16[(size_t)d * a_rows + n] = float_to_bf16_bits(__uint_as_float(o[jj]) + bias);
+              }
             }
           }
         }
@@ -484,9 +528,9 @@ cudaError_t make_row_map(CUtensorMap *map, const uint16_t *base, int K, int rows
 template <int N, int MODE>
 cudaError_t launch_tc_n(const CUtensorMap &map_w, const CUtensorMap &map_src, int src_rows,
                         const int32_t *sorted_ids, const int32_t *expert_ids, const int32_t *n_post,
-                        const float *topk_w, int P, int top_k, int E, int K, int R_out, int B,
-                        int cap, uint16_t *a_out, float *y_acc, int H_out, int *status, int tiles,
-                        cudaStream_t s) {
+                        const float *vec, int P, int top_k, int E, int K, int R_out, int a_rows,
+                        int B, int cap, uint16_t *out16, float *y_acc, int H_out, int *status,
+                        int n_ctiles, long max_blocks, cudaStream_t s) {
   using Cfg = TcConfig<N>;
   auto kern = k_gemm_tc<N, MODE>;
   cudaError_t err = cudaFuncSetAttribute(reinterpret_cast<const void *>(kern),
@@ -494,27 +538,26 @@ cudaError_t launch_tc_n(const CUtensorMap &map_w, const CUtensorMap &map_src, in
                                          static_cast<int>(Cfg::kSmemBytes));
   if (err != cudaSuccess) return err;
   // persistent: one CTA per SM at most, each walking the tile list with stride gridDim.x
-  const long max_tiles = static_cast<long>(cap / B) * tiles;
-  const int grid = static_cast<int>(std::min<long>(max_tiles, num_sms()));
+  const int grid = static_cast<int>(std::min<long>(max_blocks * n_ctiles, num_sms()));
   if (grid <= 0) return cudaSuccess;
   kern<<<grid, kTcThreads, Cfg::kSmemBytes, s>>>(map_w, map_src, src_rows, sorted_ids, expert_ids,
-                                                 n_post, topk_w, P, top_k, E, K, R_out, B, cap,
-                                                 tiles, a_out, y_acc, H_out, status);
+                                                 n_post, vec, P, top_k, E, K, R_out, a_rows, B, cap,
+                                                 n_ctiles, out16, y_acc, H_out, status);
   return cudaGetLastError();
 }
 
 template <int MODE>
-cudaError_t launch_tc(const CUtensorMap &map_w, const CUtensorMap &map_src, int src_rows,
+cudaError_t launch_tc(int N, const CUtensorMap &map_w, const CUtensorMap &map_src, int src_rows,
                       const int32_t *sorted_ids, const int32_t *expert_ids, const int32_t *n_post,
-                      const float *topk_w, int P, int top_k, int E, int K, int R_out, int B,
-                      int cap, uint16_t *a_out, float *y_acc, int H_out, int *status, int tiles,
-                      cudaStream_t s) {
-#define MOE_TC_CASE(NN)                                                                            \
-  case NN:                                                                                         \
-    return launch_tc_n<NN, MODE>(map_w, map_src, src_rows, sorted_ids, expert_ids, n_post, topk_w, \
-                                 P, top_k, E, K, R_out, B, cap, a_out, y_acc, H_out, status,      \
-                                 tiles, s)
-  switch (B) {
+                      const float *vec, int P, int top_k, int E, int K, int R_out, int a_rows, int B,
+                      int cap, uint16_t *out16, float *y_acc, int H_out, int *status, int n_ctiles,
+                      long max_blocks, cudaStream_t s) {
+#define MOE_TC_CASE(NN)                                                                          \
+  case NN:                                                                                       \
+    return launch_tc_n<NN, MODE>(map_w, map_src, src_rows, sorted_ids, expert_ids, n_post, vec, \
+                                 P, top_k, E, K, R_out, a_rows, B, cap, out16, y_acc, H_out,    \
+                                 status, n_ctiles, max_blocks, s)
+  switch (N) {
     MOE_TC_CASE(16);
     MOE_TC_CASE(32);
     MOE_TC_CASE(64);
@@ -540,9 +583,9 @@ cudaError_t launch_tc_w13_act(const uint16_t *x, const uint16_t *w13, const int3
   const int M = (P + top_k - 1) / top_k;
   err = make_row_map(&map_x, x, H, M);
   if (err != cudaSuccess) return err;
-  const int tiles = (I + kTileM - 1) / kTileM;
-  return launch_tc<0>(map_w, map_x, M, sorted_ids, expert_ids, n_post, nullptr, P, top_k, E, H, I,
-                      B, cap, a, nullptr, 0, status, tiles, s);
+  const int n_ctiles = (I + kTileM - 1) / kTileM;
+  return launch_tc<0>(B, map_w, map_x, M, sorted_ids, expert_ids, n_post, nullptr, P, top_k, E, H,
+                      I, 2 * I, B, cap, a, nullptr, 0, status, n_ctiles, cap / B, s);
 }
 
 cudaError_t launch_tc_w2_combine(const uint16_t *a, const uint16_t *w2, const int32_t *sorted_ids,
@@ -554,9 +597,22 @@ cudaError_t launch_tc_w2_combine(const uint16_t *a, const uint16_t *w2, const in
   if (err != cudaSuccess) return err;
   err = make_row_map(&map_a, a, I, P);
   if (err != cudaSuccess) return err;
-  const int tiles = (H + 2 * kTileM - 1) / (2 * kTileM);
-  return launch_tc<1>(map_w, map_a, P, sorted_ids, expert_ids, n_post, topk_weights, P, top_k, E,
-                      I, H, B, cap, nullptr, y_acc, H, status, tiles, s);
+  const int n_ctiles = (H + 2 * kTileM - 1) / (2 * kTileM);
+  return launch_tc<1>(B, map_w, map_a, P, sorted_ids, expert_ids, n_post, topk_weights, P, top_k,
+                      E, I, H, H, B, cap, nullptr, y_acc, H, status, n_ctiles, cap / B, s);
+}
+
+cudaError_t launch_tc_router(const uint16_t *x, const uint16_t *w_router, const float *bias, int M,
+                             int E, int H, uint16_t *logits, int *status, cudaStream_t s) {
+  CUtensorMap map_w, map_x;
+  cudaError_t err = make_weight_map(&map_w, w_router, H, E, 1);
+  if (err != cudaSuccess) return err;
+  err = make_row_map(&map_x, x, H, M);
+  if (err != cudaSuccess) return err;
+  const int N = 128;
+  const int n_ctiles = (E + 2 * kTileM - 1) / (2 * kTileM);
+  return launch_tc<2>(N, map_w, map_x, M, nullptr, nullptr, nullptr, bias, M, 1, 1, H, E, E, N, 0,
+                      logits, nullptr, 0, status, n_ctiles, (M + N - 1) / N, s);
 }
 
 }  // namespace moe

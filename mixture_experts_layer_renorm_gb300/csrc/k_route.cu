@@ -12,13 +12,15 @@ namespace moe {
 namespace {
 
 constexpr int kRouterTok = 8;        // tokens per CTA
-constexpr int kRouterWarps = 8;
-constexpr int kRouterExpPerCta = 16; // experts per CTA (2 per warp)
+constexpr int kRouterWarps = 8;      // one expert per warp
 constexpr int kRouterKChunk = 2048;  // x columns staged in shared memory at once
+constexpr int kRouterVec = kRouterKChunk / 8 / 32;  // 16-byte router loads per lane per chunk
 
-// One CTA: kRouterTok tokens x kRouterExpPerCta experts.  x rows are staged in
-// shared memory chunk by chunk; each warp streams one router row with 16-byte
-// loads and accumulates all staged tokens against it in fp32.
+// CUDA-core router for small batches: one CTA covers kRouterTok tokens and
+// kRouterWarps experts.  x rows are staged in shared memory chunk by chunk;
+// each warp issues all of its router row's loads for the chunk at once
+// (kRouterVec 16-byte loads per lane in flight), then accumulates every staged
+// token against them in fp32.  Large batches use the tensor-core router.
 __global__ void __launch_bounds__(kRouterWarps * 32)
 k_router_logits(const uint16_t *__restrict__ x, const uint16_t *__restrict__ w_router,
                 const float *__restrict__ bias, int M, int E, int H, uint16_t *__restrict__ logits) {
@@ -26,14 +28,10 @@ k_router_logits(const uint16_t *__restrict__ x, const uint16_t *__restrict__ w_r
   const int t0 = blockIdx.x * kRouterTok;
   const int nt = min(kRouterTok, M - t0);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int e_begin = blockIdx.y * kRouterExpPerCta;
-  const int e_end = min(E, e_begin + kRouterExpPerCta);
-  constexpr int kPerWarp = kRouterExpPerCta / kRouterWarps;
-  float acc[kPerWarp][kRouterTok];
+  const int e = blockIdx.y * kRouterWarps + warp;
+  float acc[kRouterTok];
 #pragma unroll
-  for (int r = 0; r < kPerWarp; ++r)
-#pragma unroll
-    for (int j = 0; j < kRouterTok; ++j) acc[r][j] = 0.f;
+  for (int j = 0; j < kRouterTok; ++j) acc[j] = 0.f;
 
   for (int kc = 0; kc < H; kc += kRouterKChunk) {
     const int kw = min(kRouterKChunk, H - kc);
@@ -46,40 +44,43 @@ k_router_logits(const uint16_t *__restrict__ x, const uint16_t *__restrict__ w_r
       xs[r * (kRouterKChunk / 8) + c] = val;
     }
     __syncthreads();
-#pragma unroll
-    for (int r = 0; r < kPerWarp; ++r) {
-      const int e = e_begin + warp + r * kRouterWarps;
-      if (e >= e_end) continue;
+    if (e < E) {
       const uint16_t *wrow = w_router + (size_t)e * H + kc;
-      for (int c = lane; c < vrow; c += 32) {
-        float wf[8];
-        bf16x8_to_float(ld_stream_16(wrow + c * 8), wf);
+      uint4 wv[kRouterVec];
 #pragma unroll
-        for (int j = 0; j < kRouterTok; ++j) {
-          float xf[8];
-          bf16x8_to_float(xs[j * (kRouterKChunk / 8) + c], xf);
+      for (int u = 0; u < kRouterVec; ++u) {
+        const int c = lane + 32 * u;
+        wv[u] = c < vrow ? ld_stream_16(wrow + c * 8) : make_uint4(0, 0, 0, 0);
+      }
 #pragma unroll
-          for (int q = 0; q < 8; ++q) acc[r][j] = fmaf(xf[q], wf[q], acc[r][j]);
+      for (int u = 0; u < kRouterVec; ++u) {
+        const int c = lane + 32 * u;
+        if (c < vrow) {
+          float wf[8];
+          bf16x8_to_float(wv[u], wf);
+#pragma unroll
+          for (int j = 0; j < kRouterTok; ++j) {
+            float xf[8];
+            bf16x8_to_float(xs[j * (kRouterKChunk / 8) + c], xf);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[j] = fmaf(xf[q], wf[q], acc[j]);
+          }
         }
       }
     }
   }
+  if (e >= E) return;
+  float mine = 0.f;
 #pragma unroll
-  for (int r = 0; r < kPerWarp; ++r) {
-    const int e = e_begin + warp + r * kRouterWarps;
-    if (e >= e_end) continue;
-    float mine = 0.f;
+  for (int j = 0; j < kRouterTok; ++j) {
+    float v = acc[j];
 #pragma unroll
-    for (int j = 0; j < kRouterTok; ++j) {
-      float v = acc[r][j];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      if (lane == j) mine = v;
-    }
-    if (lane < nt) {
-      if (bias != nullptr) mine += bias[e];
-      logits[(size_t)(t0 + lane) * E + e] = float_to_bf16_bits(mine);
-    }
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == j) mine = v;
+  }
+  if (lane < nt) {
+    if (bias != nullptr) mine += bias[e];
+    logits[(size_t)(t0 + lane) * E + e] = float_to_bf16_bits(mine);
   }
 }
 
@@ -158,7 +159,7 @@ k_topk_softmax(const uint16_t *__restrict__ logits, int M, int E, int top_k, int
 
 cudaError_t launch_router_logits(const uint16_t *x, const uint16_t *w_router, const float *bias,
                                  int M, int E, int H, uint16_t *logits, cudaStream_t s) {
-  dim3 grid((M + kRouterTok - 1) / kRouterTok, (E + kRouterExpPerCta - 1) / kRouterExpPerCta);
+  dim3 grid((M + kRouterTok - 1) / kRouterTok, (E + kRouterWarps - 1) / kRouterWarps);
   k_router_logits<<<grid, kRouterWarps * 32, 0, s>>>(x, w_router, bias, M, E, H, logits);
   return cudaGetLastError();
 }

@@ -120,6 +120,16 @@ int *lib_status() {
   return g_lib_status_ptr[dev];
 }
 
+// S0: the tensor-core router from 256 tokens up, the CUDA-core one below.
+constexpr int kTcRouterMinTokens = 256;
+
+moe_status_t run_router(const uint16_t *x, const uint16_t *w_router, const float *bias, int M,
+                        int E, int H, uint16_t *logits, int *status, cudaStream_t s) {
+  if (M >= kTcRouterMinTokens && forced_path() != 1)
+    return cuda_status(moe::launch_tc_router(x, w_router, bias, M, E, H, logits, status, s));
+  return cuda_status(moe::launch_router_logits(x, w_router, bias, M, E, H, logits, s));
+}
+
 moe_status_t run_gemm1(const uint16_t *x, const uint16_t *w13, const int32_t *sorted,
                        const int32_t *eids, const int32_t *npost, int M, int top_k, int E, int H,
                        int I, int B, uint16_t *a, int *status, cudaStream_t s) {
@@ -206,7 +216,7 @@ moe_status_t moe_router_logits(const moe_bf16_t *x, const moe_bf16_t *w_router,
   if (M == 0) return MOE_OK;
   if (!x || !w_router || !logits) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w_router)) return MOE_ERR_INVALID_ARG;
-  return cuda_status(moe::launch_router_logits(x, w_router, router_bias, M, E, H, logits, stream));
+  return run_router(x, w_router, router_bias, M, E, H, logits, lib_status(), stream);
 }
 
 moe_status_t moe_topk_softmax(const moe_bf16_t *logits, int M, int E, int top_k, int renormalize,
@@ -319,7 +329,7 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *w_router,
   const uint16_t *logits = router_logits;
   if (w_router) {
     uint16_t *lg = at<uint16_t>(ws, L.logits);
-    st = cuda_status(moe::launch_router_logits(x, w_router, router_bias, M, E, H, lg, stream));
+    st = run_router(x, w_router, router_bias, M, E, H, lg, status, stream);
     if (st != MOE_OK) return st;
     logits = lg;
   }

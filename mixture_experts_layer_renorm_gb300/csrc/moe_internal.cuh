@@ -95,6 +95,10 @@ cudaError_t launch_tc_w2_combine(const uint16_t *a, const uint16_t *w2, const in
                                  const float *topk_weights, int P, int top_k, int E, int H, int I,
                                  int B, int cap, float *y_acc, int *status, cudaStream_t s);
 
+// S0 on the tensor cores: logits [M,E] = bf16(x . w_router^T + bias), blocks of 128 tokens.
+cudaError_t launch_tc_router(const uint16_t *x, const uint16_t *w_router, const float *bias, int M,
+                             int E, int H, uint16_t *logits, int *status, cudaStream_t s);
+
 // y = bf16(y_acc + residual)
 cudaError_t launch_finalize(const float *y_acc, const uint16_t *residual, int M, int H, uint16_t *y,
                             cudaStream_t s);

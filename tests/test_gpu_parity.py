@@ -46,6 +46,14 @@ def tie_heavy_logits(M, E, seed):
     return levels[torch.randint(0, len(levels), (M, E), generator=g)].to(torch.bfloat16)
 
 
+@pytest.fixture(params=["tc", "gemv"])
+def gemm_path(request, monkeypatch):
+    """Runs a test once per implementation: the tensor-core kernels, and the
+    CUDA-core ones (MOE_FORCE_PATH=gemv) that serve shapes the former do not tile."""
+    monkeypatch.setenv("MOE_FORCE_PATH", request.param)
+    return request.param
+
+
 # ----------------------------------------------------------------------------- S0 router
 
 def check_logits(got_bits, x, wr, bias):
@@ -74,8 +82,10 @@ def check_logits(got_bits, x, wr, bias):
 
 @pytest.mark.parametrize("M,E,H,with_bias", [(3, 4, 128, False), (64, 128, 2048, False),
                                              (37, 256, 2048, False), (200, 33, 160, True),
-                                             (1, 128, 2048, True), (515, 128, 2048, True)])
-def test_router_logits(M, E, H, with_bias):
+                                             (1, 128, 2048, True), (515, 128, 2048, True),
+                                             (4096, 256, 2048, False), (300, 60, 2048, True),
+                                             (1000, 1024, 128, True)])
+def test_router_logits(M, E, H, with_bias, gemm_path):
     x = rand_bf16((M, H), 1.0, 11 + M)
     wr = rand_bf16((E, H), 0.02, 12 + E)
     bias = synth.zipf_router_bias(E, 1.1).to(DEV) if with_bias else None
@@ -200,14 +210,6 @@ GEMM_SHAPES = [(3, 4, 2, 128, 64, 16), (64, 128, 8, 2048, 768, 16), (64, 60, 4, 
                (33, 16, 3, 256, 160, 4), (200, 32, 4, 512, 96, 32), (128, 256, 8, 2048, 512, 16),
                (512, 128, 8, 2048, 768, 32), (1, 128, 8, 2048, 768, 16), (300, 8, 2, 192, 48, 64),
                (1000, 16, 4, 320, 208, 128), (700, 4, 2, 256, 128, 256), (40, 3, 3, 80, 16, 16)]
-
-
-@pytest.fixture(params=["tc", "gemv"])
-def gemm_path(request, monkeypatch):
-    """Runs a test once per grouped-GEMM implementation (tensor-core kernels for
-    block sizes 16..256, CUDA-core weight-streaming kernels otherwise)."""
-    monkeypatch.setenv("MOE_FORCE_PATH", request.param)
-    return request.param
 
 
 @pytest.mark.parametrize("M,E,k,H,I,B", GEMM_SHAPES)

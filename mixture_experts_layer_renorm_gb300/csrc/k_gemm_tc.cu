@@ -21,16 +21,17 @@
 //           epilogue: y_acc[t, n] += topk_weight[p] * D (fp32 red.add)
 //
 // Persistent CTAs (one per SM) walk the list of (block, weight tile) tiles.
-// Warp roles (192 threads): warp 0 loads -- one lane issues the TMA copies
-// of the two 128 x 64 weight tiles (128-byte swizzle) and each lane gathers
-// four of the block's rows with TMA tile::gather4 into the same swizzled
-// K-major layout; warp 1 allocates TMEM and one lane issues tcgen05.mma;
-// warps 2-5 are the epilogue, one TMEM lane quarter each (tcgen05.ld
-// 32x32b).  Two accumulator buffers in TMEM (while 4B fp32 columns fit) let
-// the epilogue of one tile overlap the mainloop of the next.  A ring of
-// shared-memory stages with full/empty mbarriers connects the roles.  Every
-// wait is bounded: after 2 s the kernel records MOE_ERR_DEVICE_TIMEOUT in the
-// status word, lets its own copies land and returns; it never traps.
+// Warp roles (320 threads): warp 0 -- one lane issues the TMA copies of the
+// two 128 x 64 weight tiles (128-byte swizzle); warps 6-9 gather the block's
+// rows with 16-byte cp.async into the same swizzled K-major layout (a TMA
+// instruction costs too much issue time per 512 bytes to gather with it);
+// warp 1 allocates TMEM and one lane issues tcgen05.mma; warps 2-5 are the
+// epilogue, one TMEM lane quarter each (tcgen05.ld 32x32b).  Two accumulator
+// buffers in TMEM (while 4B fp32 columns fit) let the epilogue of one tile
+// overlap the mainloop of the next.  A ring of shared-memory stages with
+// full/empty mbarriers connects the roles.  Every wait is bounded: after
+// about 2 s the kernel records MOE_ERR_DEVICE_TIMEOUT in the status word,
+// lets its own copies land and returns; it never traps.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -43,23 +44,20 @@ namespace moe {
 
 namespace {
 
-constexpr int kTcThreads = 192;
+constexpr int kGatherWarp0 = 6;                      // warps 6..9 gather the block's rows
+constexpr int kGatherThreads = 128;
+constexpr int kTcThreads = 192 + kGatherThreads;
 constexpr int kBK = 64;                              // K per stage: one 128-byte swizzle row
 constexpr int kTileM = 128;                          // weight rows per MMA
 constexpr uint32_t kATileBytes = kTileM * kBK * 2;   // 16 KB
 constexpr int kSmemBudget = 220 * 1024;
 constexpr int kMaxStages = 6;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;     // 2 s
+constexpr long long kWaitLimitCycles = 4000000000ll;  // about 2 s at the SM clock
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ uint64_t globaltimer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
 
 // ---------------------------------------------------------------- mbarrier
 
@@ -85,15 +83,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits for phase `parity` of the barrier; gives up after kWaitLimitNs (or
-// when another role already gave up), recording the timeout.
+// Waits for phase `parity` of the barrier; gives up after about 2 s of SM
+// clock (or when another role already gave up), recording the timeout.
 __device__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort, int *status) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
+  const long long t0 = clock64();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (clock64() - t0 > kWaitLimitCycles) {
       *abort = 1;
       report_status(status, kStatusTimeout);
       return false;
@@ -112,16 +112,19 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
-// Gathers four 128-byte rows (rows r0..r3, columns c0..c0+63 of a 2-D map
-// whose box is 64 x 1) into 512 consecutive bytes of shared memory, applying
-// the map's 128-byte swizzle; rows outside the tensor read as zero.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *map, int c0, int r0,
-                                            int r1, int r2, int r3, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
-      : "memory");
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// Makes this thread's completed generic-proxy writes to shared memory visible
+// to the async proxy (the tensor core reads operands through it).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05
@@ -207,11 +210,16 @@ struct TcConfig {
                                         : (kAccBufs * kAccCols <= 64) ? 64
                                         : (kAccBufs * kAccCols <= 128) ? 128
                                         : (kAccBufs * kAccCols <= 256) ? 256 : 512;
+  // a stage's row gathers may complete this many stages after they are issued
+  static constexpr int kLag = kStages - 1 < 3 ? kStages - 1 : 3;
+  // 16-byte chunks of one stage's gathered rows per gather thread
+  static constexpr int kChunksPerThread = N * 8 / kGatherThreads;
   // barriers: full[S], empty[S], acc_full[2], acc_empty[2]; tmem address,
-  // abort flag; producer rows[N]; epilogue destination rows[N], weights[N]
-  static constexpr uint32_t kCtlBytes = 8 * (2 * kStages + 4) + 16 + 12 * N;
+  // abort flag; epilogue destination rows[N], weights[N]
+  static constexpr uint32_t kCtlBytes = 8 * (2 * kStages + 4) + 16 + 8 * N;
   static constexpr uint32_t kSmemBytes = 1024 + kStages * kStageBytes + kCtlBytes;
   static_assert(kStages >= 3, "pipeline needs at least three stages");
+  static_assert(N * 8 % kGatherThreads == 0, "gather threads split a stage evenly");
 };
 
 __device__ __forceinline__ void epilogue_bar_sync() {
@@ -230,13 +238,14 @@ __device__ __forceinline__ void epilogue_bar_sync() {
 //                                 A = W_r rows e0..e0+255, logits[t, e] = bf16(D + bias[e])
 template <int N, int MODE>
 __global__ void __launch_bounds__(kTcThreads, 1)
-k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_src,
+k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict__ src,
           int src_rows, const int32_t *__restrict__ sorted_ids, const int32_t *__restrict__ expert_ids,
           const int32_t *__restrict__ n_post_ptr, const float *__restrict__ vec, int P, int top_k,
           int E, int K, int R_out, int a_rows, int B, int cap, int n_ctiles,
           uint16_t *__restrict__ out16, float *__restrict__ y_acc, int H_out, int *status) {
   using Cfg = TcConfig<N>;
   constexpr int S = Cfg::kStages;
+  constexpr int LAG = Cfg::kLag;
   int n_blocks;
   if (MODE == 2) {
     n_blocks = (src_rows + N - 1) / N;
@@ -258,14 +267,14 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CU
   uint64_t *acc_empty = bars + 2 * S + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 4);
   volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
-  int *rows = reinterpret_cast<int *>(tmem_slot + 4);        // producer's current block
-  int *dst_row = rows + N;                                   // epilogue's current block
+  int *dst_row = reinterpret_cast<int *>(tmem_slot + 4);     // epilogue's current block
   float *dst_w = reinterpret_cast<float *>(dst_row + N);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(smem_u32(&full[s]), 1);       // lane 0's expect_tx; the bytes complete it
+      // the weight lane's expect_tx + one (lagged) arrival per gather thread
+      mbar_init(smem_u32(&full[s]), 1 + kGatherThreads);
       mbar_init(smem_u32(&empty[s]), 1);      // one tcgen05.commit
     }
     for (int a = 0; a < 2; ++a) {
@@ -286,63 +295,95 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CU
   const int nk = (K + kBK - 1) / kBK;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ loads
-    // Lane 0 issues the weight tiles; lane L gathers rows 4q..4q+3 of the
-    // block for q = L, L+32, ... (tile::gather4), straight into the swizzled
-    // K-major layout.
-    int g = 0;  // stages issued by this CTA so far
-    bool stop = false;
-    for (int t = blockIdx.x; t < n_tiles && !stop; t += gridDim.x) {
-      const int b = t / n_ctiles, c = t - b * n_ctiles;
-      const int e = MODE == 2 ? 0 : expert_ids[b];
-      if (e < 0 || e >= E) continue;  // the MMA and epilogue skip this tile too
-      __syncwarp();
-      for (int j = lane; j < N; j += 32) {
-        int row = src_rows;  // past the end: reads as zero
-        if (MODE == 2) {
-          if (b * N + j < src_rows) row = b * N + j;
-        } else if (j < B) {
-          const int p = sorted_ids[(size_t)b * B + j];
-          if (p >= 0 && p < P) row = MODE == 0 ? p / top_k : p;
-        }
-        rows[j] = row;
-      }
-      __syncwarp();
-      const int row0 = MODE == 0 ? c * kTileM : c * 2 * kTileM;
-      const int row1 = MODE == 0 ? R_out + c * kTileM : c * 2 * kTileM + kTileM;
-      const bool two = MODE == 0 || row1 < a_rows;
-      const uint32_t stage_tx = (two ? 2 : 1) * kATileBytes + Cfg::kBStageBytes;
-      for (int kb = 0; kb < nk; ++kb, ++g) {
-        const int s = g % S;
-        const uint32_t ph = (g / S) & 1;
-        if (!wait_bounded(smem_u32(&empty[s]), ph ^ 1, abort, status)) {
-          stop = true;
-          break;
-        }
-        const uint32_t fb = smem_u32(&full[s]);
-        const uint32_t a_s = smem_u32(a_tiles + s * 2 * kATileBytes);
-        if (lane == 0) {
-          mbar_arrive_expect_tx(fb, stage_tx);
+    // ------------------------------------------------------------ weight tiles (TMA)
+    if (lane == 0) {
+      int g = 0;
+      bool stop = false;
+      for (int t = blockIdx.x; t < n_tiles && !stop; t += gridDim.x) {
+        const int b = t / n_ctiles, c = t - b * n_ctiles;
+        const int e = MODE == 2 ? 0 : expert_ids[b];
+        if (e < 0 || e >= E) continue;  // every role skips this tile
+        const int row0 = MODE == 0 ? c * kTileM : c * 2 * kTileM;
+        const int row1 = MODE == 0 ? R_out + c * kTileM : c * 2 * kTileM + kTileM;
+        const bool two = MODE == 0 || row1 < a_rows;
+        for (int kb = 0; kb < nk; ++kb, ++g) {
+          const int s = g % S;
+          if (!wait_bounded(smem_u32(&empty[s]), ((g / S) & 1) ^ 1, abort, status)) {
+            stop = true;
+            break;
+          }
+          const uint32_t fb = smem_u32(&full[s]);
+          const uint32_t a_s = smem_u32(a_tiles + s * 2 * kATileBytes);
+          mbar_arrive_expect_tx(fb, (two ? 2 : 1) * kATileBytes);
           tma_load_3d(a_s, &tmap_w, kb * kBK, row0, e, fb);
           if (two) tma_load_3d(a_s + kATileBytes, &tmap_w, kb * kBK, row1, e, fb);
         }
-        __syncwarp();
-        const uint32_t b_s = smem_u32(b_tiles + s * Cfg::kBStageBytes);
-#pragma unroll
-        for (int q4 = lane; q4 < N / 4; q4 += 32)
-          tma_gather4(b_s + q4 * 512, &tmap_src, kb * kBK, rows[4 * q4], rows[4 * q4 + 1],
-                      rows[4 * q4 + 2], rows[4 * q4 + 3], fb);
       }
-    }
-    // after an abort: let the copies already issued land before exit
-    if (*abort && lane == 0) {
-      for (int g2 = (g > S ? g - S : 0); g2 < g; ++g2) {
-        const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(smem_u32(&full[g2 % S]), (g2 / S) & 1) &&
-               globaltimer_ns() - t0 < kWaitLimitNs) {
+      // after an abort: let the copies already issued land before exit
+      if (*abort) {
+        for (int g2 = (g > S ? g - S : 0); g2 < g; ++g2) {
+          const long long t0 = clock64();
+          while (!mbar_try_wait(smem_u32(&full[g2 % S]), (g2 / S) & 1) &&
+                 clock64() - t0 < kWaitLimitCycles) {
+          }
         }
       }
     }
+    __syncwarp();
+  } else if (warp >= kGatherWarp0) {
+    // ------------------------------------------------------------ row gathers (cp.async)
+    // Thread gt copies chunk (gt & 7) -- 16 bytes of the stage's 128-byte K
+    // slice -- of rows gt/8, gt/8 + 16, ...; a stage's arrival trails by LAG
+    // stages so the thread never waits on its own latest copies.
+    const int gt = threadIdx.x - kGatherWarp0 * 32;
+    const int ch = gt & 7;
+    int g = 0;
+    bool stop = false;
+    for (int t = blockIdx.x; t < n_tiles && !stop; t += gridDim.x) {
+      const int b = t / n_ctiles;
+      const int e = MODE == 2 ? 0 : expert_ids[b];
+      if (e < 0 || e >= E) continue;
+      int rowv[Cfg::kChunksPerThread];
+#pragma unroll
+      for (int u = 0; u < Cfg::kChunksPerThread; ++u) {
+        const int r = (gt >> 3) + 16 * u;
+        int row = -1;
+        if (MODE == 2) {
+          if (b * N + r < src_rows) row = b * N + r;
+        } else if (r < B) {
+          const int p = sorted_ids[(size_t)b * B + r];
+          if (p >= 0 && p < P) row = MODE == 0 ? p / top_k : p;
+        }
+        rowv[u] = row;
+      }
+      for (int kb = 0; kb < nk; ++kb, ++g) {
+        const int s = g % S;
+        if (!wait_bounded(smem_u32(&empty[s]), ((g / S) & 1) ^ 1, abort, status)) {
+          stop = true;
+          break;
+        }
+        const uint32_t b_s = smem_u32(b_tiles + s * Cfg::kBStageBytes);
+        const int kel = kb * kBK + ch * 8;
+#pragma unroll
+        for (int u = 0; u < Cfg::kChunksPerThread; ++u) {
+          const int r = (gt >> 3) + 16 * u;
+          const bool ok = rowv[u] >= 0 && kel < K;
+          const uint16_t *gp = ok ? src + (size_t)rowv[u] * K + kel : src;
+          const uint32_t dst = b_s + (r >> 3) * 1024 + (r & 7) * 128 + ((ch ^ (r & 7)) << 4);
+          cp_async_16(dst, gp, ok ? 16u : 0u);
+        }
+        cp_async_commit();
+        if (g >= LAG) {
+          cp_async_wait<LAG>();
+          fence_proxy_async_smem();
+          mbar_arrive(smem_u32(&full[(g - LAG) % S]));
+        }
+      }
+    }
+    // the last stages' copies (and, after an abort, every copy still in flight)
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    for (int g2 = (g > LAG ? g - LAG : 0); g2 < g; ++g2) mbar_arrive(smem_u32(&full[g2 % S]));
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA
     if (lane == 0) {
@@ -421,8 +462,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CU
       if (!ok) break;
       const uint32_t d0 = tmem + lane_base + acc * Cfg::kAccCols;
       if (MODE == 0) {
-        const int ch = c * kTileM + q * 32 + lane;
-        const bool valid = ch < R_out;
+        const int chn = c * kTileM + q * 32 + lane;
+        const bool valid = chn < R_out;
 #pragma unroll 1
         for (int j0 = 0; j0 < N; j0 += 16) {
           uint32_t gt[16], up[16];
@@ -436,7 +477,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CU
               const float gb = bf16_bits_to_float(float_to_bf16_bits(__uint_as_float(gt[jj])));
               const float ub = bf16_bits_to_float(float_to_bf16_bits(__uint_as_float(up[jj])));
               const float silu = gb / (1.0f + expf(-gb));
-              out16[(size_t)p * R_out + ch] = float_to_bf16_bits(silu * ub);
+              out16[(size_t)p * R_out + chn] = float_to_bf16_bits(silu * ub);
             }
           }
         }
@@ -509,24 +550,8 @@ cudaError_t make_weight_map(CUtensorMap *map, const uint16_t *w, int K, int rows
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// 2-D map over gathered rows [rows][K] (bf16, K contiguous), box 64 x 1 (one
-// row high, as tile::gather4 requires), 128-byte swizzle.
-cudaError_t make_row_map(CUtensorMap *map, const uint16_t *base, int K, int rows) {
-  PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode_fn();
-  if (encode == nullptr) return cudaErrorNotSupported;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-  const cuuint32_t box[2] = {kBK, 1};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(base),
-                            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
 template <int N, int MODE>
-cudaError_t launch_tc_n(const CUtensorMap &map_w, const CUtensorMap &map_src, int src_rows,
+cudaError_t launch_tc_n(const CUtensorMap &map_w, const uint16_t *src, int src_rows,
                         const int32_t *sorted_ids, const int32_t *expert_ids, const int32_t *n_post,
                         const float *vec, int P, int top_k, int E, int K, int R_out, int a_rows,
                         int B, int cap, uint16_t *out16, float *y_acc, int H_out, int *status,
@@ -540,21 +565,21 @@ cudaError_t launch_tc_n(const CUtensorMap &map_w, const CUtensorMap &map_src, in
   // persistent: one CTA per SM at most, each walking the tile list with stride gridDim.x
   const int grid = static_cast<int>(std::min<long>(max_blocks * n_ctiles, num_sms()));
   if (grid <= 0) return cudaSuccess;
-  kern<<<grid, kTcThreads, Cfg::kSmemBytes, s>>>(map_w, map_src, src_rows, sorted_ids, expert_ids,
+  kern<<<grid, kTcThreads, Cfg::kSmemBytes, s>>>(map_w, src, src_rows, sorted_ids, expert_ids,
                                                  n_post, vec, P, top_k, E, K, R_out, a_rows, B, cap,
                                                  n_ctiles, out16, y_acc, H_out, status);
   return cudaGetLastError();
 }
 
 template <int MODE>
-cudaError_t launch_tc(int N, const CUtensorMap &map_w, const CUtensorMap &map_src, int src_rows,
+cudaError_t launch_tc(int N, const CUtensorMap &map_w, const uint16_t *src, int src_rows,
                       const int32_t *sorted_ids, const int32_t *expert_ids, const int32_t *n_post,
                       const float *vec, int P, int top_k, int E, int K, int R_out, int a_rows, int B,
                       int cap, uint16_t *out16, float *y_acc, int H_out, int *status, int n_ctiles,
                       long max_blocks, cudaStream_t s) {
 #define MOE_TC_CASE(NN)                                                                          \
   case NN:                                                                                       \
-    return launch_tc_n<NN, MODE>(map_w, map_src, src_rows, sorted_ids, expert_ids, n_post, vec, \
+    return launch_tc_n<NN, MODE>(map_w, src, src_rows, sorted_ids, expert_ids, n_post, vec,     \
                                  P, top_k, E, K, R_out, a_rows, B, cap, out16, y_acc, H_out,    \
                                  status, n_ctiles, max_blocks, s)
   switch (N) {
@@ -577,14 +602,12 @@ cudaError_t launch_tc_w13_act(const uint16_t *x, const uint16_t *w13, const int3
                               const int32_t *expert_ids, const int32_t *n_post, int P, int top_k,
                               int E, int H, int I, int B, int cap, uint16_t *a, int *status,
                               cudaStream_t s) {
-  CUtensorMap map_w, map_x;
+  CUtensorMap map_w;
   cudaError_t err = make_weight_map(&map_w, w13, H, 2 * I, E);
   if (err != cudaSuccess) return err;
   const int M = (P + top_k - 1) / top_k;
-  err = make_row_map(&map_x, x, H, M);
-  if (err != cudaSuccess) return err;
   const int n_ctiles = (I + kTileM - 1) / kTileM;
-  return launch_tc<0>(B, map_w, map_x, M, sorted_ids, expert_ids, n_post, nullptr, P, top_k, E, H,
+  return launch_tc<0>(B, map_w, x, M, sorted_ids, expert_ids, n_post, nullptr, P, top_k, E, H,
                       I, 2 * I, B, cap, a, nullptr, 0, status, n_ctiles, cap / B, s);
 }
 
@@ -592,26 +615,22 @@ cudaError_t launch_tc_w2_combine(const uint16_t *a, const uint16_t *w2, const in
                                  const int32_t *expert_ids, const int32_t *n_post,
                                  const float *topk_weights, int P, int top_k, int E, int H, int I,
                                  int B, int cap, float *y_acc, int *status, cudaStream_t s) {
-  CUtensorMap map_w, map_a;
+  CUtensorMap map_w;
   cudaError_t err = make_weight_map(&map_w, w2, I, H, E);
   if (err != cudaSuccess) return err;
-  err = make_row_map(&map_a, a, I, P);
-  if (err != cudaSuccess) return err;
   const int n_ctiles = (H + 2 * kTileM - 1) / (2 * kTileM);
-  return launch_tc<1>(B, map_w, map_a, P, sorted_ids, expert_ids, n_post, topk_weights, P, top_k,
+  return launch_tc<1>(B, map_w, a, P, sorted_ids, expert_ids, n_post, topk_weights, P, top_k,
                       E, I, H, H, B, cap, nullptr, y_acc, H, status, n_ctiles, cap / B, s);
 }
 
 cudaError_t launch_tc_router(const uint16_t *x, const uint16_t *w_router, const float *bias, int M,
                              int E, int H, uint16_t *logits, int *status, cudaStream_t s) {
-  CUtensorMap map_w, map_x;
+  CUtensorMap map_w;
   cudaError_t err = make_weight_map(&map_w, w_router, H, E, 1);
-  if (err != cudaSuccess) return err;
-  err = make_row_map(&map_x, x, H, M);
   if (err != cudaSuccess) return err;
   const int N = 128;
   const int n_ctiles = (E + 2 * kTileM - 1) / (2 * kTileM);
-  return launch_tc<2>(N, map_w, map_x, M, nullptr, nullptr, nullptr, bias, M, 1, 1, H, E, E, N, 0,
+  return launch_tc<2>(N, map_w, x, M, nullptr, nullptr, nullptr, bias, M, 1, 1, H, E, E, N, 0,
                       logits, nullptr, 0, status, n_ctiles, (M + N - 1) / N, s);
 }
 

@@ -52,6 +52,7 @@ constexpr int kTileM = 128;                          // weight rows per MMA
 constexpr uint32_t kATileBytes = kTileM * kBK * 2;   // 16 KB
 constexpr int kSmemBudget = 220 * 1024;
 constexpr int kMaxStages = 6;
+constexpr int kPrefetchStages = 8;                   // weight stages requested into L2 ahead of their load
 constexpr long long kWaitLimitCycles = 4000000000ll;  // about 2 s at the SM clock
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -110,6 +111,14 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
       : "memory");
+}
+
+// Asks the TMA unit to bring a 3-D box into L2 (no shared memory involved).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap *map, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
 }
 
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes) {
@@ -297,6 +306,34 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
   if (warp == 0) {
     // ------------------------------------------------------------ weight tiles (TMA)
     if (lane == 0) {
+      // A second cursor walks the same stage sequence kPrefetchStages ahead
+      // and asks for those weight boxes to be brought into L2, so that most
+      // loads find their data there (the ring holds only a few stages).
+      int pt = blockIdx.x, pkb = 0, pe = -1, pr0 = 0, pr1 = 0;
+      bool ptwo = false;
+      auto pf_seek = [&]() {
+        for (; pt < n_tiles; pt += gridDim.x) {
+          const int b = pt / n_ctiles, c = pt - b * n_ctiles;
+          pe = MODE == 2 ? 0 : expert_ids[b];
+          if (pe < 0 || pe >= E) continue;
+          pr0 = MODE == 0 ? c * kTileM : c * 2 * kTileM;
+          pr1 = MODE == 0 ? R_out + c * kTileM : c * 2 * kTileM + kTileM;
+          ptwo = MODE == 0 || pr1 < a_rows;
+          return;
+        }
+      };
+      auto pf_step = [&]() {
+        if (pt >= n_tiles) return;
+        tma_prefetch_l2_3d(&tmap_w, pkb * kBK, pr0, pe);
+        if (ptwo) tma_prefetch_l2_3d(&tmap_w, pkb * kBK, pr1, pe);
+        if (++pkb == nk) {
+          pkb = 0;
+          pt += gridDim.x;
+          pf_seek();
+        }
+      };
+      pf_seek();
+      for (int k2 = 0; k2 < kPrefetchStages; ++k2) pf_step();
       int g = 0;
       bool stop = false;
       for (int t = blockIdx.x; t < n_tiles && !stop; t += gridDim.x) {
@@ -317,6 +354,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
           mbar_arrive_expect_tx(fb, (two ? 2 : 1) * kATileBytes);
           tma_load_3d(a_s, &tmap_w, kb * kBK, row0, e, fb);
           if (two) tma_load_3d(a_s + kATileBytes, &tmap_w, kb * kBK, row1, e, fb);
+          pf_step();
         }
       }
       // after an abort: let the copies already issued land before exit

@@ -52,7 +52,6 @@ constexpr int kTileM = 128;                          // weight rows per MMA
 constexpr uint32_t kATileBytes = kTileM * kBK * 2;   // 16 KB
 constexpr int kSmemBudget = 220 * 1024;
 constexpr int kMaxStages = 6;
-constexpr int kPrefetchStages = 8;                   // weight stages requested into L2 ahead of their load
 constexpr long long kWaitLimitCycles = 4000000000ll;  // about 2 s at the SM clock
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -113,25 +112,22 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
-// Asks the TMA unit to bring a 3-D box into L2 (no shared memory involved).
-__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap *map, int c0, int c1, int c2) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(c0), "r"(c1), "r"(c2)
-               : "memory");
-}
-
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
                : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
-// Makes this thread's completed generic-proxy writes to shared memory visible
-// to the async proxy (the tensor core reads operands through it).
+// Arrives on the barrier once every cp.async this thread issued so far has
+// landed; the barrier's expected count already includes this arrival.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+// Orders shared-memory writes made through the generic proxy (the row
+// gathers), which this thread has observed through an mbarrier, before its
+// following async-proxy accesses (the tensor core's operand reads).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -219,8 +215,6 @@ struct TcConfig {
                                         : (kAccBufs * kAccCols <= 64) ? 64
                                         : (kAccBufs * kAccCols <= 128) ? 128
                                         : (kAccBufs * kAccCols <= 256) ? 256 : 512;
-  // a stage's row gathers may complete this many stages after they are issued
-  static constexpr int kLag = kStages - 1 < 3 ? kStages - 1 : 3;
   // 16-byte chunks of one stage's gathered rows per gather thread
   static constexpr int kChunksPerThread = N * 8 / kGatherThreads;
   // barriers: full[S], empty[S], acc_full[2], acc_empty[2]; tmem address,
@@ -254,7 +248,6 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
           uint16_t *__restrict__ out16, float *__restrict__ y_acc, int H_out, int *status) {
   using Cfg = TcConfig<N>;
   constexpr int S = Cfg::kStages;
-  constexpr int LAG = Cfg::kLag;
   int n_blocks;
   if (MODE == 2) {
     n_blocks = (src_rows + N - 1) / N;
@@ -282,7 +275,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      // the weight lane's expect_tx + one (lagged) arrival per gather thread
+      // the weight lane's expect_tx + one cp.async-completion arrival per gather thread
       mbar_init(smem_u32(&full[s]), 1 + kGatherThreads);
       mbar_init(smem_u32(&empty[s]), 1);      // one tcgen05.commit
     }
@@ -306,34 +299,6 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
   if (warp == 0) {
     // ------------------------------------------------------------ weight tiles (TMA)
     if (lane == 0) {
-      // A second cursor walks the same stage sequence kPrefetchStages ahead
-      // and asks for those weight boxes to be brought into L2, so that most
-      // loads find their data there (the ring holds only a few stages).
-      int pt = blockIdx.x, pkb = 0, pe = -1, pr0 = 0, pr1 = 0;
-      bool ptwo = false;
-      auto pf_seek = [&]() {
-        for (; pt < n_tiles; pt += gridDim.x) {
-          const int b = pt / n_ctiles, c = pt - b * n_ctiles;
-          pe = MODE == 2 ? 0 : expert_ids[b];
-          if (pe < 0 || pe >= E) continue;
-          pr0 = MODE == 0 ? c * kTileM : c * 2 * kTileM;
-          pr1 = MODE == 0 ? R_out + c * kTileM : c * 2 * kTileM + kTileM;
-          ptwo = MODE == 0 || pr1 < a_rows;
-          return;
-        }
-      };
-      auto pf_step = [&]() {
-        if (pt >= n_tiles) return;
-        tma_prefetch_l2_3d(&tmap_w, pkb * kBK, pr0, pe);
-        if (ptwo) tma_prefetch_l2_3d(&tmap_w, pkb * kBK, pr1, pe);
-        if (++pkb == nk) {
-          pkb = 0;
-          pt += gridDim.x;
-          pf_seek();
-        }
-      };
-      pf_seek();
-      for (int k2 = 0; k2 < kPrefetchStages; ++k2) pf_step();
       int g = 0;
       bool stop = false;
       for (int t = blockIdx.x; t < n_tiles && !stop; t += gridDim.x) {
@@ -354,7 +319,6 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
           mbar_arrive_expect_tx(fb, (two ? 2 : 1) * kATileBytes);
           tma_load_3d(a_s, &tmap_w, kb * kBK, row0, e, fb);
           if (two) tma_load_3d(a_s + kATileBytes, &tmap_w, kb * kBK, row1, e, fb);
-          pf_step();
         }
       }
       // after an abort: let the copies already issued land before exit
@@ -371,8 +335,9 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
   } else if (warp >= kGatherWarp0) {
     // ------------------------------------------------------------ row gathers (cp.async)
     // Thread gt copies chunk (gt & 7) -- 16 bytes of the stage's 128-byte K
-    // slice -- of rows gt/8, gt/8 + 16, ...; a stage's arrival trails by LAG
-    // stages so the thread never waits on its own latest copies.
+    // slice -- of rows gt/8, gt/8 + 16, ...; the hardware arrives on the
+    // stage's full barrier for it when those copies land, so the thread moves
+    // straight on to the next stage.
     const int gt = threadIdx.x - kGatherWarp0 * 32;
     const int ch = gt & 7;
     int g = 0;
@@ -410,18 +375,10 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
           const uint32_t dst = b_s + (r >> 3) * 1024 + (r & 7) * 128 + ((ch ^ (r & 7)) << 4);
           cp_async_16(dst, gp, ok ? 16u : 0u);
         }
-        cp_async_commit();
-        if (g >= LAG) {
-          cp_async_wait<LAG>();
-          fence_proxy_async_smem();
-          mbar_arrive(smem_u32(&full[(g - LAG) % S]));
-        }
+        cp_async_arrive_noinc(smem_u32(&full[s]));
       }
     }
-    // the last stages' copies (and, after an abort, every copy still in flight)
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
-    for (int g2 = (g > LAG ? g - LAG : 0); g2 < g; ++g2) mbar_arrive(smem_u32(&full[g2 % S]));
+    cp_async_wait<0>();  // nothing of ours still in flight at exit
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA
     if (lane == 0) {
@@ -445,6 +402,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
             stop = true;
             break;
           }
+          fence_proxy_async_smem();  // the gathered rows were written by cp.async
           tc_fence_after();
           const uint32_t a0 = smem_u32(a_tiles + s * 2 * kATileBytes);
           const uint32_t a1 = a0 + kATileBytes;

@@ -322,6 +322,117 @@ def cpu_baseline(w, L, budget_s=12.0):
             "sample": f"{n} x {w.name} layer on {sample_tokens} tokens (full expert weights), {dt:.1f} s"}
 
 
+# ----------------------------------------------------------------------------- the 64-layer stack
+
+class Stack:
+    """The 64-layer decode stack: independent seeded weights per layer, layer
+    l+1 reads y_l (computed with residual x_l), one workspace for every layer."""
+
+    def __init__(self, moe, w, M, n_inputs, device):
+        self.w, self.M = w, M
+        self.layers = [synth.layer_weights(w, layer=l, device=device) for l in range(w.layers)]
+        self.inputs = [synth.layer_input(w, M, rep=r, device=device)["x"] for r in range(n_inputs)]
+        self.B = w.block_size_m or moe.moe_pick_block_size(M, w.E, w.top_k, w.H, w.I)
+        self.ws = moe.Workspace(M, w.E, w.top_k, w.H, w.I, 0, device=device)
+        self.buf = [torch.empty((M, w.H), dtype=torch.bfloat16, device=device) for _ in range(2)]
+        self.ids = [torch.empty((M, w.top_k), dtype=torch.int32, device=device)
+                    for _ in range(w.layers)]
+
+    def kernels_per_step(self):
+        align = 1 if self.M * self.w.top_k <= 16384 else 2
+        return self.w.layers * (1 + 1 + align + 1 + 2)
+
+    def step(self, moe, x, stream, keep_ids=False):
+        """x (held in buf[0]) through every layer; returns the output buffer."""
+        w = self.w
+        cur, nxt = self.buf[0], self.buf[1]
+        if x is not cur:
+            cur.copy_(x, non_blocking=True)
+        for l, wt in enumerate(self.layers):
+            moe.moe_forward(cur, wt["w13"], wt["w2"], w.top_k, nxt, self.ws, w_router=wt["w_router"],
+                            router_bias=wt["router_bias"], residual=cur, renormalize=w.renormalize,
+                            block_size_m=self.B, topk_ids_out=self.ids[l] if keep_ids else None,
+                            stream=stream)
+            cur, nxt = nxt, cur  # ping-pong: a layer's input is dead once its output exists
+        return cur
+
+
+def stack_bytes(w, M, distinct_per_layer):
+    return sum(layer_bytes(w, M, d) for d in distinct_per_layer)
+
+
+def run_stack(moe, args, w, M, device, stream, flush, world):
+    S = Stack(moe, w, M, args.warmup + args.steps, device)
+    torch.cuda.synchronize()
+    graph = None
+    if args.graph:
+        # capture one step (64 layers) reading buf[0]; replay it per step
+        with torch.cuda.stream(stream):
+            S.step(moe, S.buf[0], stream)  # first calls do per-device set-up outside the capture
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            out_buf = S.step(moe, S.buf[0], stream)
+    times = []
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(device) as clk:
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup + args.steps):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                if graph is not None:
+                    S.buf[0].copy_(S.inputs[i], non_blocking=True)
+                    graph.replay()
+                else:
+                    S.step(moe, S.inputs[i], stream)
+                e1.record(stream)
+                if i >= args.warmup:
+                    times.append((e0, e1))
+        stream.synchronize()
+    torch.cuda.synchronize()
+    barrier(world)
+    step_ms = [a.elapsed_time(b) for a, b in times]
+    # distinct experts per layer of the last step's routing, for the byte count
+    with torch.cuda.stream(stream):
+        S.step(moe, S.inputs[-1], stream, keep_ids=True)
+    stream.synchronize()
+    D = [int(torch.unique(ids).numel()) for ids in S.ids]
+    return S, step_ms, D, clk
+
+
+def ours_stack(args, moe, w, M, device, stream, flush, world, rank, peaks):
+    S, step_ms, D, clk = run_stack(moe, args, w, M, device, stream, flush, world)
+    total_ms = max_over_ranks(sum(step_ms), world, device)
+    ms_per_step = total_ms / args.steps
+    value = world * M * args.steps / (total_ms / 1e3)
+    sb = stack_bytes(w, M, D)
+    gbs = sb / (ms_per_step / 1e3) / 1e9
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: seeded x ~ N(0,1), 64 layers of weights ~ N(0,0.02), bf16; new x every step",
+        "config": {"workload": f"{w.name}_m{M}", "M": M, "E": w.E, "top_k": w.top_k, "H": w.H,
+                   "I": w.I, "layers": w.layers, "block_size_m": S.B, "residual": True,
+                   "cuda_graph": bool(args.graph),
+                   "l2": f"flushed between steps ({args.flush_mb} MB write, outside the events)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"kernel": "whole 64-layer step", "bound": "hbm", "achieved": round(gbs, 1),
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                     "traffic": None, "peak_source": peaks["source"], "algorithmic_bytes": int(sb)},
+        "distinct_experts_per_layer": round(statistics.mean(D), 2),
+        "e2e": None, "cpu_baseline": None,
+        "gpu_launches": S.kernels_per_step() * args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
+
 def ours(args):
     import mixture_experts_layer_renorm_gb300 as moe
     world, rank, local = dist_env()
@@ -336,6 +447,9 @@ def ours(args):
     peaks = load_peaks()
     stream = torch.cuda.Stream(device=device)
     flush = torch.empty(args.flush_mb << 20, dtype=torch.uint8, device=device)
+    if w.layers > 1:
+        ours_stack(args, moe, w, M, device, stream, flush, world, rank, peaks)
+        return
 
     L = Layer(moe, w, M, args.warmup + args.steps, device)
     # the timed region: K steps, barrier + synchronize on both sides
@@ -487,6 +601,8 @@ def main(argv=None):
     ap.add_argument("--no-points", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-tokens", type=int, default=64)
+    ap.add_argument("--graph", action="store_true",
+                    help="stack workload: replay each 64-layer step from a CUDA graph")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     if args.impl == "reference":

@@ -327,3 +327,56 @@ def test_forward_full_size_sampled(cfg, M):
                              wt["w_router"], wt["router_bias"])
     # routing is complete: every token has top_k distinct experts
     assert (np.sort(ids, axis=1)[:, 1:] != np.sort(ids, axis=1)[:, :-1]).all()
+
+
+# ----------------------------------------------------------------------------- the 64-layer stack
+
+def test_stack_chain_against_the_oracle_on_sampled_tokens():
+    """The 256-expert, 64-layer decode stack: layer l+1 reads y_l computed with
+    residual x_l.  The GPU runs all M=16 tokens through every layer; the oracle
+    chains 3 sampled tokens through the same layers on its own (each token is
+    independent), copying only the experts it routes to.  Each sampled token
+    must route identically and match y layer by layer until its first routing
+    difference, which must come with a differently rounded logit."""
+    w = synth.WORKLOADS[4]
+    M, sample = 16, [0, 7, 13]
+    x0 = synth.layer_input(w, M, device=DEV)["x"]
+    ws = moe.Workspace(M, w.E, w.top_k, w.H, w.I, 0)
+    cur = x0.clone()
+    ox = bits(x0)[sample]
+    live = np.ones(len(sample), bool)
+    compared = 0
+    for l in range(w.layers):
+        wt = synth.layer_weights(w, layer=l, device=DEV)
+        y = torch.empty_like(cur)
+        ids = torch.empty((M, w.top_k), dtype=torch.int32, device=DEV)
+        lg = torch.empty((M, w.E), dtype=torch.bfloat16, device=DEV)
+        moe.moe_router_logits(cur, wt["w_router"], lg)
+        moe.moe_forward(cur, wt["w13"], wt["w2"], w.top_k, y, ws, w_router=wt["w_router"],
+                        residual=cur, topk_ids_out=ids)
+        torch.cuda.synchronize()
+        g_y, g_ids, g_lg = bits(y)[sample], ids.cpu().numpy()[sample], bits(lg)[sample]
+        # the oracle's own chain for the sampled tokens
+        o_lg = oracle.router_logits(ox, bits(wt["w_router"]))
+        o_ids, o_w = oracle.topk_softmax(o_lg, w.top_k)
+        used = np.unique(o_ids)
+        idx = torch.from_numpy(used.astype(np.int64)).to(DEV)
+        w13 = np.zeros((w.E, 2 * w.I, w.H), np.uint16)
+        w2 = np.zeros((w.E, w.H, w.I), np.uint16)
+        w13[used] = bits(wt["w13"].index_select(0, idx))
+        w2[used] = bits(wt["w2"].index_select(0, idx))
+        a = oracle.expert_act(ox, w13, o_ids)
+        oy = oracle.expert_down_combine(a, w2, o_ids, o_w, residual=ox)
+        for s_i in range(len(sample)):
+            if not live[s_i]:
+                continue
+            if not np.array_equal(o_ids[s_i], g_ids[s_i]):
+                assert (o_lg[s_i] != g_lg[s_i]).any(), f"layer {l}: routing differs, logits equal"
+                live[s_i] = False
+                continue
+            assert_close_bf16(g_y[s_i:s_i + 1], oy[s_i:s_i + 1], f"y layer {l} token {sample[s_i]}")
+            compared += 1
+        ox, cur = oy, y
+        del wt
+    assert moe.moe_get_device_status(ws) == 0
+    assert compared >= 0.5 * w.layers * len(sample), f"only {compared} (token, layer) pairs compared"

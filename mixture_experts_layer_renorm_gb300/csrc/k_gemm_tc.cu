@@ -21,12 +21,13 @@
 //           epilogue: y_acc[t, n] += topk_weight[p] * D (fp32 red.add)
 //
 // Persistent CTAs (one per SM) walk the list of (block, weight tile) tiles.
-// Warp roles (320 threads): warp 0 -- one lane issues the TMA copies of the
-// two 128 x 64 weight tiles (128-byte swizzle); warps 6-9 gather the block's
+// Warp roles (448 threads): warp 0 -- one lane issues the TMA copies of the
+// two 128 x 64 weight tiles (128-byte swizzle); warps 10-13 gather the block's
 // rows with 16-byte cp.async into the same swizzled K-major layout (a TMA
 // instruction costs too much issue time per 512 bytes to gather with it);
-// warp 1 allocates TMEM and one lane issues tcgen05.mma; warps 2-5 are the
-// epilogue, one TMEM lane quarter each (tcgen05.ld 32x32b).  Two accumulator
+// warp 1 allocates TMEM and one lane issues tcgen05.mma; warps 2-9 are the
+// epilogue, two per TMEM lane quarter splitting its columns (tcgen05.ld
+// 32x32b).  Waiting threads sleep in mbarrier.try_wait rather than spin.  Two accumulator
 // buffers in TMEM (while 4B fp32 columns fit) let the epilogue of one tile
 // overlap the mainloop of the next.  A ring of shared-memory stages with
 // full/empty mbarriers connects the roles.  Every wait is bounded: after
@@ -44,15 +45,18 @@ namespace moe {
 
 namespace {
 
-constexpr int kGatherWarp0 = 6;                      // warps 6..9 gather the block's rows
+constexpr int kEpiWarps = 8;                         // warps 2..9: two per TMEM lane quarter
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kGatherWarp0 = 2 + kEpiWarps;          // warps 10..13 gather the block's rows
 constexpr int kGatherThreads = 128;
-constexpr int kTcThreads = 192 + kGatherThreads;
+constexpr int kTcThreads = 64 + kEpiThreads + kGatherThreads;
 constexpr int kBK = 64;                              // K per stage: one 128-byte swizzle row
 constexpr int kTileM = 128;                          // weight rows per MMA
 constexpr uint32_t kATileBytes = kTileM * kBK * 2;   // 16 KB
 constexpr int kSmemBudget = 220 * 1024;
 constexpr int kMaxStages = 6;
 constexpr long long kWaitLimitCycles = 4000000000ll;  // about 2 s at the SM clock
+constexpr uint32_t kSuspendHintNs = 20000;           // a waiting thread sleeps until the phase completes
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -82,6 +86,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// As mbar_try_wait, but the thread may stay suspended (off the issue slots the
+// other roles need) for up to kSuspendHintNs unless the phase completes first.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "n"(kSuspendHintNs)
+      : "memory");
+  return ok != 0;
+}
 
 // Waits for phase `parity` of the barrier; gives up after about 2 s of SM
 // clock (or when another role already gave up), recording the timeout.
@@ -91,7 +108,7 @@ __device__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort,
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 16; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+      if (mbar_try_wait_sleep(bar, parity)) return true;
     if (*abort) return false;
     if (clock64() - t0 > kWaitLimitCycles) {
       *abort = 1;
@@ -226,7 +243,7 @@ struct TcConfig {
 };
 
 __device__ __forceinline__ void epilogue_bar_sync() {
-  asm volatile("bar.sync 1, 128;" ::: "memory");  // the four epilogue warps only
+  asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");  // the epilogue warps only
 }
 
 // Persistent tiles: tile t = (block t / n_ctiles, weight tile t % n_ctiles);
@@ -281,7 +298,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&acc_full[a]), 1);   // one tcgen05.commit
-      mbar_init(smem_u32(&acc_empty[a]), 4);  // one arrive per epilogue warp
+      mbar_init(smem_u32(&acc_empty[a]), kEpiWarps);  // one arrive per epilogue warp
     }
     *abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -423,7 +440,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const int et = threadIdx.x - 64;  // 0..127 over the four epilogue warps
+    const int half = (warp - 2) >> 2;  // the two warps of a quarter split the column chunks
+    const int et = threadIdx.x - 64;   // 0..255 over the epilogue warps
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     int i = 0;
     for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
@@ -436,7 +454,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
       ++i;
       // the block's destinations (and router weights), staged while the MMAs run
       epilogue_bar_sync();  // the previous tile's readers are done
-      for (int j = et; j < N; j += 128) {
+      for (int j = et; j < N; j += kEpiThreads) {
         int d = -1;
         float wgt = 0.f;
         if (MODE == 2) {
@@ -461,7 +479,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
         const int chn = c * kTileM + q * 32 + lane;
         const bool valid = chn < R_out;
 #pragma unroll 1
-        for (int j0 = 0; j0 < N; j0 += 16) {
+        for (int j0 = 16 * half; j0 < N; j0 += 32) {
           uint32_t gt[16], up[16];
           tmem_ld_32x32b_x16(d0 + j0, gt);
           tmem_ld_32x32b_x16(d0 + N + j0, up);
@@ -472,19 +490,21 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
             if (valid && p >= 0) {
               const float gb = bf16_bits_to_float(float_to_bf16_bits(__uint_as_float(gt[jj])));
               const float ub = bf16_bits_to_float(float_to_bf16_bits(__uint_as_float(up[jj])));
-              const float silu = gb / (1.0f + expf(-gb));
+              const float silu = gb * __frcp_rn(1.0f + expf(-gb));
               out16[(size_t)p * R_out + chn] = float_to_bf16_bits(silu * ub);
             }
           }
         }
       } else {
+        // work items (h, chunk of 16 columns), alternating between the two warps of a quarter
+        const int n_chunks = N / 16;
 #pragma unroll 1
-        for (int h = 0; h < (two ? 2 : 1); ++h) {
+        for (int item = half; item < (two ? 2 : 1) * n_chunks; item += 2) {
+          const int h = item / n_chunks, j0 = (item - h * n_chunks) * 16;
           const int n = c * 2 * kTileM + h * kTileM + q * 32 + lane;
           const bool valid = n < (MODE == 1 ? H_out : a_rows);
           const float bias = (MODE == 2 && valid && vec != nullptr) ? vec[n] : 0.f;
-#pragma unroll 1
-          for (int j0 = 0; j0 < N; j0 += 16) {
+          {
             uint32_t o[16];
             tmem_ld_32x32b_x16(d0 + h * N + j0, o);
             tmem_ld_wait();
@@ -501,7 +521,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
           }
         }
       }
-      // this accumulator buffer may be overwritten once all four warps are done with it
+      // this accumulator buffer may be overwritten once all epilogue warps are done with it
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&acc_empty[acc]));

@@ -337,15 +337,27 @@ def test_stack_chain_against_the_oracle_on_sampled_tokens():
     chains 3 sampled tokens through the same layers on its own (each token is
     independent), copying only the experts it routes to.  Each sampled token
     must route identically and match y layer by layer until its first routing
-    difference, which must come with a differently rounded logit."""
+    difference, which must come at a near-tie of the k-th logit.  Such a
+    difference is expected within tens of layers: each layer's y is rounded to
+    bf16 on both sides from differently ordered sums, the residual carries the
+    difference forward, and with 256 experts a near-tie at the k-th logit
+    somewhere along the chain is likely.  So every sampled token must agree on
+    its first layers, and a tenth of the (token, layer) pairs at least are
+    compared."""
+
+    def ordered(bits_):
+        b = np.asarray(bits_, dtype=np.int64)
+        return np.where(b & 0x8000, -(b & 0x7FFF), b)
+
     w = synth.WORKLOADS[4]
-    M, sample = 16, [0, 7, 13]
+    M, sample = 16, [0, 3, 7, 10, 13]
     x0 = synth.layer_input(w, M, device=DEV)["x"]
     ws = moe.Workspace(M, w.E, w.top_k, w.H, w.I, 0)
     cur = x0.clone()
     ox = bits(x0)[sample]
     live = np.ones(len(sample), bool)
     compared = 0
+    first_diff = [w.layers] * len(sample)
     for l in range(w.layers):
         wt = synth.layer_weights(w, layer=l, device=DEV)
         y = torch.empty_like(cur)
@@ -371,12 +383,20 @@ def test_stack_chain_against_the_oracle_on_sampled_tokens():
             if not live[s_i]:
                 continue
             if not np.array_equal(o_ids[s_i], g_ids[s_i]):
+                # a near-tie: every expert chosen by one side only sits within a few
+                # bf16 steps of the oracle's k-th largest logit
                 assert (o_lg[s_i] != g_lg[s_i]).any(), f"layer {l}: routing differs, logits equal"
+                kth = ordered(o_lg[s_i][o_ids[s_i][-1]])
+                odd = np.setxor1d(o_ids[s_i], g_ids[s_i])
+                assert (np.abs(ordered(o_lg[s_i][odd]) - kth) <= 8).all(), \
+                    f"layer {l} token {sample[s_i]}: routing differs away from a near-tie"
                 live[s_i] = False
+                first_diff[s_i] = l
                 continue
             assert_close_bf16(g_y[s_i:s_i + 1], oy[s_i:s_i + 1], f"y layer {l} token {sample[s_i]}")
             compared += 1
         ox, cur = oy, y
         del wt
     assert moe.moe_get_device_status(ws) == 0
-    assert compared >= 0.5 * w.layers * len(sample), f"only {compared} (token, layer) pairs compared"
+    assert min(first_diff) >= 2, f"routing differs too early: first differing layers {first_diff}"
+    assert compared >= 0.1 * w.layers * len(sample), f"only {compared} pairs compared ({first_diff})"

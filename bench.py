@@ -199,34 +199,32 @@ class Layer:
         self.ws = moe.Workspace(M, w.E, w.top_k, w.H, w.I, 0, device=device)
 
     def kernels_per_step(self):
-        align = 1 if self.M * self.w.top_k <= 16384 else 2
-        router = 0 if self.w.logits_given else 1
-        return router + 1 + align + 1 + 2  # + topk, GEMM 1, GEMM 2 and the output pass
+        """Our kernels per step: routing (one fused launch up to 256 tokens, else
+        router + top-k + align), GEMM 1, GEMM 2 and the output pass."""
+        if self.M <= 256 and self.M * self.w.top_k <= 16384:
+            route = 1
+        else:
+            route = (0 if self.w.logits_given else 1) + 1 + (1 if self.M * self.w.top_k <= 16384 else 2)
+        return route + 1 + 2
 
     def step(self, moe, i, stream, ev):
-        """One pass of the layer through the step entry points; ev[0..5] bracket the steps."""
+        """One pass of the layer through the step entry points; ev[0..3] bracket
+        routing (S0-S2), GEMM 1 + activation and GEMM 2 + combine."""
         w, inp = self.w, self.inputs[i]
         x = inp["x"]
         ev[0].record(stream)
-        if w.logits_given:
-            logits = inp["router_logits"]
-        else:
-            moe.moe_router_logits(x, self.wr, self.logits, router_bias=self.bias, stream=stream)
-            logits = self.logits
+        moe.moe_route(w.top_k, self.B, self.ids, self.wts, self.sorted, self.eids, self.offs,
+                      self.npost, self.ws, x=None if w.logits_given else x,
+                      w_router=self.wr, router_logits=inp["router_logits"], router_bias=self.bias,
+                      renormalize=w.renormalize, stream=stream)
         ev[1].record(stream)
-        moe.moe_topk_softmax(logits, w.top_k, self.ids, self.wts, renormalize=w.renormalize,
-                             stream=stream)
-        ev[2].record(stream)
-        moe.moe_align_block_size(self.ids, w.E, self.B, self.sorted, self.eids, self.offs,
-                                 self.npost, self.ws, stream=stream)
-        ev[3].record(stream)
         moe.moe_grouped_gemm_w13_act(x, self.w13, self.sorted, self.eids, self.npost, w.top_k,
                                      self.B, self.a, stream=stream)
-        ev[4].record(stream)
+        ev[2].record(stream)
         moe.moe_grouped_gemm_w2_combine(self.a, self.w2, self.sorted, self.eids, self.npost,
                                         self.wts, w.top_k, self.B, self.y, self.ws,
                                         residual=x if w.residual else None, stream=stream)
-        ev[5].record(stream)
+        ev[3].record(stream)
 
     def distinct_experts(self, moe, i, stream):
         inp = self.inputs[i]
@@ -245,7 +243,7 @@ def run_point(moe, w, M, steps, warmup, device, stream, flush, L=None):
         L = Layer(moe, w, M, warmup + steps, device)
     # inputs are drawn on the default stream; the steps run on `stream`
     torch.cuda.synchronize()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(warmup + steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(warmup + steps)]
     with torch.cuda.stream(stream):
         for i in range(warmup):
             flush.zero_()
@@ -255,8 +253,8 @@ def run_point(moe, w, M, steps, warmup, device, stream, flush, L=None):
             flush.zero_()
             L.step(moe, i, stream, evs[i])
         stream.synchronize()
-    per = [[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(5)] for i in range(warmup, warmup + steps)]
-    step_ms = [evs[i][0].elapsed_time(evs[i][5]) for i in range(warmup, warmup + steps)]
+    per = [[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(3)] for i in range(warmup, warmup + steps)]
+    step_ms = [evs[i][0].elapsed_time(evs[i][3]) for i in range(warmup, warmup + steps)]
     D = [L.distinct_experts(moe, i, stream) for i in range(warmup, warmup + steps)]
     return L, per, step_ms, D
 
@@ -464,7 +462,7 @@ def ours(args):
     ms_per_step = total_ms / args.steps
     value = world * M * args.steps / (total_ms / 1e3)
 
-    gemm1_ms = statistics.mean(p[3] for p in per)
+    gemm1_ms = statistics.mean(p[1] for p in per)
     D_mean = statistics.mean(D)
     g1_bytes = statistics.mean(gemm1_bytes(w, M, d) for d in D)
     g1_flops = gemm1_flops(w, M)
@@ -500,8 +498,9 @@ def ours(args):
                            "hbm_frac_layer": round(bpl / (ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
                            "tc_frac_layer": round(layer_flops(w, m) / (ms / 1e3) / 1e12
                                                   / peaks["bf16_tflops"], 4),
-                           "gemm1_ms": round(statistics.mean(p[3] for p in p_per), 5),
-                           "gemm2_ms": round(statistics.mean(p[4] for p in p_per), 5),
+                           "route_ms": round(statistics.mean(p[0] for p in p_per), 5),
+                           "gemm1_ms": round(statistics.mean(p[1] for p in p_per), 5),
+                           "gemm2_ms": round(statistics.mean(p[2] for p in p_per), 5),
                            "distinct_experts": round(statistics.mean(p_D), 2)})
 
     if rank != 0:
@@ -526,7 +525,7 @@ def ours(args):
                            "algorithmic_bytes": int(lay_bytes), "flops": int(flops),
                            "distinct_experts": round(D_mean, 2)},
         "step_breakdown_ms": {k: round(statistics.mean(p[j] for p in per), 5) for j, k in
-                              enumerate(["router", "topk", "align", "gemm1_act", "gemm2_combine"])},
+                              enumerate(["route", "gemm1_act", "gemm2_combine"])},
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_total / args.steps, 5)},
         "cpu_baseline": cpu,

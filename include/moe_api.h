@@ -120,6 +120,27 @@ moe_status_t moe_align_block_size(const int32_t *topk_ids, int M, int top_k, int
                                   int32_t *num_tokens_post_padded, void *ws, size_t ws_bytes,
                                   cudaStream_t stream);
 
+/* S0 + S1 + S2 together: router logits (or the given logits), softmax /
+ * top-k / renormalize and the block-padded grouping, with the results of
+ * moe_router_logits, moe_topk_softmax and moe_align_block_size.  The SGLang
+ * issue page describes a kernel that fuses the router with softmax and top-k,
+ * and the MoE execution analysis page ("Per-decode-step kernel launches")
+ * counts one launch per step per layer; for batches of up to 256 tokens (with
+ * M * top_k <= 16384) this runs as one launch, otherwise as three kernels.
+ * Exactly one of w_router [E, H] and router_logits [M, E] is non-NULL
+ * (router_bias only with w_router; H is ignored with router_logits).
+ * Outputs as for moe_topk_softmax and moe_align_block_size (block_size_m
+ * explicit).  ws/ws_bytes: a workspace of at least moe_workspace_size(M, E,
+ * top_k, 16, 16, block_size_m) bytes, initialised once with moe_workspace_init
+ * (its control block holds counters that must start at zero; each call leaves
+ * them at zero); calls sharing a workspace must not overlap on the GPU. */
+moe_status_t moe_route(const moe_bf16_t *x, const moe_bf16_t *w_router,
+                       const moe_bf16_t *router_logits, const float *router_bias, int M, int E,
+                       int top_k, int H, int renormalize, int block_size_m, int32_t *topk_ids,
+                       float *topk_weights, int32_t *sorted_token_ids, int32_t *expert_ids,
+                       int32_t *expert_offsets, int32_t *num_tokens_post_padded, void *ws,
+                       size_t ws_bytes, cudaStream_t stream);
+
 /* S3. Grouped GEMM 1 with SiLU-and-mul.  [vLLM] "One GEMM 1 program, step by
  * step" and "The rest of the layer stays in pair order": for every real pair
  * p in block b (p < M*top_k), with e = expert_ids[b] and t = p / top_k,

@@ -26,7 +26,7 @@ __all__ = [
     "moe_pick_block_size", "moe_workspace_init", "moe_router_logits", "moe_topk_softmax",
     "moe_align_block_size", "moe_grouped_gemm_w13_act", "moe_grouped_gemm_w2_combine",
     "moe_forward", "moe_get_device_status", "moe_status_string", "Workspace",
-    "moe_grouped_gemm_w2_combine_noalloc",
+    "moe_grouped_gemm_w2_combine_noalloc", "moe_route",
 ]
 
 STATUS_NAMES = {
@@ -40,7 +40,7 @@ EXPORTED = (
     "moe_workspace_size", "moe_align_capacity", "moe_pick_block_size", "moe_router_logits",
     "moe_topk_softmax", "moe_align_block_size", "moe_grouped_gemm_w13_act",
     "moe_grouped_gemm_w2_combine", "moe_forward", "moe_workspace_init", "moe_get_device_status",
-    "moe_status_string", "moe_grouped_gemm_w2_combine_noalloc",
+    "moe_status_string", "moe_grouped_gemm_w2_combine_noalloc", "moe_route",
 )
 
 
@@ -78,6 +78,7 @@ def load_library(build_if_missing: bool = False):
         "moe_topk_softmax": ([P, I, I, I, I, P, P, P], I),
         "moe_align_block_size": ([P, I, I, I, I, P, P, P, P, P, Z, P], I),
         "moe_grouped_gemm_w13_act": ([P, P, P, P, P, I, I, I, I, I, I, P, P], I),
+        "moe_route": ([P, P, P, P, I, I, I, I, I, I, P, P, P, P, P, P, P, Z, P], I),
         "moe_grouped_gemm_w2_combine": ([P, P, P, P, P, P, P, I, I, I, I, I, I, P, P, Z, P], I),
         "moe_grouped_gemm_w2_combine_noalloc": ([P, P, P, P, P, P, P, I, I, I, I, I, I, P, P], I),
         "moe_forward": ([P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, P, P, Z, P], I),
@@ -210,6 +211,29 @@ def moe_align_block_size(topk_ids, E: int, block_size_m: int, sorted_token_ids, 
                                             _p(sorted_token_ids), _p(expert_ids),
                                             _p(expert_offsets), _p(num_tokens_post_padded), ptr, n,
                                             _stream(stream)), "moe_align_block_size")
+
+
+def moe_route(top_k: int, block_size_m: int, topk_ids, topk_weights, sorted_token_ids,
+              expert_ids, expert_offsets, num_tokens_post_padded, ws, *, x=None, w_router=None,
+              router_logits=None, router_bias=None, renormalize: bool = True, stream=None) -> None:
+    """Router logits (or the given logits), top-k and align in as few launches as the shape allows."""
+    for t, n in ((x, "x"), (w_router, "w_router"), (router_logits, "router_logits")):
+        _check_dtype(t, torch.bfloat16, n)
+    _check_dtype(router_bias, torch.float32, "router_bias")
+    _check_dtype(topk_ids, torch.int32, "topk_ids")
+    _check_dtype(topk_weights, torch.float32, "topk_weights")
+    if w_router is not None:
+        M, H = x.shape
+        E = w_router.shape[0]
+    else:
+        M, E = router_logits.shape
+        H = 16
+    ptr, n = _ws(ws)
+    _ok(load_library().moe_route(_p(x), _p(w_router), _p(router_logits), _p(router_bias), M, E,
+                                 top_k, H, int(bool(renormalize)), block_size_m, _p(topk_ids),
+                                 _p(topk_weights), _p(sorted_token_ids), _p(expert_ids),
+                                 _p(expert_offsets), _p(num_tokens_post_padded), ptr, n,
+                                 _stream(stream)), "moe_route")
 
 
 def moe_grouped_gemm_w13_act(x, w13, sorted_token_ids, expert_ids, num_tokens_post_padded,

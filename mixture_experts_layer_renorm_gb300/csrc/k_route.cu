@@ -5,7 +5,7 @@
 // section "One token uses only 8 experts": the router is one linear layer
 // W_r [E, H]; softmax over the E scores; keep the top_k largest; rescale the
 // kept weights to sum to 1 (renormalize).
-#include "moe_internal.cuh"
+#include "route_dev.cuh"
 
 namespace moe {
 
@@ -84,75 +84,16 @@ k_router_logits(const uint16_t *__restrict__ x, const uint16_t *__restrict__ w_r
   }
 }
 
-// Order-preserving map of a bf16 pattern to 16 unsigned bits: larger value ->
-// larger key; -0 is folded onto +0 so that the two compare equal.
-__device__ __forceinline__ uint32_t bf16_order_key(uint16_t b) {
-  if (b == 0x8000u) b = 0;
-  return (b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u);
-}
-__device__ __forceinline__ uint16_t bf16_from_order_key(uint32_t k) {
-  return (k & 0x8000u) ? static_cast<uint16_t>(k & 0x7FFFu) : static_cast<uint16_t>(~k & 0xFFFFu);
-}
-
-// One warp per token.  Lane l holds logits l, l+32, ... as 32-bit keys
-// (order key << 16 | (0xFFFF - e)), so the largest key is the largest logit
-// and, among equal logits, the lowest expert id.  top_k rounds of a warp
-// max-reduction pick the slots in order; the winner's key is cleared.
+// One warp per token.
 template <int VPL>
 __global__ void __launch_bounds__(256)
 k_topk_softmax(const uint16_t *__restrict__ logits, int M, int E, int top_k, int renormalize,
                int32_t *__restrict__ topk_ids, float *__restrict__ topk_weights) {
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
   if (t >= M) return;
-  const uint16_t *row = logits + (size_t)t * E;
-  uint32_t key[VPL];
-  float val[VPL];
-  float mx = -INFINITY;
-#pragma unroll
-  for (int i = 0; i < VPL; ++i) {
-    const int e = lane + 32 * i;
-    key[i] = 0;
-    val[i] = -INFINITY;
-    if (e < E) {
-      const uint16_t b = row[e];
-      key[i] = (bf16_order_key(b) << 16) | (0xFFFFu - static_cast<uint32_t>(e));
-      val[i] = bf16_bits_to_float(b);
-      mx = fmaxf(mx, val[i]);
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  float den = 0.f;
-#pragma unroll
-  for (int i = 0; i < VPL; ++i)
-    if (lane + 32 * i < E) den += expf(val[i] - mx);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-
-  int my_id = 0;
-  float my_p = 0.f, kept = 0.f;
-  for (int j = 0; j < top_k; ++j) {
-    uint32_t best = 0;
-#pragma unroll
-    for (int i = 0; i < VPL; ++i) best = max(best, key[i]);
-    best = __reduce_max_sync(0xffffffffu, best);
-#pragma unroll
-    for (int i = 0; i < VPL; ++i)
-      if (key[i] == best) key[i] = 0;
-    const int e = static_cast<int>(0xFFFFu - (best & 0xFFFFu));
-    const float v = bf16_bits_to_float(bf16_from_order_key(best >> 16));
-    const float pj = expf(v - mx);
-    kept += pj;
-    if (lane == j) {
-      my_id = e;
-      my_p = pj;
-    }
-  }
-  if (lane < top_k) {
-    topk_ids[(size_t)t * top_k + lane] = my_id;
-    topk_weights[(size_t)t * top_k + lane] = renormalize ? my_p / kept : my_p / den;
-  }
+  topk_softmax_warp<VPL, false>(logits + (size_t)t * E, E, top_k, renormalize,
+                                topk_ids + (size_t)t * top_k, topk_weights + (size_t)t * top_k,
+                                threadIdx.x & 31);
 }
 
 }  // namespace

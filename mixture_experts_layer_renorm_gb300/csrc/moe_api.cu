@@ -130,6 +130,38 @@ moe_status_t run_router(const uint16_t *x, const uint16_t *w_router, const float
   return cuda_status(moe::launch_router_logits(x, w_router, bias, M, E, H, logits, s));
 }
 
+// S0 + S1 + S2.  Decode-sized batches take one fused launch (which also
+// clears zero_buf, the combine accumulator, when given); larger ones run the
+// router, top-k and align kernels.  *zeroed tells whether zero_buf was cleared.
+constexpr int kFusedRouteMaxTokens = 256;
+
+moe_status_t run_route(const uint16_t *x, const uint16_t *w_router, const uint16_t *router_logits,
+                       const float *bias, int M, int E, int top_k, int H, int renormalize, int B,
+                       uint16_t *logits_ws, int32_t *ids, float *wts, int32_t *sorted,
+                       int32_t *eids, int32_t *offs, int32_t *npost, int32_t *hist, int *control,
+                       float *zero_buf, long zero_n, bool *zeroed, cudaStream_t s) {
+  const long P = static_cast<long>(M) * top_k;
+  const int cap = static_cast<int>(capacity(P, E, B));
+  *zeroed = false;
+  if (M <= kFusedRouteMaxTokens && moe::route_fused_supports(M, E, top_k) && forced_path() != 1) {
+    *zeroed = zero_buf != nullptr;
+    return cuda_status(moe::launch_route_fused(
+        x, w_router, bias, router_logits, M, E, H, top_k, renormalize, B, logits_ws, ids, wts,
+        sorted, eids, offs, npost, control + moe::kCountersOffset, control, zero_buf, zero_n, s));
+  }
+  const uint16_t *logits = router_logits;
+  if (w_router) {
+    moe_status_t st = run_router(x, w_router, bias, M, E, H, logits_ws, control, s);
+    if (st != MOE_OK) return st;
+    logits = logits_ws;
+  }
+  moe_status_t st =
+      cuda_status(moe::launch_topk_softmax(logits, M, E, top_k, renormalize, ids, wts, s));
+  if (st != MOE_OK) return st;
+  return cuda_status(moe::launch_align(ids, static_cast<int>(P), E, B, cap, sorted, eids, offs,
+                                       npost, hist, control, s));
+}
+
 moe_status_t run_gemm1(const uint16_t *x, const uint16_t *w13, const int32_t *sorted,
                        const int32_t *eids, const int32_t *npost, int M, int top_k, int E, int H,
                        int I, int B, uint16_t *a, int *status, cudaStream_t s) {
@@ -326,33 +358,56 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *w_router,
   const long P = static_cast<long>(M) * top_k;
   const int cap = static_cast<int>(capacity(P, E, B));
   int *status = at<int>(ws, L.status);
-  const uint16_t *logits = router_logits;
-  if (w_router) {
-    uint16_t *lg = at<uint16_t>(ws, L.logits);
-    st = run_router(x, w_router, router_bias, M, E, H, lg, status, stream);
-    if (st != MOE_OK) return st;
-    logits = lg;
-  }
   int32_t *ids = topk_ids_out ? topk_ids_out : at<int32_t>(ws, L.ids);
   float *wts = topk_weights_out ? topk_weights_out : at<float>(ws, L.wts);
-  st = cuda_status(moe::launch_topk_softmax(logits, M, E, top_k, renormalize, ids, wts, stream));
-  if (st != MOE_OK) return st;
   int32_t *sorted = at<int32_t>(ws, L.sorted);
   int32_t *eids = at<int32_t>(ws, L.eids);
   int32_t *offs = at<int32_t>(ws, L.offsets);
   int32_t *npost = at<int32_t>(ws, L.npost);
-  st = cuda_status(moe::launch_align(ids, static_cast<int>(P), E, B, cap, sorted, eids, offs, npost,
-                                     at<int32_t>(ws, L.hist), status, stream));
+  float *yacc = at<float>(ws, L.yacc);
+  const long yn = static_cast<long>(M) * H;
+  bool zeroed = false;
+  st = run_route(x, w_router, router_logits, router_bias, M, E, top_k, H, renormalize, B,
+                 at<uint16_t>(ws, L.logits), ids, wts, sorted, eids, offs, npost,
+                 at<int32_t>(ws, L.hist), status, yacc, yn, &zeroed, stream);
   if (st != MOE_OK) return st;
   uint16_t *a = at<uint16_t>(ws, L.a);
   st = run_gemm1(x, w13, sorted, eids, npost, M, top_k, E, H, I, B, a, status, stream);
   if (st != MOE_OK) return st;
-  float *yacc = at<float>(ws, L.yacc);
-  if (cudaMemsetAsync(yacc, 0, sizeof(float) * static_cast<size_t>(M) * H, stream) != cudaSuccess)
+  if (!zeroed && cudaMemsetAsync(yacc, 0, sizeof(float) * static_cast<size_t>(yn), stream) != cudaSuccess)
     return MOE_ERR_CUDA;
   st = run_gemm2(a, w2, sorted, eids, npost, wts, M, top_k, E, H, I, B, yacc, status, stream);
   if (st != MOE_OK) return st;
   return cuda_status(moe::launch_finalize(yacc, residual, M, H, y, stream));
+}
+
+moe_status_t moe_route(const moe_bf16_t *x, const moe_bf16_t *w_router,
+                       const moe_bf16_t *router_logits, const float *router_bias, int M, int E,
+                       int top_k, int H, int renormalize, int block_size_m, int32_t *topk_ids,
+                       float *topk_weights, int32_t *sorted_token_ids, int32_t *expert_ids,
+                       int32_t *expert_offsets, int32_t *num_tokens_post_padded, void *ws,
+                       size_t ws_bytes, cudaStream_t stream) {
+  if (M < 0) return MOE_ERR_INVALID_ARG;
+  if (E < 1 || E > kMaxExperts || top_k < 1 || top_k > std::min(E, kMaxTopK) ||
+      !valid_block_size(block_size_m))
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (w_router && (H < 16 || H > kMaxDim || H % 16 != 0)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (static_cast<long long>(M) * top_k >= (1LL << 31) - kMaxExperts * 256LL)
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  if ((w_router == nullptr) == (router_logits == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (router_bias && !w_router) return MOE_ERR_INVALID_ARG;
+  if (M == 0) return MOE_OK;
+  if ((w_router && (!x || !aligned16(x) || !aligned16(w_router))) || !topk_ids || !topk_weights ||
+      !sorted_token_ids || !expert_ids || !expert_offsets || !num_tokens_post_padded || !ws)
+    return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(M, E, top_k, 16, 16, block_size_m);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  bool zeroed = false;
+  return run_route(x, w_router, router_logits, router_bias, M, E, top_k, H, renormalize,
+                   block_size_m, at<uint16_t>(ws, L.logits), topk_ids, topk_weights,
+                   sorted_token_ids, expert_ids, expert_offsets, num_tokens_post_padded,
+                   at<int32_t>(ws, L.hist), at<int>(ws, 0), nullptr, 0, &zeroed, stream);
 }
 
 moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream) {

@@ -10,7 +10,12 @@ namespace moe {
 
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
-constexpr int kStatusBytes = 256;  // the status word lives in the first 256 B of the workspace
+// The workspace starts with a control block: the status word at int 0 and the
+// fused routing kernel's completion counters from int kCountersOffset on.
+constexpr int kStatusBytes = 1024;
+constexpr int kCountersOffset = 64;
+constexpr int kRouteFusedTok = 8;          // tokens per CTA of the fused routing kernel
+constexpr int kRouteFusedMaxGroups = 64;   // so at most 512 tokens; one more counter for the align
 
 // Device status codes (same numbering as moe_status_t).
 constexpr int kStatusBadExpertId = 5;
@@ -102,6 +107,17 @@ cudaError_t launch_tc_router(const uint16_t *x, const uint16_t *w_router, const 
 // y = bf16(y_acc + residual)
 cudaError_t launch_finalize(const float *y_acc, const uint16_t *residual, int M, int H, uint16_t *y,
                             cudaStream_t s);
+
+// S0 + S1 + S2 in one launch (decode-sized batches).  logits_in given: no
+// router.  counters: kRouteFusedMaxGroups + 1 ints in the workspace control
+// block, zero between calls.  zero_buf (nullable): zero_n floats cleared on the side.
+bool route_fused_supports(int M, int E, int top_k);
+cudaError_t launch_route_fused(const uint16_t *x, const uint16_t *w_router, const float *bias,
+                               const uint16_t *logits_in, int M, int E, int H, int top_k,
+                               int renormalize, int B, uint16_t *logits_ws, int32_t *topk_ids,
+                               float *topk_w, int32_t *sorted_ids, int32_t *expert_ids,
+                               int32_t *expert_offsets, int32_t *n_post, int *counters,
+                               int *status, float *zero_buf, long zero_n, cudaStream_t s);
 
 int num_sms();
 

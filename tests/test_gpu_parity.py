@@ -400,3 +400,70 @@ def test_stack_chain_against_the_oracle_on_sampled_tokens():
     assert moe.moe_get_device_status(ws) == 0
     assert min(first_diff) >= 2, f"routing differs too early: first differing layers {first_diff}"
     assert compared >= 0.1 * w.layers * len(sample), f"only {compared} pairs compared ({first_diff})"
+
+
+# ----------------------------------------------------------------------------- S0 + S1 + S2 together
+
+def run_route(M, E, k, B, *, lg=None, x=None, wr=None, bias=None, ws=None, renorm=True):
+    cap = moe.moe_align_capacity(M, k, E, B)
+    out = dict(ids=torch.empty((M, k), dtype=torch.int32, device=DEV),
+               w=torch.empty((M, k), dtype=torch.float32, device=DEV),
+               s=torch.full((cap,), -7, dtype=torch.int32, device=DEV),
+               e=torch.full((cap // B,), -7, dtype=torch.int32, device=DEV),
+               o=torch.empty((E + 1,), dtype=torch.int32, device=DEV),
+               n=torch.empty((1,), dtype=torch.int32, device=DEV))
+    ws = ws or moe.Workspace(M, E, k, 16, 16, B)
+    moe.moe_route(k, B, out["ids"], out["w"], out["s"], out["e"], out["o"], out["n"], ws, x=x,
+                  w_router=wr, router_logits=lg, router_bias=bias, renormalize=renorm)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status(ws) == 0
+    return {kk: v.cpu().numpy() for kk, v in out.items()}, ws
+
+
+@pytest.mark.parametrize("M,E,k,B", [(1, 128, 8, 16), (64, 128, 8, 16), (64, 60, 4, 16), (3, 4, 2, 4),
+                                     (256, 256, 8, 16), (200, 1024, 32, 32), (37, 33, 3, 64),
+                                     (300, 128, 8, 16)])
+def test_route_given_logits_matches_the_steps(M, E, k, B):
+    """One launch (M <= 256) or three kernels (M = 300): the same ids, weights and
+    lists as the oracle's top-k and align; a second call on the same workspace
+    (its counters reset by the first) gives the same result."""
+    lg = rand_bf16((M, E), 1.0, 4000 + M + E, "cpu")
+    rid, rw = oracle.topk_softmax(bits(lg), k)
+    rs, re_, ro, rn = oracle.align_block_size(rid, E, B)
+    ws = None
+    for _ in range(2):
+        out, ws = run_route(M, E, k, B, lg=lg.to(DEV), ws=ws)
+        assert np.array_equal(out["ids"], rid)
+        assert np.abs(out["w"].astype(np.float64) - rw).max() <= W_ABS
+        n = int(out["n"][0])
+        assert n == rn
+        assert np.array_equal(out["s"][:n], rs[:n])
+        assert np.array_equal(out["e"][: n // B], re_[: n // B])
+        assert np.array_equal(out["o"], ro)
+
+
+@pytest.mark.parametrize("cfg,M", [(2, 1), (2, 64), (4, 128), (3, 512)])
+def test_route_with_router_weights(cfg, M):
+    w = synth.WORKLOADS[cfg]
+    wt = synth.layer_weights(w, device=DEV)
+    x = synth.layer_input(w, M, device=DEV)["x"]
+    B = 16
+    out, _ = run_route(M, w.E, w.top_k, B, x=x, wr=wt["w_router"], bias=wt["router_bias"])
+    bias_np = None if wt["router_bias"] is None else wt["router_bias"].cpu().numpy()
+    o_lg = oracle.router_logits(bits(x), bits(wt["w_router"]), bias_np)
+    rid, _ = oracle.topk_softmax(o_lg, w.top_k)
+    agree = (out["ids"] == rid).all(axis=1)
+    assert agree.mean() >= 0.98
+    # whatever the routing, the lists group exactly the routed pairs
+    ids = out["ids"]
+    P = ids.size
+    n = int(out["n"][0])
+    body = out["s"][:n]
+    real = body[body < P]
+    assert np.array_equal(real, np.argsort(ids.reshape(-1), kind="stable"))
+    for b, e in enumerate(out["e"][: n // B]):
+        seg = body[b * B:(b + 1) * B]
+        assert (ids.reshape(-1)[seg[seg < P]] == e).all()
+    if agree.all():
+        rs, re_, ro, rn = oracle.align_block_size(rid, w.E, B)
+        assert n == rn and np.array_equal(body, rs[:n]) and np.array_equal(out["o"], ro)

@@ -337,8 +337,13 @@ class Stack:
                     for _ in range(w.layers)]
 
     def kernels_per_step(self):
-        align = 1 if self.M * self.w.top_k <= 16384 else 2
-        return self.w.layers * (1 + 1 + align + 1 + 2)
+        """moe_forward per layer: routing (one fused launch up to 256 tokens, else
+        router + top-k + align), GEMM 1, GEMM 2 and the output pass."""
+        if self.M <= 256 and self.M * self.w.top_k <= 16384:
+            route = 1
+        else:
+            route = 2 + (1 if self.M * self.w.top_k <= 16384 else 2)
+        return self.w.layers * (route + 3)
 
     def step(self, moe, x, stream, keep_ids=False):
         """x (held in buf[0]) through every layer; returns the output buffer."""

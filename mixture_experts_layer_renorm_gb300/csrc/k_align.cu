@@ -107,12 +107,10 @@ cudaError_t launch_align(const int32_t *topk_ids, int P, int E, int B, int cap,
                          int32_t *n_post, int32_t *hist, int *status, cudaStream_t s) {
   (void)cap;
   const size_t smem = align_smem_bytes(E);
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaFuncSetAttribute(k_align_single, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
-    cudaFuncSetAttribute(k_align_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
-    attr_done = true;
-  }
+  cudaError_t attr = ensure_smem_limit(reinterpret_cast<const void *>(k_align_single), 96 * 1024);
+  if (attr == cudaSuccess)
+    attr = ensure_smem_limit(reinterpret_cast<const void *>(k_align_scatter), 96 * 1024);
+  if (attr != cudaSuccess) return attr;
   const int C = align_num_ctas(P);
   if (C == 1) {
     k_align_single<<<1, kAlignThreads, smem, s>>>(topk_ids, P, E, B, sorted_ids, expert_ids,

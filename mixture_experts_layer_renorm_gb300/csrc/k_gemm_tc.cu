@@ -242,13 +242,43 @@ struct TcConfig {
   static_assert(N * 8 % kGatherThreads == 0, "gather threads split a stage evenly");
 };
 
+// Tile t of the persistent schedule: block b, weight tile c, and the K-stage
+// range [kb0, kb1) of split sp (ksplit splits; the splits of one tile are
+// neighbours in the schedule and run side by side).
+struct TileCoord {
+  int b, c, kb0, kb1;
+};
+__device__ __forceinline__ TileCoord tile_coord(int t, int n_ctiles, int ksplit, int nk) {
+  const int per_b = n_ctiles * ksplit;
+  TileCoord tc;
+  tc.b = t / per_b;
+  const int r = t - tc.b * per_b;
+  tc.c = r / ksplit;
+  const int sp = r - tc.c * ksplit;
+  const int span = (nk + ksplit - 1) / ksplit;
+  tc.kb0 = min(nk, sp * span);
+  tc.kb1 = min(nk, tc.kb0 + span);
+  return tc;
+}
+
+// a = bf16( SiLU(bf16(gate)) * bf16(up) ) from fp32 GEMM-1 sums.
+__device__ __forceinline__ uint16_t silu_mul_bf16(float gate, float up) {
+  const float gb = bf16_bits_to_float(float_to_bf16_bits(gate));
+  const float ub = bf16_bits_to_float(float_to_bf16_bits(up));
+  const float silu = gb * __frcp_rn(1.0f + expf(-gb));
+  return float_to_bf16_bits(silu * ub);
+}
+
 __device__ __forceinline__ void epilogue_bar_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");  // the epilogue warps only
 }
 
-// Persistent tiles: tile t = (block t / n_ctiles, weight tile t % n_ctiles);
-// the weight tiles of one block are neighbours, so concurrently running CTAs
-// share the block's gathered rows and the expert's weights in L2.
+// Persistent tiles (tile_coord): block, weight tile, K split; the weight tiles
+// (and splits) of one block are neighbours, so concurrently running CTAs share
+// the block's gathered rows and the expert's weights in L2.  With ksplit > 1
+// (decode-sized GEMM 1 with too few tiles for the SMs) each split adds its
+// fp32 partial gate/up sums into h_acc [P, 2I] and the last split of the tile
+// forms a; h_acc and tile_cnt must be zero on entry and tile_cnt is left zero.
 //
 // MODE 0: GEMM 1 + SiLU-and-mul   rows = x[p / top_k], A = W13_e gate | up tiles,
 //                                 a[p, i] = bf16(SiLU(bf16 gate) * bf16 up)
@@ -261,8 +291,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict__ src,
           int src_rows, const int32_t *__restrict__ sorted_ids, const int32_t *__restrict__ expert_ids,
           const int32_t *__restrict__ n_post_ptr, const float *__restrict__ vec, int P, int top_k,
-          int E, int K, int R_out, int a_rows, int B, int cap, int n_ctiles,
-          uint16_t *__restrict__ out16, float *__restrict__ y_acc, int H_out, int *status) {
+          int E, int K, int R_out, int a_rows, int B, int cap, int n_ctiles, int ksplit,
+          float *__restrict__ h_acc, int *__restrict__ tile_cnt, uint16_t *__restrict__ out16,
+          float *__restrict__ y_acc, int H_out, int *status) {
   using Cfg = TcConfig<N>;
   constexpr int S = Cfg::kStages;
   int n_blocks;
@@ -272,7 +303,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
     const int n_post = min(max(*n_post_ptr, 0), cap);
     n_blocks = n_post / B;
   }
-  const int n_tiles = n_blocks * n_ctiles;
+  const int n_tiles = n_blocks * n_ctiles * ksplit;
   if (static_cast<int>(blockIdx.x) >= n_tiles) return;
 
   extern __shared__ uint8_t smem_raw[];
@@ -288,6 +319,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
   volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
   int *dst_row = reinterpret_cast<int *>(tmem_slot + 4);     // epilogue's current block
   float *dst_w = reinterpret_cast<float *>(dst_row + N);
+  volatile int *split_last = reinterpret_cast<volatile int *>(tmem_slot + 2);
+  volatile int *epi_stop = reinterpret_cast<volatile int *>(tmem_slot + 3);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -301,6 +334,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
       mbar_init(smem_u32(&acc_empty[a]), kEpiWarps);  // one arrive per epilogue warp
     }
     *abort = 0;
+    *epi_stop = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
@@ -319,13 +353,14 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
       int g = 0;
       bool stop = false;
       for (int t = blockIdx.x; t < n_tiles && !stop; t += gridDim.x) {
-        const int b = t / n_ctiles, c = t - b * n_ctiles;
+        const TileCoord tc = tile_coord(t, n_ctiles, ksplit, nk);
+        const int b = tc.b, c = tc.c;
         const int e = MODE == 2 ? 0 : expert_ids[b];
         if (e < 0 || e >= E) continue;  // every role skips this tile
         const int row0 = MODE == 0 ? c * kTileM : c * 2 * kTileM;
         const int row1 = MODE == 0 ? R_out + c * kTileM : c * 2 * kTileM + kTileM;
         const bool two = MODE == 0 || row1 < a_rows;
-        for (int kb = 0; kb < nk; ++kb, ++g) {
+        for (int kb = tc.kb0; kb < tc.kb1; ++kb, ++g) {
           const int s = g % S;
           if (!wait_bounded(smem_u32(&empty[s]), ((g / S) & 1) ^ 1, abort, status)) {
             stop = true;
@@ -360,7 +395,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
     int g = 0;
     bool stop = false;
     for (int t = blockIdx.x; t < n_tiles && !stop; t += gridDim.x) {
-      const int b = t / n_ctiles;
+      const TileCoord tc = tile_coord(t, n_ctiles, ksplit, nk);
+      const int b = tc.b;
       const int e = MODE == 2 ? 0 : expert_ids[b];
       if (e < 0 || e >= E) continue;
       int rowv[Cfg::kChunksPerThread];
@@ -376,7 +412,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
         }
         rowv[u] = row;
       }
-      for (int kb = 0; kb < nk; ++kb, ++g) {
+      for (int kb = tc.kb0; kb < tc.kb1; ++kb, ++g) {
         const int s = g % S;
         if (!wait_bounded(smem_u32(&empty[s]), ((g / S) & 1) ^ 1, abort, status)) {
           stop = true;
@@ -403,7 +439,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
       int g = 0, i = 0;
       bool stop = false;
       for (int t = blockIdx.x; t < n_tiles && !stop; t += gridDim.x) {
-        const int b = t / n_ctiles, c = t - b * n_ctiles;
+        const TileCoord tc = tile_coord(t, n_ctiles, ksplit, nk);
+        const int b = tc.b, c = tc.c;
         const int e = MODE == 2 ? 0 : expert_ids[b];
         if (e < 0 || e >= E) continue;
         const bool two = MODE == 0 || c * 2 * kTileM + kTileM < a_rows;
@@ -413,7 +450,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
         if (!wait_bounded(smem_u32(&acc_empty[acc]), (use & 1) ^ 1, abort, status)) break;
         tc_fence_after();
         const uint32_t d0 = tmem + acc * Cfg::kAccCols;
-        for (int kb = 0; kb < nk; ++kb, ++g) {
+        for (int kb = tc.kb0; kb < tc.kb1; ++kb, ++g) {
           const int s = g % S;
           if (!wait_bounded(smem_u32(&full[s]), (g / S) & 1, abort, status)) {
             stop = true;
@@ -426,7 +463,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
           const uint32_t bt = smem_u32(b_tiles + s * Cfg::kBStageBytes);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint32_t accumulate = (kb > 0 || kk > 0) ? 1u : 0u;
+            const uint32_t accumulate = (kb > tc.kb0 || kk > 0) ? 1u : 0u;
             const uint64_t bd = sw128_kmajor_desc(bt + kk * 32);
             umma_bf16(d0, sw128_kmajor_desc(a0 + kk * 32), bd, idesc, accumulate);
             if (two) umma_bf16(d0 + N, sw128_kmajor_desc(a1 + kk * 32), bd, idesc, accumulate);
@@ -445,7 +482,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     int i = 0;
     for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
-      const int b = t / n_ctiles, c = t - b * n_ctiles;
+      const TileCoord tc = tile_coord(t, n_ctiles, ksplit, nk);
+      const int b = tc.b, c = tc.c;
       const int e = MODE == 2 ? 0 : expert_ids[b];
       if (e < 0 || e >= E) continue;
       const bool two = MODE == 0 || c * 2 * kTileM + kTileM < a_rows;
@@ -470,10 +508,12 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
         dst_w[j] = wgt;
       }
       epilogue_bar_sync();
-      bool ok = wait_bounded(smem_u32(&acc_full[acc]), use & 1, abort, status);
+      const bool ok = wait_bounded(smem_u32(&acc_full[acc]), use & 1, abort, status);
       tc_fence_after();
-      ok = __all_sync(0xffffffffu, ok && !*abort);  // tcgen05.ld needs the whole warp
-      if (!ok) break;
+      // stop together: every epilogue warp meets the same named barriers
+      if (!ok || *abort) *epi_stop = 1;
+      epilogue_bar_sync();
+      if (*epi_stop) break;
       const uint32_t d0 = tmem + lane_base + acc * Cfg::kAccCols;
       if (MODE == 0) {
         const int chn = c * kTileM + q * 32 + lane;
@@ -488,10 +528,14 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
           for (int jj = 0; jj < 16; ++jj) {
             const int p = dst_row[j0 + jj];
             if (valid && p >= 0) {
-              const float gb = bf16_bits_to_float(float_to_bf16_bits(__uint_as_float(gt[jj])));
-              const float ub = bf16_bits_to_float(float_to_bf16_bits(__uint_as_float(up[jj])));
-              const float silu = gb * __frcp_rn(1.0f + expf(-gb));
-              out16[(size_t)p * R_out + chn] = float_to_bf16_bits(silu * ub);
+              if (ksplit > 1) {
+                // a partial sum over this split's K range: add it up in fp32
+                atomicAdd(h_acc + (size_t)p * 2 * R_out + chn, __uint_as_float(gt[jj]));
+                atomicAdd(h_acc + (size_t)p * 2 * R_out + R_out + chn, __uint_as_float(up[jj]));
+              } else {
+                out16[(size_t)p * R_out + chn] =
+                    silu_mul_bf16(__uint_as_float(gt[jj]), __uint_as_float(up[jj]));
+              }
             }
           }
         }
@@ -525,6 +569,28 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&acc_empty[acc]));
+      if (MODE == 0 && ksplit > 1) {
+        // The last split of this tile to finish (an atomic count after a fence;
+        // nobody waits) reads the summed h back and writes a.
+        __threadfence();
+        epilogue_bar_sync();
+        if (et == 0) *split_last = atomicAdd(&tile_cnt[b * n_ctiles + c], 1) == ksplit - 1;
+        epilogue_bar_sync();
+        if (*split_last) {
+          __threadfence();
+          const int chn = c * kTileM + q * 32 + lane;
+          if (chn < R_out) {
+            for (int j = half; j < N; j += 2) {
+              const int p = dst_row[j];
+              if (p < 0) continue;
+              const float gs = __ldcg(h_acc + (size_t)p * 2 * R_out + chn);
+              const float us = __ldcg(h_acc + (size_t)p * 2 * R_out + R_out + chn);
+              out16[(size_t)p * R_out + chn] = silu_mul_bf16(gs, us);
+            }
+          }
+          if (et == 0) tile_cnt[b * n_ctiles + c] = 0;
+        }
+      }
     }
   }
   tc_fence_before();
@@ -550,7 +616,7 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
 
 // 3-D map over weights [E][rows][K] (bf16, K contiguous), box 64 x 128 x 1,
 // 128-byte swizzle; out-of-range rows and columns read as zero.
-cudaError_t make_weight_map(CUtensorMap *map, const uint16_t *w, int K, int rows, int E) {
+cudaError_t encode_weight_map(CUtensorMap *map, const uint16_t *w, int K, int rows, int E) {
   PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode_fn();
   if (encode == nullptr) return cudaErrorNotSupported;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows),
@@ -566,48 +632,82 @@ cudaError_t make_weight_map(CUtensorMap *map, const uint16_t *w, int K, int rows
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Encoded maps, keyed by (device, address, shape): a layer's weights keep
+// their map from call to call, so the host encodes each one once.
+struct MapEntry {
+  int dev;
+  const void *ptr;
+  int K, rows, E;
+  CUtensorMap map;
+};
+std::mutex g_map_mutex;
+MapEntry g_maps[128];
+int g_map_next = 0, g_map_count = 0;
+
+cudaError_t make_weight_map(CUtensorMap *map, const uint16_t *w, int K, int rows, int E) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  std::lock_guard<std::mutex> lock(g_map_mutex);
+  for (int i = 0; i < g_map_count; ++i) {
+    const MapEntry &m = g_maps[i];
+    if (m.dev == dev && m.ptr == w && m.K == K && m.rows == rows && m.E == E) {
+      *map = m.map;
+      return cudaSuccess;
+    }
+  }
+  err = encode_weight_map(map, w, K, rows, E);
+  if (err != cudaSuccess) return err;
+  MapEntry &m = g_maps[g_map_next];
+  m = MapEntry{dev, w, K, rows, E, *map};
+  g_map_next = (g_map_next + 1) % 128;
+  if (g_map_count < 128) ++g_map_count;
+  return cudaSuccess;
+}
+
+// Everything a launch of k_gemm_tc needs besides the weight map.
+struct TcArgs {
+  const uint16_t *src;
+  int src_rows;
+  const int32_t *sorted_ids, *expert_ids, *n_post;
+  const float *vec;
+  int P, top_k, E, K, R_out, a_rows, B, cap, n_ctiles, ksplit;
+  float *h_acc;
+  int *tile_cnt;
+  uint16_t *out16;
+  float *y_acc;
+  int H_out;
+  int *status;
+  long max_blocks;  // host-side bound on the blocks (tiles = blocks * n_ctiles * ksplit)
+};
+
 template <int N, int MODE>
-cudaError_t launch_tc_n(const CUtensorMap &map_w, const uint16_t *src, int src_rows,
-                        const int32_t *sorted_ids, const int32_t *expert_ids, const int32_t *n_post,
-                        const float *vec, int P, int top_k, int E, int K, int R_out, int a_rows,
-                        int B, int cap, uint16_t *out16, float *y_acc, int H_out, int *status,
-                        int n_ctiles, long max_blocks, cudaStream_t s) {
+cudaError_t launch_tc_n(const CUtensorMap &map_w, const TcArgs &a, cudaStream_t s) {
   using Cfg = TcConfig<N>;
   auto kern = k_gemm_tc<N, MODE>;
-  cudaError_t err = cudaFuncSetAttribute(reinterpret_cast<const void *>(kern),
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(Cfg::kSmemBytes));
+  cudaError_t err = ensure_smem_limit(reinterpret_cast<const void *>(kern), Cfg::kSmemBytes);
   if (err != cudaSuccess) return err;
   // persistent: one CTA per SM at most, each walking the tile list with stride gridDim.x
-  const int grid = static_cast<int>(std::min<long>(max_blocks * n_ctiles, num_sms()));
+  const int grid = static_cast<int>(
+      std::min<long>(a.max_blocks * a.n_ctiles * a.ksplit, num_sms()));
   if (grid <= 0) return cudaSuccess;
-  kern<<<grid, kTcThreads, Cfg::kSmemBytes, s>>>(map_w, src, src_rows, sorted_ids, expert_ids,
-                                                 n_post, vec, P, top_k, E, K, R_out, a_rows, B, cap,
-                                                 n_ctiles, out16, y_acc, H_out, status);
+  kern<<<grid, kTcThreads, Cfg::kSmemBytes, s>>>(
+      map_w, a.src, a.src_rows, a.sorted_ids, a.expert_ids, a.n_post, a.vec, a.P, a.top_k, a.E,
+      a.K, a.R_out, a.a_rows, a.B, a.cap, a.n_ctiles, a.ksplit, a.h_acc, a.tile_cnt, a.out16,
+      a.y_acc, a.H_out, a.status);
   return cudaGetLastError();
 }
 
 template <int MODE>
-cudaError_t launch_tc(int N, const CUtensorMap &map_w, const uint16_t *src, int src_rows,
-                      const int32_t *sorted_ids, const int32_t *expert_ids, const int32_t *n_post,
-                      const float *vec, int P, int top_k, int E, int K, int R_out, int a_rows, int B,
-                      int cap, uint16_t *out16, float *y_acc, int H_out, int *status, int n_ctiles,
-                      long max_blocks, cudaStream_t s) {
-#define MOE_TC_CASE(NN)                                                                          \
-  case NN:                                                                                       \
-    return launch_tc_n<NN, MODE>(map_w, src, src_rows, sorted_ids, expert_ids, n_post, vec,     \
-                                 P, top_k, E, K, R_out, a_rows, B, cap, out16, y_acc, H_out,    \
-                                 status, n_ctiles, max_blocks, s)
+cudaError_t launch_tc(int N, const CUtensorMap &map_w, const TcArgs &a, cudaStream_t s) {
   switch (N) {
-    MOE_TC_CASE(16);
-    MOE_TC_CASE(32);
-    MOE_TC_CASE(64);
-    MOE_TC_CASE(128);
-    MOE_TC_CASE(256);
-    default:
-      return cudaErrorInvalidValue;
+    case 16: return launch_tc_n<16, MODE>(map_w, a, s);
+    case 32: return launch_tc_n<32, MODE>(map_w, a, s);
+    case 64: return launch_tc_n<64, MODE>(map_w, a, s);
+    case 128: return launch_tc_n<128, MODE>(map_w, a, s);
+    case 256: return launch_tc_n<256, MODE>(map_w, a, s);
+    default: return cudaErrorInvalidValue;
   }
-#undef MOE_TC_CASE
 }
 
 }  // namespace
@@ -616,27 +716,68 @@ bool tc_supports_block(int B) { return B == 16 || B == 32 || B == 64 || B == 128
 
 cudaError_t launch_tc_w13_act(const uint16_t *x, const uint16_t *w13, const int32_t *sorted_ids,
                               const int32_t *expert_ids, const int32_t *n_post, int P, int top_k,
-                              int E, int H, int I, int B, int cap, uint16_t *a, int *status,
-                              cudaStream_t s) {
+                              int E, int H, int I, int B, int cap, uint16_t *a, int ksplit,
+                              float *h_acc, int *tile_cnt, int *status, cudaStream_t s) {
   CUtensorMap map_w;
   cudaError_t err = make_weight_map(&map_w, w13, H, 2 * I, E);
   if (err != cudaSuccess) return err;
-  const int M = (P + top_k - 1) / top_k;
-  const int n_ctiles = (I + kTileM - 1) / kTileM;
-  return launch_tc<0>(B, map_w, x, M, sorted_ids, expert_ids, n_post, nullptr, P, top_k, E, H,
-                      I, 2 * I, B, cap, a, nullptr, 0, status, n_ctiles, cap / B, s);
+  const int nk = (H + kBK - 1) / kBK;
+  if (ksplit < 1 || ksplit > nk || h_acc == nullptr || tile_cnt == nullptr) ksplit = 1;
+  TcArgs args{};
+  args.src = x;
+  args.src_rows = (P + top_k - 1) / top_k;
+  args.sorted_ids = sorted_ids;
+  args.expert_ids = expert_ids;
+  args.n_post = n_post;
+  args.P = P;
+  args.top_k = top_k;
+  args.E = E;
+  args.K = H;
+  args.R_out = I;
+  args.a_rows = 2 * I;
+  args.B = B;
+  args.cap = cap;
+  args.n_ctiles = (I + kTileM - 1) / kTileM;
+  args.ksplit = ksplit;
+  args.h_acc = h_acc;
+  args.tile_cnt = tile_cnt;
+  args.out16 = a;
+  args.status = status;
+  args.max_blocks = cap / B;
+  return launch_tc<0>(B, map_w, args, s);
 }
 
 cudaError_t launch_tc_w2_combine(const uint16_t *a, const uint16_t *w2, const int32_t *sorted_ids,
                                  const int32_t *expert_ids, const int32_t *n_post,
                                  const float *topk_weights, int P, int top_k, int E, int H, int I,
-                                 int B, int cap, float *y_acc, int *status, cudaStream_t s) {
+                                 int B, int cap, float *y_acc, int ksplit, int *status,
+                                 cudaStream_t s) {
   CUtensorMap map_w;
   cudaError_t err = make_weight_map(&map_w, w2, I, H, E);
   if (err != cudaSuccess) return err;
-  const int n_ctiles = (H + 2 * kTileM - 1) / (2 * kTileM);
-  return launch_tc<1>(B, map_w, a, P, sorted_ids, expert_ids, n_post, topk_weights, P, top_k,
-                      E, I, H, H, B, cap, nullptr, y_acc, H, status, n_ctiles, cap / B, s);
+  const int nk = (I + kBK - 1) / kBK;
+  TcArgs args{};
+  args.src = a;
+  args.src_rows = P;
+  args.sorted_ids = sorted_ids;
+  args.expert_ids = expert_ids;
+  args.n_post = n_post;
+  args.vec = topk_weights;
+  args.P = P;
+  args.top_k = top_k;
+  args.E = E;
+  args.K = I;
+  args.R_out = H;
+  args.a_rows = H;
+  args.B = B;
+  args.cap = cap;
+  args.n_ctiles = (H + 2 * kTileM - 1) / (2 * kTileM);
+  args.ksplit = std::max(1, std::min(ksplit, nk));  // the combine adds partial sums anyway
+  args.y_acc = y_acc;
+  args.H_out = H;
+  args.status = status;
+  args.max_blocks = cap / B;
+  return launch_tc<1>(B, map_w, args, s);
 }
 
 cudaError_t launch_tc_router(const uint16_t *x, const uint16_t *w_router, const float *bias, int M,
@@ -645,9 +786,23 @@ cudaError_t launch_tc_router(const uint16_t *x, const uint16_t *w_router, const 
   cudaError_t err = make_weight_map(&map_w, w_router, H, E, 1);
   if (err != cudaSuccess) return err;
   const int N = 128;
-  const int n_ctiles = (E + 2 * kTileM - 1) / (2 * kTileM);
-  return launch_tc<2>(N, map_w, x, M, nullptr, nullptr, nullptr, bias, M, 1, 1, H, E, E, N, 0,
-                      logits, nullptr, 0, status, n_ctiles, (M + N - 1) / N, s);
+  TcArgs args{};
+  args.src = x;
+  args.src_rows = M;
+  args.vec = bias;
+  args.P = M;
+  args.top_k = 1;
+  args.E = 1;
+  args.K = H;
+  args.R_out = E;
+  args.a_rows = E;
+  args.B = N;
+  args.n_ctiles = (E + 2 * kTileM - 1) / (2 * kTileM);
+  args.ksplit = 1;
+  args.out16 = logits;
+  args.status = status;
+  args.max_blocks = (M + N - 1) / N;
+  return launch_tc<2>(N, map_w, args, s);
 }
 
 }  // namespace moe

@@ -21,6 +21,7 @@
 // blocks is read on the device from num_tokens_post_padded, so no host
 // synchronisation is needed and the launch can be captured in a CUDA graph.
 #include <algorithm>
+#include <mutex>
 
 #include "moe_internal.cuh"
 
@@ -300,10 +301,38 @@ int num_sms() {
   return cached[dev];
 }
 
-static cudaError_t set_smem_attr(const void *fn, size_t bytes) {
+namespace {
+struct SmemLimit {
+  const void *fn;
+  int dev;
+  size_t bytes;
+};
+std::mutex g_smem_mutex;
+SmemLimit g_smem_limits[256];
+int g_smem_count = 0;
+}  // namespace
+
+cudaError_t ensure_smem_limit(const void *fn, size_t bytes) {
   if (bytes <= 48 * 1024) return cudaSuccess;
-  return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  std::lock_guard<std::mutex> lock(g_smem_mutex);
+  for (int i = 0; i < g_smem_count; ++i)
+    if (g_smem_limits[i].fn == fn && g_smem_limits[i].dev == dev && g_smem_limits[i].bytes >= bytes)
+      return cudaSuccess;
+  err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (err != cudaSuccess) return err;
+  for (int i = 0; i < g_smem_count; ++i)
+    if (g_smem_limits[i].fn == fn && g_smem_limits[i].dev == dev) {
+      g_smem_limits[i].bytes = bytes;
+      return cudaSuccess;
+    }
+  if (g_smem_count < 256) g_smem_limits[g_smem_count++] = {fn, dev, bytes};
+  return cudaSuccess;
 }
+
+static cudaError_t set_smem_attr(const void *fn, size_t bytes) { return ensure_smem_limit(fn, bytes); }
 
 cudaError_t launch_gemv_w13_act(const uint16_t *x, const uint16_t *w13, const int32_t *sorted_ids,
                                 const int32_t *expert_ids, const int32_t *n_post, int P, int top_k,

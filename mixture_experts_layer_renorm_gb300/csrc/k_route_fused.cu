@@ -29,7 +29,7 @@ namespace {
 
 constexpr int kFusedThreads = kAlignThreads;  // 16 warps: the align needs 512 threads
 constexpr int kFusedWarps = kFusedThreads / 32;
-constexpr int kFusedKChunk = 1024;             // x columns staged per chunk
+constexpr int kFusedKChunk = 2048;             // x columns staged per chunk
 constexpr int kFusedVec = kFusedKChunk / 8 / 32;  // 16-byte router loads per lane per chunk
 
 template <int VPL>
@@ -68,6 +68,16 @@ k_route_fused(const uint16_t *__restrict__ x, const uint16_t *__restrict__ w_rou
     for (int kc = 0; kc < H; kc += kFusedKChunk) {
       const int kw = min(kFusedKChunk, H - kc);
       const int vrow = kw / 8;
+      // the router row's loads go out first, so their latency overlaps the x staging
+      uint4 wv[kFusedVec];
+      if (e < E) {
+        const uint16_t *wrow = w_router + (size_t)e * H + kc;
+#pragma unroll
+        for (int u = 0; u < kFusedVec; ++u) {
+          const int c = lane + 32 * u;
+          wv[u] = c < vrow ? ld_stream_16(wrow + c * 8) : make_uint4(0, 0, 0, 0);
+        }
+      }
       __syncthreads();
       for (int v = tid; v < kRouteFusedTok * vrow; v += kFusedThreads) {
         const int r = v / vrow, c = v - r * vrow;
@@ -77,13 +87,6 @@ k_route_fused(const uint16_t *__restrict__ x, const uint16_t *__restrict__ w_rou
       }
       __syncthreads();
       if (e < E) {
-        const uint16_t *wrow = w_router + (size_t)e * H + kc;
-        uint4 wv[kFusedVec];
-#pragma unroll
-        for (int u = 0; u < kFusedVec; ++u) {
-          const int c = lane + 32 * u;
-          wv[u] = c < vrow ? ld_stream_16(wrow + c * 8) : make_uint4(0, 0, 0, 0);
-        }
 #pragma unroll
         for (int u = 0; u < kFusedVec; ++u) {
           const int c = lane + 32 * u;
@@ -167,9 +170,7 @@ cudaError_t launch_route_fused(const uint16_t *x, const uint16_t *w_router, cons
   const long zn4 = zero_buf != nullptr ? zero_n / 4 : 0;
 #define MOE_FUSED_CASE(V)                                                                          \
   do {                                                                                             \
-    cudaError_t err = cudaFuncSetAttribute(reinterpret_cast<const void *>(k_route_fused<V>),       \
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,            \
-                                           static_cast<int>(smem));                                \
+    cudaError_t err = ensure_smem_limit(reinterpret_cast<const void *>(k_route_fused<V>), smem);   \
     if (err != cudaSuccess) return err;                                                            \
     k_route_fused<V><<<grid, kFusedThreads, smem, s>>>(                                            \
         x, w_router, bias, logits_in, M, E, H, top_k, renormalize, B, logits_ws, topk_ids, topk_w, \

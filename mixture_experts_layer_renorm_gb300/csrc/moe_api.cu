@@ -5,6 +5,7 @@
 // moe_get_device_status); every launch goes to the caller's stream, so the
 // calls can be captured in a CUDA graph.
 #include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -47,8 +48,12 @@ long capacity(long P, int E, int B) {
 // Workspace regions, each 256-byte aligned.  The status word is always at
 // offset 0 so that moe_get_device_status can find it from the pointer alone.
 struct WsLayout {
-  size_t status, logits, ids, wts, sorted, eids, offsets, npost, hist, a, yacc, total;
+  size_t status, logits, ids, wts, sorted, eids, offsets, npost, hist, a, yacc, hacc, tcnt, total;
 };
+
+// Decode-sized batches (those the fused routing kernel serves) may split
+// GEMM 1's K range; they reserve its fp32 partial sums and tile counters.
+constexpr int kSplitMaxTokens = 256;
 
 WsLayout ws_layout(int M, int E, int top_k, int H, int I, int B) {
   const long P = static_cast<long>(M) * top_k;
@@ -71,6 +76,10 @@ WsLayout ws_layout(int M, int E, int top_k, int H, int I, int B) {
   w.hist = take(sizeof(int32_t) * static_cast<size_t>(moe::align_hist_entries(P, E)));
   w.a = take(sizeof(uint16_t) * static_cast<size_t>(P) * I);
   w.yacc = take(sizeof(float) * static_cast<size_t>(M) * H);
+  // h_acc and the tile counters directly follow y_acc: one span to clear
+  const bool split = M <= kSplitMaxTokens;
+  w.hacc = take(split ? sizeof(float) * static_cast<size_t>(P) * 2 * I : 0);
+  w.tcnt = take(split ? sizeof(int32_t) * static_cast<size_t>(cap / B) * ((I + 127) / 128) : 0);
   w.total = o;
   return w;
 }
@@ -162,15 +171,42 @@ moe_status_t run_route(const uint16_t *x, const uint16_t *w_router, const uint16
                                        npost, hist, control, s));
 }
 
+// Splits of each tile's K range for a grouped GEMM with n_ctiles weight tiles
+// per block: decode batches can have fewer tiles than SMs, or a last wave
+// that leaves most SMs idle.  The block count is estimated on the host as the
+// expected number of distinct experts, E (1 - (1 - top_k/E)^M).
+int pick_ksplit(int M, int E, int top_k, int n_ctiles, int nk) {
+  if (M > kSplitMaxTokens) return 1;
+  const double D = E * (1.0 - std::pow(1.0 - static_cast<double>(top_k) / E, M));
+  const double tiles = std::max(1.0, std::ceil(D)) * n_ctiles;
+  const double sms = moe::num_sms();
+  int best = 1;
+  double best_score = 0;
+  for (int ks = 1; ks <= 4 && ks <= nk; ++ks) {
+    const double units = tiles * ks;
+    const double eff = units / (std::ceil(units / sms) * sms);  // busy fraction of the waves
+    const double score = eff / (1.0 + 0.03 * (ks - 1));          // a split costs a little
+    if (score > best_score + 1e-9) {
+      best_score = score;
+      best = ks;
+    }
+  }
+  return best;
+}
+
 moe_status_t run_gemm1(const uint16_t *x, const uint16_t *w13, const int32_t *sorted,
                        const int32_t *eids, const int32_t *npost, int M, int top_k, int E, int H,
-                       int I, int B, uint16_t *a, int *status, cudaStream_t s) {
+                       int I, int B, uint16_t *a, float *h_acc, int *tile_cnt, int *status,
+                       cudaStream_t s) {
   const long P = static_cast<long>(M) * top_k;
   const int cap = static_cast<int>(capacity(P, E, B));
   switch (pick_path(M, E, top_k, B)) {
-    case GemmPath::kTensorCore:
+    case GemmPath::kTensorCore: {
+      const int ks = h_acc != nullptr ? pick_ksplit(M, E, top_k, (I + 127) / 128, (H + 63) / 64) : 1;
       return cuda_status(moe::launch_tc_w13_act(x, w13, sorted, eids, npost, static_cast<int>(P),
-                                                top_k, E, H, I, B, cap, a, status, s));
+                                                top_k, E, H, I, B, cap, a, ks, h_acc, tile_cnt,
+                                                status, s));
+    }
     case GemmPath::kGemv:
     default:
       return cuda_status(moe::launch_gemv_w13_act(x, w13, sorted, eids, npost, static_cast<int>(P),
@@ -185,10 +221,12 @@ moe_status_t run_gemm2(const uint16_t *a, const uint16_t *w2, const int32_t *sor
   const long P = static_cast<long>(M) * top_k;
   const int cap = static_cast<int>(capacity(P, E, B));
   switch (pick_path(M, E, top_k, B)) {
-    case GemmPath::kTensorCore:
+    case GemmPath::kTensorCore: {
+      const int ks = pick_ksplit(M, E, top_k, (H + 255) / 256, (I + 63) / 64);
       return cuda_status(moe::launch_tc_w2_combine(a, w2, sorted, eids, npost, wts,
                                                    static_cast<int>(P), top_k, E, H, I, B, cap,
-                                                   yacc, status, s));
+                                                   yacc, ks, status, s));
+    }
     case GemmPath::kGemv:
     default:
       return cuda_status(moe::launch_gemv_w2_combine(a, w2, sorted, eids, npost, wts,
@@ -234,9 +272,14 @@ long moe_align_capacity(int M, int top_k, int E, int block_size_m) {
 size_t moe_workspace_size(int M_max, int E, int top_k, int H, int I, int block_size_m) {
   if (check_shapes(M_max, E, top_k, H, I) != MOE_OK) return 0;
   if (block_size_m != 0 && !valid_block_size(block_size_m)) return 0;
-  if (block_size_m != 0) return ws_layout(M_max, E, top_k, H, I, block_size_m).total;
+  // a smaller batch may reserve split-K scratch that M_max does not
+  const int M_split = std::min(M_max, kSplitMaxTokens);
   size_t best = 0;
-  for (int B : {16, 32, 64, 128, 256}) best = std::max(best, ws_layout(M_max, E, top_k, H, I, B).total);
+  for (int B : {16, 32, 64, 128, 256}) {
+    if (block_size_m != 0 && B != block_size_m) continue;
+    best = std::max(best, ws_layout(M_max, E, top_k, H, I, B).total);
+    best = std::max(best, ws_layout(M_split, E, top_k, H, I, B).total);
+  }
   return best;
 }
 
@@ -302,7 +345,7 @@ moe_status_t moe_grouped_gemm_w13_act(const moe_bf16_t *x, const moe_bf16_t *w13
     return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w13)) return MOE_ERR_INVALID_ARG;
   return run_gemm1(x, w13, sorted_token_ids, expert_ids, num_tokens_post_padded, M, top_k, E, H, I,
-                   block_size_m, a, lib_status(), stream);
+                   block_size_m, a, nullptr, nullptr, lib_status(), stream);
 }
 
 moe_status_t moe_grouped_gemm_w2_combine(const moe_bf16_t *a, const moe_bf16_t *w2,
@@ -366,13 +409,21 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *w_router,
   int32_t *npost = at<int32_t>(ws, L.npost);
   float *yacc = at<float>(ws, L.yacc);
   const long yn = static_cast<long>(M) * H;
+  // the fused routing kernel clears y_acc, and h_acc and the tile counters
+  // behind it when GEMM 1 will split its K range (one span)
+  const bool want_split = L.hacc != L.tcnt && pick_path(M, E, top_k, B) == GemmPath::kTensorCore &&
+                          pick_ksplit(M, E, top_k, (I + 127) / 128, (H + 63) / 64) > 1;
+  const long zn = want_split ? static_cast<long>((L.total - L.yacc) / sizeof(float)) : yn;
   bool zeroed = false;
   st = run_route(x, w_router, router_logits, router_bias, M, E, top_k, H, renormalize, B,
                  at<uint16_t>(ws, L.logits), ids, wts, sorted, eids, offs, npost,
-                 at<int32_t>(ws, L.hist), status, yacc, yn, &zeroed, stream);
+                 at<int32_t>(ws, L.hist), status, yacc, zn, &zeroed, stream);
   if (st != MOE_OK) return st;
   uint16_t *a = at<uint16_t>(ws, L.a);
-  st = run_gemm1(x, w13, sorted, eids, npost, M, top_k, E, H, I, B, a, status, stream);
+  const bool split_ok = zeroed && want_split;  // scratch reserved and cleared
+  st = run_gemm1(x, w13, sorted, eids, npost, M, top_k, E, H, I, B, a,
+                 split_ok ? at<float>(ws, L.hacc) : nullptr,
+                 split_ok ? at<int>(ws, L.tcnt) : nullptr, status, stream);
   if (st != MOE_OK) return st;
   if (!zeroed && cudaMemsetAsync(yacc, 0, sizeof(float) * static_cast<size_t>(yn), stream) != cudaSuccess)
     return MOE_ERR_CUDA;

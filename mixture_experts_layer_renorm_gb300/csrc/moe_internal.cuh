@@ -93,12 +93,16 @@ cudaError_t launch_gemv_w2_combine(const uint16_t *a, const uint16_t *w2, const 
 bool tc_supports_block(int B);
 cudaError_t launch_tc_w13_act(const uint16_t *x, const uint16_t *w13, const int32_t *sorted_ids,
                               const int32_t *expert_ids, const int32_t *n_post, int P, int top_k,
-                              int E, int H, int I, int B, int cap, uint16_t *a, int *status,
-                              cudaStream_t s);
+                              int E, int H, int I, int B, int cap, uint16_t *a, int ksplit,
+                              float *h_acc, int *tile_cnt, int *status, cudaStream_t s);
+// ksplit > 1 splits each tile's K range across CTAs (GEMM 1: partial sums go
+// through h_acc [P, 2I] fp32 and tile_cnt [cap/B * ceil(I/128)] ints, both zero
+// on entry; GEMM 2 adds its partial sums into y_acc directly).
 cudaError_t launch_tc_w2_combine(const uint16_t *a, const uint16_t *w2, const int32_t *sorted_ids,
                                  const int32_t *expert_ids, const int32_t *n_post,
                                  const float *topk_weights, int P, int top_k, int E, int H, int I,
-                                 int B, int cap, float *y_acc, int *status, cudaStream_t s);
+                                 int B, int cap, float *y_acc, int ksplit, int *status,
+                                 cudaStream_t s);
 
 // S0 on the tensor cores: logits [M,E] = bf16(x . w_router^T + bias), blocks of 128 tokens.
 cudaError_t launch_tc_router(const uint16_t *x, const uint16_t *w_router, const float *bias, int M,
@@ -120,5 +124,10 @@ cudaError_t launch_route_fused(const uint16_t *x, const uint16_t *w_router, cons
                                int *status, float *zero_buf, long zero_n, cudaStream_t s);
 
 int num_sms();
+
+// Raises a kernel's dynamic shared-memory limit to at least `bytes` on the
+// current device.  The driver call happens once per (kernel, device, size);
+// later launches only look the pair up in a table.
+cudaError_t ensure_smem_limit(const void *fn, size_t bytes);
 
 }  // namespace moe

@@ -274,12 +274,13 @@ size_t moe_workspace_size(int M_max, int E, int top_k, int H, int I, int block_s
   if (block_size_m != 0 && !valid_block_size(block_size_m)) return 0;
   // a smaller batch may reserve split-K scratch that M_max does not
   const int M_split = std::min(M_max, kSplitMaxTokens);
+  auto need = [&](int B) {
+    return std::max(ws_layout(M_max, E, top_k, H, I, B).total,
+                    ws_layout(M_split, E, top_k, H, I, B).total);
+  };
+  if (block_size_m != 0) return need(block_size_m);
   size_t best = 0;
-  for (int B : {16, 32, 64, 128, 256}) {
-    if (block_size_m != 0 && B != block_size_m) continue;
-    best = std::max(best, ws_layout(M_max, E, top_k, H, I, B).total);
-    best = std::max(best, ws_layout(M_split, E, top_k, H, I, B).total);
-  }
+  for (int B : {16, 32, 64, 128, 256}) best = std::max(best, need(B));
   return best;
 }
 

@@ -60,6 +60,10 @@ def test_sizes_and_capacity(lib):
     assert lib.moe_workspace_size(64, 128, 8, 2047, 768, 16) == 0   # H not a multiple of 16
     assert lib.moe_workspace_size(64, 2000, 8, 2048, 768, 16) == 0  # E > 1024
     assert lib.moe_workspace_size(64, 128, 8, 2048, 768, 257) == 0  # block size > 256
+    for B in (1, 4, 8, 24, 200):                                    # any block size in [1, 256]
+        assert moe.moe_workspace_size(3, 4, 2, 128, 64, B) > 0
+    # a batch below M_max may need more (it reserves split-K scratch): the size covers it
+    assert moe.moe_workspace_size(300, 128, 8, 2048, 768, 16) >= moe.moe_workspace_size(256, 128, 8, 2048, 768, 16)
     for M in (1, 8, 64, 512, 4096, 16384):
         assert moe.moe_pick_block_size(M, 128, 8, 2048, 768) in (16, 32, 64, 128, 256)
 

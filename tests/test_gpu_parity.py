@@ -11,6 +11,8 @@ checks that the GPU logit is the rounding of a value within the fp32
 summation error bound of the exact dot product, and then compares the layer
 outputs only on tokens whose routing agrees.
 """
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -18,7 +20,7 @@ import torch
 import mixture_experts_layer_renorm_gb300 as moe
 import oracle
 import synth
-from _util import (W_ABS, assert_close_bf16, bits, f64_of_bits, fp32_dot_error_bound,
+from _util import (W_ABS, Y_MAX_REL, Y_MEAN_REL, assert_close_bf16, bits, f64_of_bits, fp32_dot_error_bound,
                    tensor_of_bits)
 
 pytestmark = pytest.mark.gpu
@@ -393,7 +395,12 @@ def test_stack_chain_against_the_oracle_on_sampled_tokens():
                 live[s_i] = False
                 first_diff[s_i] = l
                 continue
-            assert_close_bf16(g_y[s_i:s_i + 1], oy[s_i:s_i + 1], f"y layer {l} token {sample[s_i]}")
+            # each side rounds every layer's y to bf16 from its own input; the
+            # residual carries those differences forward, so they add up like
+            # a random walk: the tolerance grows with sqrt(depth) from layer 0's
+            grow = math.sqrt(1.0 + l / 4.0)
+            assert_close_bf16(g_y[s_i:s_i + 1], oy[s_i:s_i + 1], f"y layer {l} token {sample[s_i]}",
+                              max_rel=Y_MAX_REL * grow, mean_rel=Y_MEAN_REL * grow)
             compared += 1
         ox, cur = oy, y
         del wt

@@ -349,14 +349,20 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
 
   if (warp == 0) {
     // ------------------------------------------------------------ weight tiles (TMA)
+    // The next tile's expert id is loaded while this tile's copies go out.  An
+    // id outside [0, E) needs no test here: its tiles lie outside the map and
+    // read as zeros, and the epilogue writes nothing for that block.
     if (lane == 0) {
       int g = 0;
       bool stop = false;
-      for (int t = blockIdx.x; t < n_tiles && !stop; t += gridDim.x) {
+      int t = blockIdx.x;
+      int e_next = MODE == 2 ? 0 : expert_ids[tile_coord(t, n_ctiles, ksplit, nk).b];
+      for (; t < n_tiles && !stop; t += gridDim.x) {
         const TileCoord tc = tile_coord(t, n_ctiles, ksplit, nk);
-        const int b = tc.b, c = tc.c;
-        const int e = MODE == 2 ? 0 : expert_ids[b];
-        if (e < 0 || e >= E) continue;  // every role skips this tile
+        const int c = tc.c;
+        const int e = e_next;
+        const int tn = t + static_cast<int>(gridDim.x);
+        if (MODE != 2 && tn < n_tiles) e_next = expert_ids[tile_coord(tn, n_ctiles, ksplit, nk).b];
         const int row0 = MODE == 0 ? c * kTileM : c * 2 * kTileM;
         const int row1 = MODE == 0 ? R_out + c * kTileM : c * 2 * kTileM + kTileM;
         const bool two = MODE == 0 || row1 < a_rows;
@@ -392,26 +398,37 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
     // straight on to the next stage.
     const int gt = threadIdx.x - kGatherWarp0 * 32;
     const int ch = gt & 7;
+    // Entries of sorted_token_ids (MODE 2: token ids) of this thread's rows in
+    // tile t; the next tile's are loaded while this tile's rows are copied.
+    auto fetch_ids = [&](int t, int (&ids)[Cfg::kChunksPerThread]) {
+      const int b = tile_coord(t, n_ctiles, ksplit, nk).b;
+#pragma unroll
+      for (int u = 0; u < Cfg::kChunksPerThread; ++u) {
+        const int r = (gt >> 3) + 16 * u;
+        if (MODE == 2) ids[u] = b * N + r;
+        else ids[u] = r < B ? sorted_ids[(size_t)b * B + r] : -1;
+      }
+    };
+    int ids_next[Cfg::kChunksPerThread];
+    fetch_ids(blockIdx.x, ids_next);
     int g = 0;
     bool stop = false;
     for (int t = blockIdx.x; t < n_tiles && !stop; t += gridDim.x) {
       const TileCoord tc = tile_coord(t, n_ctiles, ksplit, nk);
-      const int b = tc.b;
-      const int e = MODE == 2 ? 0 : expert_ids[b];
-      if (e < 0 || e >= E) continue;
       int rowv[Cfg::kChunksPerThread];
 #pragma unroll
       for (int u = 0; u < Cfg::kChunksPerThread; ++u) {
-        const int r = (gt >> 3) + 16 * u;
+        const int p = ids_next[u];
         int row = -1;
         if (MODE == 2) {
-          if (b * N + r < src_rows) row = b * N + r;
-        } else if (r < B) {
-          const int p = sorted_ids[(size_t)b * B + r];
-          if (p >= 0 && p < P) row = MODE == 0 ? p / top_k : p;
+          if (p < src_rows) row = p;
+        } else if (p >= 0 && p < P) {
+          row = MODE == 0 ? p / top_k : p;
         }
         rowv[u] = row;
       }
+      const int tn = t + static_cast<int>(gridDim.x);
+      if (tn < n_tiles) fetch_ids(tn, ids_next);
       for (int kb = tc.kb0; kb < tc.kb1; ++kb, ++g) {
         const int s = g % S;
         if (!wait_bounded(smem_u32(&empty[s]), ((g / S) & 1) ^ 1, abort, status)) {
@@ -440,10 +457,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
       bool stop = false;
       for (int t = blockIdx.x; t < n_tiles && !stop; t += gridDim.x) {
         const TileCoord tc = tile_coord(t, n_ctiles, ksplit, nk);
-        const int b = tc.b, c = tc.c;
-        const int e = MODE == 2 ? 0 : expert_ids[b];
-        if (e < 0 || e >= E) continue;
-        const bool two = MODE == 0 || c * 2 * kTileM + kTileM < a_rows;
+        const bool two = MODE == 0 || tc.c * 2 * kTileM + kTileM < a_rows;
         const int acc = i % Cfg::kAccBufs;
         const uint32_t use = i / Cfg::kAccBufs;
         ++i;
@@ -484,8 +498,9 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
     for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
       const TileCoord tc = tile_coord(t, n_ctiles, ksplit, nk);
       const int b = tc.b, c = tc.c;
-      const int e = MODE == 2 ? 0 : expert_ids[b];
-      if (e < 0 || e >= E) continue;
+      // a block whose expert id lies outside [0, E) is computed (on zero
+      // weights) but writes nothing
+      const bool e_ok = MODE == 2 || (static_cast<unsigned>(expert_ids[b]) < static_cast<unsigned>(E));
       const bool two = MODE == 0 || c * 2 * kTileM + kTileM < a_rows;
       const int acc = i % Cfg::kAccBufs;
       const uint32_t use = i / Cfg::kAccBufs;
@@ -497,7 +512,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
         float wgt = 0.f;
         if (MODE == 2) {
           if (b * N + j < src_rows) d = b * N + j;
-        } else if (j < B) {
+        } else if (j < B && e_ok) {
           const int p = sorted_ids[(size_t)b * B + j];
           if (p >= 0 && p < P) {
             d = MODE == 0 ? p : p / top_k;

@@ -22,6 +22,7 @@ path); the reported time is the max over ranks.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -446,6 +447,8 @@ def ours(args):
         dist.init_process_group("nccl", device_id=device)
     moe.load_library(build_if_missing=True)
     w = synth.WORKLOADS[WORKLOAD_CFG[args.workload]]
+    if args.block_size:
+        w = dataclasses.replace(w, block_size_m=args.block_size)
     M = args.M or max(w.Ms)
     peaks = load_peaks()
     stream = torch.cuda.Stream(device=device)
@@ -605,6 +608,8 @@ def main(argv=None):
     ap.add_argument("--no-points", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-tokens", type=int, default=64)
+    ap.add_argument("--block-size", type=int, default=0,
+                    help="block_size_m of the align and the grouped GEMMs (default: the library's pick)")
     ap.add_argument("--graph", action="store_true",
                     help="stack workload: replay each 64-layer step from a CUDA graph")
     args = ap.parse_args(argv)

@@ -217,17 +217,31 @@ __host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N) {
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-template <int N>
+template <int N, int MODE>
 struct TcConfig {
+  // Wide tiles (N = 256 token columns, GEMMs 1 and 2): ONE 128-row weight tile
+  // per stage -- for GEMM 1 its 64 gate rows over the matching 64 up rows -- so
+  // one accumulator takes N TMEM columns and two of them fit.  An N = 256 MMA
+  // keeps the tensor pipe busy where a chain of dependent N = 128 MMAs into
+  // one accumulator does not.  Narrower tiles use two 128-row weight tiles
+  // (GEMM 1: gate and up, GEMM 2 and the router: 256 rows).
+  static constexpr bool kWide = N == 256 && MODE != 2;
+  static constexpr int kATiles = kWide ? 1 : 2;               // 128-row weight tiles per stage
+  static constexpr int kRowsPerCTile = kWide && MODE == 0 ? 64 : kATiles * kTileM;  // output rows
   static constexpr uint32_t kBStageBytes = N * kBK * 2;
-  static constexpr uint32_t kStageBytes = 2 * kATileBytes + kBStageBytes;
+  static constexpr uint32_t kStageBytes = kATiles * kATileBytes + kBStageBytes;
+  // wide GEMM 1: gate and up of a channel sit in different TMEM lane quarters;
+  // each pair of epilogue warps trades half of its bf16 values through a
+  // double-buffered 1 KB slot (4 pairs)
+  static constexpr uint32_t kXchgBytes = kWide && MODE == 0 ? 4 * 2 * 1024 : 0;
   static constexpr int kStages =
-      (kSmemBudget / static_cast<int>(kStageBytes)) < kMaxStages ? kSmemBudget / static_cast<int>(kStageBytes)
-                                                                 : kMaxStages;
+      ((kSmemBudget - static_cast<int>(kXchgBytes)) / static_cast<int>(kStageBytes)) < kMaxStages
+          ? (kSmemBudget - static_cast<int>(kXchgBytes)) / static_cast<int>(kStageBytes)
+          : kMaxStages;
   // accumulator buffers in TMEM: two (epilogue of one tile overlaps the
-  // mainloop of the next) while 2 x 2N fp32 columns fit the 512 columns
-  static constexpr int kAccBufs = (4 * N <= 512) ? 2 : 1;
-  static constexpr uint32_t kAccCols = 2 * N;
+  // mainloop of the next) while both fit the 512 columns
+  static constexpr uint32_t kAccCols = kATiles * N;
+  static constexpr int kAccBufs = (2 * kAccCols <= 512) ? 2 : 1;
   static constexpr uint32_t kTmemCols = (kAccBufs * kAccCols <= 32) ? 32
                                         : (kAccBufs * kAccCols <= 64) ? 64
                                         : (kAccBufs * kAccCols <= 128) ? 128
@@ -237,9 +251,10 @@ struct TcConfig {
   // barriers: full[S], empty[S], acc_full[2], acc_empty[2]; tmem address,
   // abort flag; epilogue destination rows[N], weights[N]
   static constexpr uint32_t kCtlBytes = 8 * (2 * kStages + 4) + 16 + 8 * N;
-  static constexpr uint32_t kSmemBytes = 1024 + kStages * kStageBytes + kCtlBytes;
+  static constexpr uint32_t kSmemBytes = 1024 + kStages * kStageBytes + kXchgBytes + kCtlBytes;
   static_assert(kStages >= 3, "pipeline needs at least three stages");
   static_assert(N * 8 % kGatherThreads == 0, "gather threads split a stage evenly");
+  static_assert(kAccBufs * kAccCols <= 512, "accumulators fit TMEM");
 };
 
 // Tile t of the persistent schedule: block b, weight tile c, and the K-stage
@@ -272,6 +287,15 @@ __device__ __forceinline__ uint16_t silu_mul_bf16(float gate, float up) {
 __device__ __forceinline__ void epilogue_bar_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");  // the epilogue warps only
 }
+// Named barriers 2..5: the two warps of one exchange pair of the epilogue.
+__device__ __forceinline__ void pair_bar_sync(int pair) {
+  switch (pair) {
+    case 0: asm volatile("bar.sync 2, 64;" ::: "memory"); break;
+    case 1: asm volatile("bar.sync 3, 64;" ::: "memory"); break;
+    case 2: asm volatile("bar.sync 4, 64;" ::: "memory"); break;
+    default: asm volatile("bar.sync 5, 64;" ::: "memory"); break;
+  }
+}
 
 // Persistent tiles (tile_coord): block, weight tile, K split; the weight tiles
 // (and splits) of one block are neighbours, so concurrently running CTAs share
@@ -294,7 +318,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
           int E, int K, int R_out, int a_rows, int B, int cap, int n_ctiles, int ksplit,
           float *__restrict__ h_acc, int *__restrict__ tile_cnt, uint16_t *__restrict__ out16,
           float *__restrict__ y_acc, int H_out, int *status) {
-  using Cfg = TcConfig<N>;
+  using Cfg = TcConfig<N, MODE>;
   constexpr int S = Cfg::kStages;
   int n_blocks;
   if (MODE == 2) {
@@ -308,9 +332,10 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint8_t *a_tiles = smem;                                   // [S][2][16 KB]
-  uint8_t *b_tiles = smem + S * 2 * kATileBytes;             // [S][N * 128 B]
-  uint64_t *bars = reinterpret_cast<uint64_t *>(b_tiles + S * Cfg::kBStageBytes);
+  uint8_t *a_tiles = smem;                                   // [S][kATiles][16 KB]
+  uint8_t *b_tiles = smem + S * Cfg::kATiles * kATileBytes;  // [S][N * 128 B]
+  uint8_t *xchg = b_tiles + S * Cfg::kBStageBytes;           // wide GEMM 1: [4 pairs][2][1 KB]
+  uint64_t *bars = reinterpret_cast<uint64_t *>(xchg + Cfg::kXchgBytes);
   uint64_t *full = bars;
   uint64_t *empty = bars + S;
   uint64_t *acc_full = bars + 2 * S;
@@ -363,9 +388,22 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
         const int e = e_next;
         const int tn = t + static_cast<int>(gridDim.x);
         if (MODE != 2 && tn < n_tiles) e_next = expert_ids[tile_coord(tn, n_ctiles, ksplit, nk).b];
-        const int row0 = MODE == 0 ? c * kTileM : c * 2 * kTileM;
-        const int row1 = MODE == 0 ? R_out + c * kTileM : c * 2 * kTileM + kTileM;
-        const bool two = MODE == 0 || row1 < a_rows;
+        // weight rows of the stage's tile(s); wide GEMM 1 loads 64 gate rows
+        // and the matching 64 up rows as the two halves of one 128-row tile
+        // (the map's box is then 64 rows high)
+        int row0, row1;
+        bool two;
+        if (Cfg::kWide) {
+          row0 = c * Cfg::kRowsPerCTile;
+          row1 = R_out + c * Cfg::kRowsPerCTile;
+          two = MODE == 0;
+        } else {
+          row0 = MODE == 0 ? c * kTileM : c * 2 * kTileM;
+          row1 = MODE == 0 ? R_out + c * kTileM : c * 2 * kTileM + kTileM;
+          two = MODE == 0 || row1 < a_rows;
+        }
+        const uint32_t second = Cfg::kWide ? kATileBytes / 2 : kATileBytes;
+        const uint32_t tx = Cfg::kWide ? kATileBytes : (two ? 2 : 1) * kATileBytes;
         for (int kb = tc.kb0; kb < tc.kb1; ++kb, ++g) {
           const int s = g % S;
           if (!wait_bounded(smem_u32(&empty[s]), ((g / S) & 1) ^ 1, abort, status)) {
@@ -373,10 +411,10 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
             break;
           }
           const uint32_t fb = smem_u32(&full[s]);
-          const uint32_t a_s = smem_u32(a_tiles + s * 2 * kATileBytes);
-          mbar_arrive_expect_tx(fb, (two ? 2 : 1) * kATileBytes);
+          const uint32_t a_s = smem_u32(a_tiles + s * Cfg::kATiles * kATileBytes);
+          mbar_arrive_expect_tx(fb, tx);
           tma_load_3d(a_s, &tmap_w, kb * kBK, row0, e, fb);
-          if (two) tma_load_3d(a_s + kATileBytes, &tmap_w, kb * kBK, row1, e, fb);
+          if (two) tma_load_3d(a_s + second, &tmap_w, kb * kBK, row1, e, fb);
         }
       }
       // after an abort: let the copies already issued land before exit
@@ -457,7 +495,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
       bool stop = false;
       for (int t = blockIdx.x; t < n_tiles && !stop; t += gridDim.x) {
         const TileCoord tc = tile_coord(t, n_ctiles, ksplit, nk);
-        const bool two = MODE == 0 || tc.c * 2 * kTileM + kTileM < a_rows;
+        const bool two = !Cfg::kWide && (MODE == 0 || tc.c * 2 * kTileM + kTileM < a_rows);
         const int acc = i % Cfg::kAccBufs;
         const uint32_t use = i / Cfg::kAccBufs;
         ++i;
@@ -472,7 +510,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
           }
           fence_proxy_async_smem();  // the gathered rows were written by cp.async
           tc_fence_after();
-          const uint32_t a0 = smem_u32(a_tiles + s * 2 * kATileBytes);
+          const uint32_t a0 = smem_u32(a_tiles + s * Cfg::kATiles * kATileBytes);
           const uint32_t a1 = a0 + kATileBytes;
           const uint32_t bt = smem_u32(b_tiles + s * Cfg::kBStageBytes);
 #pragma unroll
@@ -501,7 +539,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
       // a block whose expert id lies outside [0, E) is computed (on zero
       // weights) but writes nothing
       const bool e_ok = MODE == 2 || (static_cast<unsigned>(expert_ids[b]) < static_cast<unsigned>(E));
-      const bool two = MODE == 0 || c * 2 * kTileM + kTileM < a_rows;
+      const bool two = !Cfg::kWide && (MODE == 0 || c * 2 * kTileM + kTileM < a_rows);
       const int acc = i % Cfg::kAccBufs;
       const uint32_t use = i / Cfg::kAccBufs;
       ++i;
@@ -530,7 +568,42 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
       epilogue_bar_sync();
       if (*epi_stop) break;
       const uint32_t d0 = tmem + lane_base + acc * Cfg::kAccCols;
-      if (MODE == 0) {
+      if (MODE == 0 && Cfg::kWide) {
+        // TMEM lanes 0-63 hold the gate sums of channels c*64 .. c*64+63,
+        // lanes 64-127 the up sums of the same channels.  Warp pair (gate
+        // quarter q, up quarter q + 2) of one column half: per chunk of 16
+        // columns each warp rounds its values to bf16, hands 8 columns to the
+        // other warp through the pair's slot, and forms a for the other 8.
+        const bool is_gate = q < 2;
+        const int pair = (q & 1) + 2 * half;
+        const int chn = c * Cfg::kRowsPerCTile + (q & 1) * 32 + lane;
+        const bool valid = chn < R_out;
+        uint16_t *slot = reinterpret_cast<uint16_t *>(xchg) + pair * 1024;  // [2][2][8][32] bf16
+#pragma unroll 1
+        for (int j0 = 16 * half, it = 0; j0 < N; j0 += 32, ++it) {
+          uint32_t v[16];
+          tmem_ld_32x32b_x16(d0 + j0, v);
+          tmem_ld_wait();
+          uint16_t *buf = slot + (it & 1) * 512;  // [0]: gate -> up warp, [1]: up -> gate warp
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) {
+            // the gate warp gives away columns 8..15, the up warp columns 0..7
+            const float give = __uint_as_float(is_gate ? v[8 + jj] : v[jj]);
+            buf[(is_gate ? 0 : 256) + jj * 32 + lane] = float_to_bf16_bits(give);
+          }
+          pair_bar_sync(pair);
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) {
+            const int col = is_gate ? jj : 8 + jj;
+            const float other = bf16_bits_to_float(buf[(is_gate ? 256 : 0) + jj * 32 + lane]);
+            const float mine = __uint_as_float(is_gate ? v[jj] : v[8 + jj]);
+            const int p = dst_row[j0 + col];
+            if (valid && p >= 0)
+              out16[(size_t)p * R_out + chn] =
+                  is_gate ? silu_mul_bf16(mine, other) : silu_mul_bf16(other, mine);
+          }
+        }
+      } else if (MODE == 0) {
         const int chn = c * kTileM + q * 32 + lane;
         const bool valid = chn < R_out;
 #pragma unroll 1
@@ -560,7 +633,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
 #pragma unroll 1
         for (int item = half; item < (two ? 2 : 1) * n_chunks; item += 2) {
           const int h = item / n_chunks, j0 = (item - h * n_chunks) * 16;
-          const int n = c * 2 * kTileM + h * kTileM + q * 32 + lane;
+          const int n = c * Cfg::kRowsPerCTile + h * kTileM + q * 32 + lane;
           const bool valid = n < (MODE == 1 ? H_out : a_rows);
           const float bias = (MODE == 2 && valid && vec != nullptr) ? vec[n] : 0.f;
           {
@@ -629,16 +702,17 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
   return fn;
 }
 
-// 3-D map over weights [E][rows][K] (bf16, K contiguous), box 64 x 128 x 1,
+// 3-D map over weights [E][rows][K] (bf16, K contiguous), box 64 x box_rows x 1,
 // 128-byte swizzle; out-of-range rows and columns read as zero.
-cudaError_t encode_weight_map(CUtensorMap *map, const uint16_t *w, int K, int rows, int E) {
+cudaError_t encode_weight_map(CUtensorMap *map, const uint16_t *w, int K, int rows, int E,
+                              int box_rows) {
   PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode_fn();
   if (encode == nullptr) return cudaErrorNotSupported;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows),
                               static_cast<cuuint64_t>(E)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2,
                                  static_cast<cuuint64_t>(K) * 2 * rows};
-  const cuuint32_t box[3] = {kBK, kTileM, 1};
+  const cuuint32_t box[3] = {kBK, static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t *>(w),
                             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -652,29 +726,31 @@ cudaError_t encode_weight_map(CUtensorMap *map, const uint16_t *w, int K, int ro
 struct MapEntry {
   int dev;
   const void *ptr;
-  int K, rows, E;
+  int K, rows, E, box_rows;
   CUtensorMap map;
 };
 std::mutex g_map_mutex;
 MapEntry g_maps[128];
 int g_map_next = 0, g_map_count = 0;
 
-cudaError_t make_weight_map(CUtensorMap *map, const uint16_t *w, int K, int rows, int E) {
+cudaError_t make_weight_map(CUtensorMap *map, const uint16_t *w, int K, int rows, int E,
+                            int box_rows = kTileM) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   std::lock_guard<std::mutex> lock(g_map_mutex);
   for (int i = 0; i < g_map_count; ++i) {
     const MapEntry &m = g_maps[i];
-    if (m.dev == dev && m.ptr == w && m.K == K && m.rows == rows && m.E == E) {
+    if (m.dev == dev && m.ptr == w && m.K == K && m.rows == rows && m.E == E &&
+        m.box_rows == box_rows) {
       *map = m.map;
       return cudaSuccess;
     }
   }
-  err = encode_weight_map(map, w, K, rows, E);
+  err = encode_weight_map(map, w, K, rows, E, box_rows);
   if (err != cudaSuccess) return err;
   MapEntry &m = g_maps[g_map_next];
-  m = MapEntry{dev, w, K, rows, E, *map};
+  m = MapEntry{dev, w, K, rows, E, box_rows, *map};
   g_map_next = (g_map_next + 1) % 128;
   if (g_map_count < 128) ++g_map_count;
   return cudaSuccess;
@@ -698,7 +774,7 @@ struct TcArgs {
 
 template <int N, int MODE>
 cudaError_t launch_tc_n(const CUtensorMap &map_w, const TcArgs &a, cudaStream_t s) {
-  using Cfg = TcConfig<N>;
+  using Cfg = TcConfig<N, MODE>;
   auto kern = k_gemm_tc<N, MODE>;
   cudaError_t err = ensure_smem_limit(reinterpret_cast<const void *>(kern), Cfg::kSmemBytes);
   if (err != cudaSuccess) return err;
@@ -733,11 +809,13 @@ cudaError_t launch_tc_w13_act(const uint16_t *x, const uint16_t *w13, const int3
                               const int32_t *expert_ids, const int32_t *n_post, int P, int top_k,
                               int E, int H, int I, int B, int cap, uint16_t *a, int ksplit,
                               float *h_acc, int *tile_cnt, int *status, cudaStream_t s) {
+  // wide tiles (B = 256): 64 gate rows over 64 up rows per weight tile, no K split
+  const bool wide = B == 256;
   CUtensorMap map_w;
-  cudaError_t err = make_weight_map(&map_w, w13, H, 2 * I, E);
+  cudaError_t err = make_weight_map(&map_w, w13, H, 2 * I, E, wide ? kTileM / 2 : kTileM);
   if (err != cudaSuccess) return err;
   const int nk = (H + kBK - 1) / kBK;
-  if (ksplit < 1 || ksplit > nk || h_acc == nullptr || tile_cnt == nullptr) ksplit = 1;
+  if (wide || ksplit < 1 || ksplit > nk || h_acc == nullptr || tile_cnt == nullptr) ksplit = 1;
   TcArgs args{};
   args.src = x;
   args.src_rows = (P + top_k - 1) / top_k;
@@ -752,7 +830,8 @@ cudaError_t launch_tc_w13_act(const uint16_t *x, const uint16_t *w13, const int3
   args.a_rows = 2 * I;
   args.B = B;
   args.cap = cap;
-  args.n_ctiles = (I + kTileM - 1) / kTileM;
+  const int ct_rows = wide ? kTileM / 2 : kTileM;
+  args.n_ctiles = (I + ct_rows - 1) / ct_rows;
   args.ksplit = ksplit;
   args.h_acc = h_acc;
   args.tile_cnt = tile_cnt;
@@ -786,7 +865,8 @@ cudaError_t launch_tc_w2_combine(const uint16_t *a, const uint16_t *w2, const in
   args.a_rows = H;
   args.B = B;
   args.cap = cap;
-  args.n_ctiles = (H + 2 * kTileM - 1) / (2 * kTileM);
+  const int ct_rows = B == 256 ? kTileM : 2 * kTileM;  // wide tiles: one 128-row weight tile
+  args.n_ctiles = (H + ct_rows - 1) / ct_rows;
   args.ksplit = std::max(1, std::min(ksplit, nk));  // the combine adds partial sums anyway
   args.y_acc = y_acc;
   args.H_out = H;

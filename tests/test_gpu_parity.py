@@ -211,7 +211,10 @@ def align_on_device(ids_np, E, B):
 GEMM_SHAPES = [(3, 4, 2, 128, 64, 16), (64, 128, 8, 2048, 768, 16), (64, 60, 4, 2048, 1408, 16),
                (33, 16, 3, 256, 160, 4), (200, 32, 4, 512, 96, 32), (128, 256, 8, 2048, 512, 16),
                (512, 128, 8, 2048, 768, 32), (1, 128, 8, 2048, 768, 16), (300, 8, 2, 192, 48, 64),
-               (1000, 16, 4, 320, 208, 128), (700, 4, 2, 256, 128, 256), (40, 3, 3, 80, 16, 16)]
+               (1000, 16, 4, 320, 208, 128), (700, 4, 2, 256, 128, 256), (40, 3, 3, 80, 16, 16),
+               # 256-token tiles: ragged K stage (H = 208), ragged 64-channel and
+               # 128-row weight tiles (I = 80, H = 208), mostly-padding blocks, real sizes
+               (1000, 16, 4, 208, 80, 256), (300, 60, 4, 512, 192, 256), (2000, 8, 2, 2048, 768, 256)]
 
 
 @pytest.mark.parametrize("M,E,k,H,I,B", GEMM_SHAPES)

@@ -232,8 +232,8 @@ struct TcConfig {
   static constexpr uint32_t kStageBytes = kATiles * kATileBytes + kBStageBytes;
   // wide GEMM 1: gate and up of a channel sit in different TMEM lane quarters;
   // each pair of epilogue warps trades half of its bf16 values through a
-  // double-buffered 1 KB slot (4 pairs)
-  static constexpr uint32_t kXchgBytes = kWide && MODE == 0 ? 4 * 2 * 1024 : 0;
+  // double-buffered slot of 2 x 1 KB (4 pairs)
+  static constexpr uint32_t kXchgBytes = kWide && MODE == 0 ? 4 * 2 * 2 * 32 * 32 : 0;
   static constexpr int kStages =
       ((kSmemBudget - static_cast<int>(kXchgBytes)) / static_cast<int>(kStageBytes)) < kMaxStages
           ? (kSmemBudget - static_cast<int>(kXchgBytes)) / static_cast<int>(kStageBytes)
@@ -277,11 +277,19 @@ __device__ __forceinline__ TileCoord tile_coord(int t, int n_ctiles, int ksplit,
 }
 
 // a = bf16( SiLU(bf16(gate)) * bf16(up) ) from fp32 GEMM-1 sums.
+// The fast exponential and division (a few fp32 ulps) are far below the final
+// bf16 rounding; 1 + exp(-g) = inf for very negative g gives SiLU = -0.
 __device__ __forceinline__ uint16_t silu_mul_bf16(float gate, float up) {
   const float gb = bf16_bits_to_float(float_to_bf16_bits(gate));
   const float ub = bf16_bits_to_float(float_to_bf16_bits(up));
-  const float silu = gb * __frcp_rn(1.0f + expf(-gb));
+  const float silu = __fdividef(gb, 1.0f + __expf(-gb));
   return float_to_bf16_bits(silu * ub);
+}
+
+// Two fp32 values -> bf16x2 bits (round to nearest even), lo in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  return static_cast<uint32_t>(float_to_bf16_bits(lo)) |
+         (static_cast<uint32_t>(float_to_bf16_bits(hi)) << 16);
 }
 
 __device__ __forceinline__ void epilogue_bar_sync() {
@@ -334,7 +342,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
   uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t *a_tiles = smem;                                   // [S][kATiles][16 KB]
   uint8_t *b_tiles = smem + S * Cfg::kATiles * kATileBytes;  // [S][N * 128 B]
-  uint8_t *xchg = b_tiles + S * Cfg::kBStageBytes;           // wide GEMM 1: [4 pairs][2][1 KB]
+  uint8_t *xchg = b_tiles + S * Cfg::kBStageBytes;           // wide GEMM 1: [4 pairs][2][2 KB]
   uint64_t *bars = reinterpret_cast<uint64_t *>(xchg + Cfg::kXchgBytes);
   uint64_t *full = bars;
   uint64_t *empty = bars + S;
@@ -571,36 +579,48 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
       if (MODE == 0 && Cfg::kWide) {
         // TMEM lanes 0-63 hold the gate sums of channels c*64 .. c*64+63,
         // lanes 64-127 the up sums of the same channels.  Warp pair (gate
-        // quarter q, up quarter q + 2) of one column half: per chunk of 16
-        // columns each warp rounds its values to bf16, hands 8 columns to the
-        // other warp through the pair's slot, and forms a for the other 8.
+        // quarter q, up quarter q + 2) of one column half: per 32 columns each
+        // warp rounds its values to bf16, hands 16 columns to the other warp
+        // through the pair's slot, and forms a for the other 16.
         const bool is_gate = q < 2;
         const int pair = (q & 1) + 2 * half;
         const int chn = c * Cfg::kRowsPerCTile + (q & 1) * 32 + lane;
         const bool valid = chn < R_out;
-        uint16_t *slot = reinterpret_cast<uint16_t *>(xchg) + pair * 1024;  // [2][2][8][32] bf16
+        // [pair][buffer][direction][column half][lane] of 16 bytes (8 bf16 columns)
+        uint4 *slot = reinterpret_cast<uint4 *>(xchg) + pair * (2 * 2 * 32 * 2);
 #pragma unroll 1
-        for (int j0 = 16 * half, it = 0; j0 < N; j0 += 32, ++it) {
-          uint32_t v[16];
-          tmem_ld_32x32b_x16(d0 + j0, v);
+        for (int j0 = 32 * half, it = 0; j0 < N; j0 += 64, ++it) {
+          uint32_t lo[16], hi[16];
+          tmem_ld_32x32b_x16(d0 + j0, lo);
+          tmem_ld_32x32b_x16(d0 + j0 + 16, hi);
           tmem_ld_wait();
-          uint16_t *buf = slot + (it & 1) * 512;  // [0]: gate -> up warp, [1]: up -> gate warp
-#pragma unroll
-          for (int jj = 0; jj < 8; ++jj) {
-            // the gate warp gives away columns 8..15, the up warp columns 0..7
-            const float give = __uint_as_float(is_gate ? v[8 + jj] : v[jj]);
-            buf[(is_gate ? 0 : 256) + jj * 32 + lane] = float_to_bf16_bits(give);
+          uint4 *buf = slot + (it & 1) * (2 * 32 * 2);
+          // the gate warp gives away columns 16..31, the up warp columns 0..15
+          {
+            const uint32_t *g = is_gate ? hi : lo;
+            uint4 *dst = buf + (is_gate ? 0 : 64) + lane;
+            dst[0] = make_uint4(pack_bf16x2(__uint_as_float(g[0]), __uint_as_float(g[1])),
+                                pack_bf16x2(__uint_as_float(g[2]), __uint_as_float(g[3])),
+                                pack_bf16x2(__uint_as_float(g[4]), __uint_as_float(g[5])),
+                                pack_bf16x2(__uint_as_float(g[6]), __uint_as_float(g[7])));
+            dst[32] = make_uint4(pack_bf16x2(__uint_as_float(g[8]), __uint_as_float(g[9])),
+                                pack_bf16x2(__uint_as_float(g[10]), __uint_as_float(g[11])),
+                                pack_bf16x2(__uint_as_float(g[12]), __uint_as_float(g[13])),
+                                pack_bf16x2(__uint_as_float(g[14]), __uint_as_float(g[15])));
           }
           pair_bar_sync(pair);
+          const uint4 *src2 = buf + (is_gate ? 64 : 0) + lane;
+          const uint4 r0 = src2[0], r1 = src2[32];
+          const uint32_t other[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+          const uint32_t *mine = is_gate ? lo : hi;
+          const int cbase = j0 + (is_gate ? 0 : 16);
 #pragma unroll
-          for (int jj = 0; jj < 8; ++jj) {
-            const int col = is_gate ? jj : 8 + jj;
-            const float other = bf16_bits_to_float(buf[(is_gate ? 256 : 0) + jj * 32 + lane]);
-            const float mine = __uint_as_float(is_gate ? v[jj] : v[8 + jj]);
-            const int p = dst_row[j0 + col];
+          for (int jj = 0; jj < 16; ++jj) {
+            const float o = __uint_as_float((jj & 1) ? (other[jj >> 1] & 0xFFFF0000u) : (other[jj >> 1] << 16));
+            const float m = __uint_as_float(mine[jj]);
+            const int p = dst_row[cbase + jj];
             if (valid && p >= 0)
-              out16[(size_t)p * R_out + chn] =
-                  is_gate ? silu_mul_bf16(mine, other) : silu_mul_bf16(other, mine);
+              out16[(size_t)p * R_out + chn] = is_gate ? silu_mul_bf16(m, o) : silu_mul_bf16(o, m);
           }
         }
       } else if (MODE == 0) {

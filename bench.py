@@ -23,8 +23,10 @@ from __future__ import annotations
 
 import argparse
 import dataclasses
+import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -82,6 +84,33 @@ def load_peaks():
                 "source": "measured"}
     except (OSError, KeyError, ValueError):
         return dict(FALLBACK_PEAKS, source="fallback")
+
+
+# ----------------------------------------------------------------------------- profiled traffic
+
+PROFILES = os.path.join(ROOT, "profiles")
+CSRC = os.path.join(ROOT, "mixture_experts_layer_renorm_gb300", "csrc")
+
+
+def profiled_traffic(summary_name, block_size):
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
+    dominant kernel, from the committed ncu summary `profiles/<summary_name>`,
+    or None when there is none for this block size or when a kernel source it
+    lists has changed since the counters were taken (sha256 per file)."""
+    path = os.path.join(PROFILES, summary_name)
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"^\s*traffic_bytes_per_launch\s*=\s*(\d+)\s*$", text, re.M)
+    b = re.search(r"^\s*block_size_m\s*=\s*(\d+)\s*$", text, re.M)
+    srcs = re.findall(r"^\s*source\s+(\S+)\s+sha256\s*=\s*([0-9a-f]{64})\s*$", text, re.M)
+    if m is None or b is None or not srcs or int(b.group(1)) != block_size:
+        return None
+    for name, digest in srcs:
+        f = os.path.join(CSRC, name)
+        if not os.path.exists(f) or hashlib.sha256(open(f, "rb").read()).hexdigest() != digest:
+            return None
+    return int(m.group(1))
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -525,7 +554,8 @@ def ours(args):
                    "l2": f"flushed between steps ({args.flush_mb} MB write, outside the events)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": dict({"kernel": "grouped GEMM 1 + SiLU-and-mul"}, **roof,
-                         traffic=None, peak_source=peaks["source"], ms=round(gemm1_ms, 5)),
+                         traffic=profiled_traffic(f"k_gemm_tc_gemm1_{w.name}_m{M}.md", L.B),
+                         peak_source=peaks["source"], ms=round(gemm1_ms, 5)),
         "layer_roofline": {"achieved_gbs": round(lay_gbs, 1),
                            "hbm_frac": round(lay_gbs / peaks["hbm_gbs"], 4),
                            "achieved_tflops": round(lay_tflops, 3),

@@ -141,14 +141,24 @@ __device__ void align_one_cta(int *smem, const int32_t *__restrict__ topk_ids, i
                               int *status) {
   const AlignSmem s = carve(smem, E);
   const int tid = threadIdx.x;
+  // up to one pair per thread: its expert id is loaded once and kept for the scatter
+  const bool one_pass = P <= kAlignThreads;
+  const int my_e = (one_pass && tid < P) ? load_id<kFromOtherCtas>(topk_ids + tid) : -1;
   for (int e = tid; e < E; e += blockDim.x) s.cnt[e] = 0;
   for (int i = tid; i < kAlignWarps * E; i += blockDim.x) s.wc[i] = 0;
   __syncthreads();
   bool bad = false;
-  for (int p = tid; p < P; p += blockDim.x) {
-    const int e = load_id<kFromOtherCtas>(topk_ids + p);
-    if (e >= 0 && e < E) atomicAdd(&s.cnt[e], 1);
-    else bad = true;
+  if (one_pass) {
+    if (tid < P) {
+      if (my_e >= 0 && my_e < E) atomicAdd(&s.cnt[my_e], 1);
+      else bad = true;
+    }
+  } else {
+    for (int p = tid; p < P; p += blockDim.x) {
+      const int e = load_id<kFromOtherCtas>(topk_ids + p);
+      if (e >= 0 && e < E) atomicAdd(&s.cnt[e], 1);
+      else bad = true;
+    }
   }
   if (bad) report_status(status, kStatusBadExpertId);
   __syncthreads();
@@ -158,7 +168,22 @@ __device__ void align_one_cta(int *smem, const int32_t *__restrict__ topk_ids, i
   for (int e = tid; e < E; e += blockDim.x) s.run[e] = s.off[e];
   write_layout(s, E, B, P, total, sorted_ids, expert_ids, expert_offsets, n_post);
   __syncthreads();
-  scatter_chunk<kFromOtherCtas>(s, topk_ids, 0, P, E, sorted_ids);
+  if (one_pass) {
+    // the single tile of scatter_chunk, with the id already in hand
+    const int warp = tid >> 5;
+    const int e = (tid < P && my_e >= 0 && my_e < E) ? my_e : -1;
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & lanemask_lt());
+    if (e >= 0 && rank == 0) s.wc[warp * E + e] = __popc(peers);
+    __syncthreads();
+    if (e >= 0) {
+      int prefix = 0;
+      for (int w = 0; w < warp; ++w) prefix += s.wc[w * E + e];
+      sorted_ids[s.run[e] + prefix + rank] = tid;
+    }
+  } else {
+    scatter_chunk<kFromOtherCtas>(s, topk_ids, 0, P, E, sorted_ids);
+  }
 }
 
 inline size_t align_smem_bytes(int E) {

@@ -30,6 +30,8 @@ __global__ void __launch_bounds__(kAlignThreads)
 k_align_single(const int32_t *__restrict__ topk_ids, int P, int E, int B,
                int32_t *__restrict__ sorted_ids, int32_t *__restrict__ expert_ids,
                int32_t *__restrict__ expert_offsets, int32_t *__restrict__ n_post, int *status) {
+  griddep_wait();
+  griddep_launch_dependents();
   extern __shared__ int smem[];
   align_one_cta<false>(smem, topk_ids, P, E, B, sorted_ids, expert_ids, expert_offsets, n_post,
                        status);
@@ -39,6 +41,8 @@ k_align_single(const int32_t *__restrict__ topk_ids, int P, int E, int B,
 __global__ void __launch_bounds__(kAlignThreads)
 k_align_count(const int32_t *__restrict__ topk_ids, int P, int E, int32_t *__restrict__ hist,
               int *status) {
+  griddep_wait();
+  griddep_launch_dependents();
   extern __shared__ int smem[];
   int *cnt = smem;
   const int tid = threadIdx.x;
@@ -65,6 +69,8 @@ k_align_scatter(const int32_t *__restrict__ topk_ids, int P, int E, int B,
                 const int32_t *__restrict__ hist, int32_t *__restrict__ sorted_ids,
                 int32_t *__restrict__ expert_ids, int32_t *__restrict__ expert_offsets,
                 int32_t *__restrict__ n_post) {
+  griddep_wait();
+  griddep_launch_dependents();
   extern __shared__ int smem[];
   const AlignSmem s = carve(smem, E);
   const int tid = threadIdx.x;
@@ -113,16 +119,15 @@ cudaError_t launch_align(const int32_t *topk_ids, int P, int E, int B, int cap,
   if (attr != cudaSuccess) return attr;
   const int C = align_num_ctas(P);
   if (C == 1) {
-    k_align_single<<<1, kAlignThreads, smem, s>>>(topk_ids, P, E, B, sorted_ids, expert_ids,
-                                                  expert_offsets, n_post, status);
-    return cudaGetLastError();
+    return launch_pdl(k_align_single, dim3(1), dim3(kAlignThreads), smem, s, topk_ids, P, E, B,
+                      sorted_ids, expert_ids, expert_offsets, n_post, status);
   }
-  k_align_count<<<C, kAlignThreads, sizeof(int) * E, s>>>(topk_ids, P, E, hist, status);
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err = launch_pdl(k_align_count, dim3(C), dim3(kAlignThreads), sizeof(int) * E, s,
+                               topk_ids, P, E, hist, status);
   if (err != cudaSuccess) return err;
-  k_align_scatter<<<C, kAlignThreads, smem, s>>>(topk_ids, P, E, B, hist, sorted_ids, expert_ids,
-                                                 expert_offsets, n_post);
-  return cudaGetLastError();
+  return launch_pdl(k_align_scatter, dim3(C), dim3(kAlignThreads), smem, s, topk_ids, P, E, B,
+                    static_cast<const int32_t *>(hist), sorted_ids, expert_ids, expert_offsets,
+                    n_post);
 }
 
 }  // namespace moe

@@ -325,9 +325,16 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
           const int32_t *__restrict__ n_post_ptr, const float *__restrict__ vec, int P, int top_k,
           int E, int K, int R_out, int a_rows, int B, int cap, int n_ctiles, int ksplit,
           float *__restrict__ h_acc, int *__restrict__ tile_cnt, uint16_t *__restrict__ out16,
-          float *__restrict__ y_acc, int H_out, int *status) {
+          float *__restrict__ y_acc, int H_out, int *status, int early_weights) {
   using Cfg = TcConfig<N, MODE>;
   constexpr int S = Cfg::kStages;
+  // With early_weights (GEMM 2 right after GEMM 1 in one layer) only the row
+  // gathers wait for the previous kernel: the weight tiles and the routing
+  // lists it reads were final before GEMM 1 started, so the weights stream
+  // while GEMM 1 drains.
+  const bool early = MODE == 1 && early_weights != 0;
+  if (!early) griddep_wait();
+  griddep_launch_dependents();
   int n_blocks;
   if (MODE == 2) {
     n_blocks = (src_rows + N - 1) / N;
@@ -336,7 +343,12 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
     n_blocks = n_post / B;
   }
   const int n_tiles = n_blocks * n_ctiles * ksplit;
-  if (static_cast<int>(blockIdx.x) >= n_tiles) return;
+  if (static_cast<int>(blockIdx.x) >= n_tiles) {
+    // this kernel must not finish before the one it follows has: the next
+    // kernels count on that when they reuse what it read
+    if (early) griddep_wait();
+    return;
+  }
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -444,6 +456,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
     // straight on to the next stage.
     const int gt = threadIdx.x - kGatherWarp0 * 32;
     const int ch = gt & 7;
+    if (early) griddep_wait();  // the gathered rows are the previous kernel's output
     // Entries of sorted_token_ids (MODE 2: token ids) of this thread's rows in
     // tile t; the next tile's are loaded while this tile's rows are copied.
     auto fetch_ids = [&](int t, int (&ids)[Cfg::kChunksPerThread]) {
@@ -790,6 +803,7 @@ struct TcArgs {
   int H_out;
   int *status;
   long max_blocks;  // host-side bound on the blocks (tiles = blocks * n_ctiles * ksplit)
+  int early_weights;
 };
 
 template <int N, int MODE>
@@ -802,11 +816,10 @@ cudaError_t launch_tc_n(const CUtensorMap &map_w, const TcArgs &a, cudaStream_t 
   const int grid = static_cast<int>(
       std::min<long>(a.max_blocks * a.n_ctiles * a.ksplit, num_sms()));
   if (grid <= 0) return cudaSuccess;
-  kern<<<grid, kTcThreads, Cfg::kSmemBytes, s>>>(
-      map_w, a.src, a.src_rows, a.sorted_ids, a.expert_ids, a.n_post, a.vec, a.P, a.top_k, a.E,
-      a.K, a.R_out, a.a_rows, a.B, a.cap, a.n_ctiles, a.ksplit, a.h_acc, a.tile_cnt, a.out16,
-      a.y_acc, a.H_out, a.status);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(kTcThreads), Cfg::kSmemBytes, s, map_w, a.src,
+                    a.src_rows, a.sorted_ids, a.expert_ids, a.n_post, a.vec, a.P, a.top_k, a.E,
+                    a.K, a.R_out, a.a_rows, a.B, a.cap, a.n_ctiles, a.ksplit, a.h_acc, a.tile_cnt,
+                    a.out16, a.y_acc, a.H_out, a.status, a.early_weights);
 }
 
 template <int MODE>
@@ -865,7 +878,7 @@ cudaError_t launch_tc_w2_combine(const uint16_t *a, const uint16_t *w2, const in
                                  const int32_t *expert_ids, const int32_t *n_post,
                                  const float *topk_weights, int P, int top_k, int E, int H, int I,
                                  int B, int cap, float *y_acc, int ksplit, int *status,
-                                 cudaStream_t s) {
+                                 bool early_weights, cudaStream_t s) {
   CUtensorMap map_w;
   cudaError_t err = make_weight_map(&map_w, w2, I, H, E);
   if (err != cudaSuccess) return err;
@@ -892,6 +905,7 @@ cudaError_t launch_tc_w2_combine(const uint16_t *a, const uint16_t *w2, const in
   args.H_out = H;
   args.status = status;
   args.max_blocks = cap / B;
+  args.early_weights = early_weights ? 1 : 0;
   return launch_tc<1>(B, map_w, args, s);
 }
 

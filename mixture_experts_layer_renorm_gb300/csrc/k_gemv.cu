@@ -181,6 +181,8 @@ k_gemv_w13_act(const uint16_t *__restrict__ x, const uint16_t *__restrict__ w13,
                const int32_t *__restrict__ sorted_ids, const int32_t *__restrict__ expert_ids,
                const int32_t *__restrict__ n_post_ptr, int P, int top_k, int E, int H, int I, int B,
                int cap, int pass_rows, uint16_t *__restrict__ a) {
+  griddep_wait();
+  griddep_launch_dependents();
   extern __shared__ uint4 xs[];
   __shared__ int pairs[kGemvMaxTok];
   const int n_post = min(max(*n_post_ptr, 0), cap);
@@ -236,6 +238,8 @@ k_gemv_w2_combine(const uint16_t *__restrict__ a, const uint16_t *__restrict__ w
                   const int32_t *__restrict__ n_post_ptr, const float *__restrict__ topk_w, int P,
                   int top_k, int E, int H, int I, int B, int cap, int pass_rows,
                   float *__restrict__ y_acc) {
+  griddep_wait();
+  griddep_launch_dependents();
   extern __shared__ uint4 xs[];
   __shared__ int pairs[kGemvMaxTok];
   const int n_post = min(max(*n_post_ptr, 0), cap);
@@ -268,6 +272,8 @@ k_gemv_w2_combine(const uint16_t *__restrict__ a, const uint16_t *__restrict__ w
 // y = bf16(y_acc + residual), 4 elements per thread.
 __global__ void k_finalize(const float4 *__restrict__ y_acc, const uint2 *__restrict__ residual,
                            long n4, uint2 *__restrict__ y) {
+  griddep_wait();
+  griddep_launch_dependents();
   for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n4; i += (long)gridDim.x * blockDim.x) {
     float4 v = y_acc[i];
     if (residual != nullptr) {
@@ -344,9 +350,8 @@ cudaError_t launch_gemv_w13_act(const uint16_t *x, const uint16_t *w13, const in
   const long units_max = (long)(cap / B) * ((I + kGemvWarps - 1) / kGemvWarps);
   const int grid = static_cast<int>(std::min<long>(units_max, (long)num_sms() * 8));
   if (grid <= 0) return cudaSuccess;
-  k_gemv_w13_act<<<grid, kGemvThreads, smem, s>>>(x, w13, sorted_ids, expert_ids, n_post, P, top_k,
-                                                  E, H, I, B, cap, pass_rows, a);
-  return cudaGetLastError();
+  return launch_pdl(k_gemv_w13_act, dim3(grid), dim3(kGemvThreads), smem, s, x, w13, sorted_ids,
+                    expert_ids, n_post, P, top_k, E, H, I, B, cap, pass_rows, a);
 }
 
 cudaError_t launch_gemv_w2_combine(const uint16_t *a, const uint16_t *w2, const int32_t *sorted_ids,
@@ -360,10 +365,8 @@ cudaError_t launch_gemv_w2_combine(const uint16_t *a, const uint16_t *w2, const 
   const long units_max = (long)(cap / B) * ((H + kGemvWarps - 1) / kGemvWarps);
   const int grid = static_cast<int>(std::min<long>(units_max, (long)num_sms() * 8));
   if (grid <= 0) return cudaSuccess;
-  k_gemv_w2_combine<<<grid, kGemvThreads, smem, s>>>(a, w2, sorted_ids, expert_ids, n_post,
-                                                     topk_weights, P, top_k, E, H, I, B, cap, pass_rows,
-                                                     y_acc);
-  return cudaGetLastError();
+  return launch_pdl(k_gemv_w2_combine, dim3(grid), dim3(kGemvThreads), smem, s, a, w2, sorted_ids,
+                    expert_ids, n_post, topk_weights, P, top_k, E, H, I, B, cap, pass_rows, y_acc);
 }
 
 cudaError_t launch_finalize(const float *y_acc, const uint16_t *residual, int M, int H, uint16_t *y,
@@ -372,10 +375,9 @@ cudaError_t launch_finalize(const float *y_acc, const uint16_t *residual, int M,
   if (n4 == 0) return cudaSuccess;
   const int threads = 256;
   const int grid = static_cast<int>(std::min<long>((n4 + threads - 1) / threads, (long)num_sms() * 8));
-  k_finalize<<<grid, threads, 0, s>>>(reinterpret_cast<const float4 *>(y_acc),
-                                      reinterpret_cast<const uint2 *>(residual), n4,
-                                      reinterpret_cast<uint2 *>(y));
-  return cudaGetLastError();
+  return launch_pdl(k_finalize, dim3(grid), dim3(threads), 0, s,
+                    reinterpret_cast<const float4 *>(y_acc),
+                    reinterpret_cast<const uint2 *>(residual), n4, reinterpret_cast<uint2 *>(y));
 }
 
 }  // namespace moe

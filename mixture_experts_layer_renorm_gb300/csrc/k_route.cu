@@ -24,6 +24,8 @@ constexpr int kRouterVec = kRouterKChunk / 8 / 32;  // 16-byte router loads per 
 __global__ void __launch_bounds__(kRouterWarps * 32)
 k_router_logits(const uint16_t *__restrict__ x, const uint16_t *__restrict__ w_router,
                 const float *__restrict__ bias, int M, int E, int H, uint16_t *__restrict__ logits) {
+  griddep_wait();
+  griddep_launch_dependents();
   __shared__ uint4 xs[kRouterTok * (kRouterKChunk / 8)];
   const int t0 = blockIdx.x * kRouterTok;
   const int nt = min(kRouterTok, M - t0);
@@ -89,6 +91,8 @@ template <int VPL>
 __global__ void __launch_bounds__(256)
 k_topk_softmax(const uint16_t *__restrict__ logits, int M, int E, int top_k, int renormalize,
                int32_t *__restrict__ topk_ids, float *__restrict__ topk_weights) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (t >= M) return;
   topk_softmax_warp<VPL, false>(logits + (size_t)t * E, E, top_k, renormalize,
@@ -101,25 +105,24 @@ k_topk_softmax(const uint16_t *__restrict__ logits, int M, int E, int top_k, int
 cudaError_t launch_router_logits(const uint16_t *x, const uint16_t *w_router, const float *bias,
                                  int M, int E, int H, uint16_t *logits, cudaStream_t s) {
   dim3 grid((M + kRouterTok - 1) / kRouterTok, (E + kRouterWarps - 1) / kRouterWarps);
-  k_router_logits<<<grid, kRouterWarps * 32, 0, s>>>(x, w_router, bias, M, E, H, logits);
-  return cudaGetLastError();
+  return launch_pdl(k_router_logits, grid, dim3(kRouterWarps * 32), 0, s, x, w_router, bias, M, E,
+                    H, logits);
 }
 
 cudaError_t launch_topk_softmax(const uint16_t *logits, int M, int E, int top_k, int renormalize,
                                 int32_t *topk_ids, float *topk_weights, cudaStream_t s) {
   const int threads = 256;
   const int blocks = (M * 32 + threads - 1) / threads;
-#define MOE_TOPK_CASE(V)                                                                       \
-  k_topk_softmax<V><<<blocks, threads, 0, s>>>(logits, M, E, top_k, renormalize, topk_ids, \
-                                               topk_weights)
+#define MOE_TOPK_CASE(V)                                                                    \
+  return launch_pdl(k_topk_softmax<V>, dim3(blocks), dim3(threads), 0, s, logits, M, E, top_k, \
+                    renormalize, topk_ids, topk_weights)
   if (E <= 32) MOE_TOPK_CASE(1);
-  else if (E <= 64) MOE_TOPK_CASE(2);
-  else if (E <= 128) MOE_TOPK_CASE(4);
-  else if (E <= 256) MOE_TOPK_CASE(8);
-  else if (E <= 512) MOE_TOPK_CASE(16);
-  else MOE_TOPK_CASE(32);
+  if (E <= 64) MOE_TOPK_CASE(2);
+  if (E <= 128) MOE_TOPK_CASE(4);
+  if (E <= 256) MOE_TOPK_CASE(8);
+  if (E <= 512) MOE_TOPK_CASE(16);
+  MOE_TOPK_CASE(32);
 #undef MOE_TOPK_CASE
-  return cudaGetLastError();
 }
 
 }  // namespace moe

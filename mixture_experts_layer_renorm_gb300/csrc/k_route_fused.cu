@@ -7,14 +7,15 @@
 // router with softmax and top-k; the MoE execution analysis page counts the
 // separate launches per decode step.  Here one launch does all three steps:
 //
-//   CTA (g, h) computes the router logits of token group g (8 tokens) against
-//   expert group h (16 experts, one per warp), writes them, and counts itself
-//   done for group g; the last CTA of group g runs the top-k of its tokens
-//   (one warp per token) and counts the group done; the last group's CTA runs
-//   the whole align in one CTA.  "Last" is decided by an atomic counter after
-//   a memory fence -- no CTA ever waits for another, so nothing can hang.
-//   The counters live in the workspace's control block; the CTA that finishes
-//   a counter resets it for the next call.
+//   CTA (g, h) computes the router logits of token group g (TOK tokens, TOK
+//   the smallest of 1, 2, 4, 8 that covers a decode batch) against expert
+//   group h (8 experts, two warps per expert splitting K), writes them, and
+//   counts itself done for group g; the last CTA of group g runs the top-k of
+//   its tokens (one warp per token) and counts the group done; the last
+//   group's CTA runs the whole align in one CTA.  "Last" is decided by an
+//   atomic counter after a memory fence -- no CTA ever waits for another, so
+//   nothing can hang.  The counters live in the workspace's control block;
+//   the CTA that finishes a counter resets it for the next call.
 //
 // As a side task every CTA zeroes its share of the combine accumulator, which
 // GEMM 2 adds into later in the same layer.
@@ -29,10 +30,11 @@ namespace {
 
 constexpr int kFusedThreads = kAlignThreads;  // 16 warps: the align needs 512 threads
 constexpr int kFusedWarps = kFusedThreads / 32;
+constexpr int kFusedExperts = kFusedWarps / 2;   // experts per CTA: two warps (K halves) each
 constexpr int kFusedKChunk = 2048;             // x columns staged per chunk
-constexpr int kFusedVec = kFusedKChunk / 8 / 32;  // 16-byte router loads per lane per chunk
+constexpr int kFusedVec = kFusedKChunk / 8 / 32 / 2;  // 16-byte router loads per lane per chunk half
 
-template <int VPL>
+template <int VPL, int TOK>
 __global__ void __launch_bounds__(kFusedThreads)
 k_route_fused(const uint16_t *__restrict__ x, const uint16_t *__restrict__ w_router,
               const float *__restrict__ bias, const uint16_t *__restrict__ logits_in, int M,
@@ -42,8 +44,12 @@ k_route_fused(const uint16_t *__restrict__ x, const uint16_t *__restrict__ w_rou
               int32_t *__restrict__ expert_offsets, int32_t *__restrict__ n_post,
               int *__restrict__ counters, int *status, float4 *__restrict__ zero_buf,
               long zero_n4) {
+  // the previous layer may still read the accumulator this kernel clears
+  griddep_wait();
+  griddep_launch_dependents();
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ int last;
+  __shared__ float half_sum[kFusedExperts][TOK];
   const int g = blockIdx.x, h = blockIdx.y;
   const int n_g = gridDim.x, n_h = gridDim.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -55,46 +61,60 @@ k_route_fused(const uint16_t *__restrict__ x, const uint16_t *__restrict__ w_rou
       zero_buf[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 
-  const int t0 = g * kRouteFusedTok;
-  const int nt = min(kRouteFusedTok, M - t0);
+  const int t0 = g * TOK;
+  const int nt = min(TOK, M - t0);
   const uint16_t *lg = logits_in;
   if (logits_in == nullptr) {
-    // ---- router logits of tokens [t0, t0 + nt) x expert e (one warp each)
+    // ---- router logits of tokens [t0, t0 + nt) x expert e; warp pair (2i, 2i+1)
+    // takes expert h*8 + i, each warp one half of every K chunk
     uint4 *xs = reinterpret_cast<uint4 *>(smem);
-    const int e = h * kFusedWarps + warp;
-    float acc[kRouteFusedTok];
+    const int el = warp >> 1, kh = warp & 1;
+    const int e = h * kFusedExperts + el;
+    float acc[TOK];
 #pragma unroll
-    for (int j = 0; j < kRouteFusedTok; ++j) acc[j] = 0.f;
+    for (int j = 0; j < TOK; ++j) acc[j] = 0.f;
     for (int kc = 0; kc < H; kc += kFusedKChunk) {
       const int kw = min(kFusedKChunk, H - kc);
-      const int vrow = kw / 8;
+      const int vrow = kw / 8;                 // 16-byte columns in this chunk
+      const int vh = (vrow + 1) / 2;           // columns of each half
+      const int c0 = kh * vh;
       // the router row's loads go out first, so their latency overlaps the x staging
       uint4 wv[kFusedVec];
       if (e < E) {
         const uint16_t *wrow = w_router + (size_t)e * H + kc;
 #pragma unroll
         for (int u = 0; u < kFusedVec; ++u) {
-          const int c = lane + 32 * u;
-          wv[u] = c < vrow ? ld_stream_16(wrow + c * 8) : make_uint4(0, 0, 0, 0);
+          const int c = c0 + lane + 32 * u;
+          wv[u] = (lane + 32 * u < vh && c < vrow) ? ld_stream_16(wrow + c * 8) : make_uint4(0, 0, 0, 0);
         }
       }
       __syncthreads();
-      for (int v = tid; v < kRouteFusedTok * vrow; v += kFusedThreads) {
+      // stage x[t0 .. t0+nt) of this chunk; every load is issued before any store
+      constexpr int kStage = (TOK * (kFusedKChunk / 8) + kFusedThreads - 1) / kFusedThreads;
+      uint4 xv[kStage];
+#pragma unroll
+      for (int it = 0; it < kStage; ++it) {
+        const int v = tid + it * kFusedThreads;
         const int r = v / vrow, c = v - r * vrow;
-        uint4 val = make_uint4(0, 0, 0, 0);
-        if (r < nt) val = *reinterpret_cast<const uint4 *>(x + (size_t)(t0 + r) * H + kc + c * 8);
-        xs[r * (kFusedKChunk / 8) + c] = val;
+        xv[it] = (r < nt) ? *reinterpret_cast<const uint4 *>(x + (size_t)(t0 + r) * H + kc + c * 8)
+                          : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int it = 0; it < kStage; ++it) {
+        const int v = tid + it * kFusedThreads;
+        const int r = v / vrow, c = v - r * vrow;
+        if (r < TOK) xs[r * (kFusedKChunk / 8) + c] = xv[it];
       }
       __syncthreads();
       if (e < E) {
 #pragma unroll
         for (int u = 0; u < kFusedVec; ++u) {
-          const int c = lane + 32 * u;
-          if (c < vrow) {
+          const int c = c0 + lane + 32 * u;
+          if (lane + 32 * u < vh && c < vrow) {
             float wf[8];
             bf16x8_to_float(wv[u], wf);
 #pragma unroll
-            for (int j = 0; j < kRouteFusedTok; ++j) {
+            for (int j = 0; j < TOK; ++j) {
               float xf[8];
               bf16x8_to_float(xs[j * (kFusedKChunk / 8) + c], xf);
 #pragma unroll
@@ -104,19 +124,22 @@ k_route_fused(const uint16_t *__restrict__ x, const uint16_t *__restrict__ w_rou
         }
       }
     }
-    if (e < E) {
-      float mine = 0.f;
+    // reduce each token's sum over the lanes; the upper K half hands its sums
+    // to the lower one through shared memory
+    float mine = 0.f;
 #pragma unroll
-      for (int j = 0; j < kRouteFusedTok; ++j) {
-        float v = acc[j];
+    for (int j = 0; j < TOK; ++j) {
+      float v = acc[j];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == j) mine = v;
-      }
-      if (lane < nt) {
-        if (bias != nullptr) mine += bias[e];
-        logits_ws[(size_t)(t0 + lane) * E + e] = float_to_bf16_bits(mine);
-      }
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == j) mine = v;
+    }
+    if (kh == 1 && lane < TOK) half_sum[el][lane] = mine;
+    __syncthreads();
+    if (kh == 0 && e < E && lane < nt) {
+      float v = mine + half_sum[el][lane];
+      if (bias != nullptr) v += bias[e];
+      logits_ws[(size_t)(t0 + lane) * E + e] = float_to_bf16_bits(v);
     }
     lg = logits_ws;
     // ---- the last CTA of token group g goes on
@@ -148,11 +171,49 @@ k_route_fused(const uint16_t *__restrict__ x, const uint16_t *__restrict__ w_rou
                       expert_ids, expert_offsets, n_post, status);
 }
 
+// Tokens per group: the smallest of 1, 2, 4, 8 covering M (decode), else 8.
+int fused_tok(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8; }
+
+template <int VPL, int TOK>
+cudaError_t launch_fused_vt(dim3 grid, size_t smem, const uint16_t *x, const uint16_t *w_router,
+                            const float *bias, const uint16_t *logits_in, int M, int E, int H,
+                            int top_k, int renormalize, int B, uint16_t *logits_ws,
+                            int32_t *topk_ids, float *topk_w, int32_t *sorted_ids,
+                            int32_t *expert_ids, int32_t *expert_offsets, int32_t *n_post,
+                            int *counters, int *status, float4 *zb, long zn4, cudaStream_t s) {
+  const void *fn = reinterpret_cast<const void *>(k_route_fused<VPL, TOK>);
+  cudaError_t err = ensure_smem_limit(fn, smem);
+  if (err != cudaSuccess) return err;
+  return launch_pdl(k_route_fused<VPL, TOK>, grid, dim3(kFusedThreads), smem, s, x, w_router, bias,
+                    logits_in, M, E, H, top_k, renormalize, B, logits_ws, topk_ids, topk_w,
+                    sorted_ids, expert_ids, expert_offsets, n_post, counters, status, zb, zn4);
+}
+
+template <int VPL>
+cudaError_t launch_fused_v(int tok, dim3 grid, size_t smem, const uint16_t *x,
+                           const uint16_t *w_router, const float *bias, const uint16_t *logits_in,
+                           int M, int E, int H, int top_k, int renormalize, int B,
+                           uint16_t *logits_ws, int32_t *topk_ids, float *topk_w,
+                           int32_t *sorted_ids, int32_t *expert_ids, int32_t *expert_offsets,
+                           int32_t *n_post, int *counters, int *status, float4 *zb, long zn4,
+                           cudaStream_t s) {
+#define MOE_FUSED_TOK(T)                                                                        \
+  return launch_fused_vt<VPL, T>(grid, smem, x, w_router, bias, logits_in, M, E, H, top_k,      \
+                                 renormalize, B, logits_ws, topk_ids, topk_w, sorted_ids,       \
+                                 expert_ids, expert_offsets, n_post, counters, status, zb, zn4, s)
+  switch (tok) {
+    case 1: MOE_FUSED_TOK(1);
+    case 2: MOE_FUSED_TOK(2);
+    case 4: MOE_FUSED_TOK(4);
+    default: MOE_FUSED_TOK(8);
+  }
+#undef MOE_FUSED_TOK
+}
+
 }  // namespace
 
 bool route_fused_supports(int M, int E, int top_k) {
-  return M >= 1 && M <= kRouteFusedTok * kRouteFusedMaxGroups && (long)M * top_k <= 16384 &&
-         E <= kMaxExperts;
+  return M >= 1 && M <= 8 * kRouteFusedMaxGroups && (long)M * top_k <= 16384 && E <= kMaxExperts;
 }
 
 cudaError_t launch_route_fused(const uint16_t *x, const uint16_t *w_router, const float *bias,
@@ -161,31 +222,27 @@ cudaError_t launch_route_fused(const uint16_t *x, const uint16_t *w_router, cons
                                float *topk_w, int32_t *sorted_ids, int32_t *expert_ids,
                                int32_t *expert_offsets, int32_t *n_post, int *counters,
                                int *status, float *zero_buf, long zero_n, cudaStream_t s) {
-  const int n_g = (M + kRouteFusedTok - 1) / kRouteFusedTok;
-  const int n_h = logits_in != nullptr ? 1 : (E + kFusedWarps - 1) / kFusedWarps;
-  const size_t x_bytes = logits_in != nullptr ? 0 : sizeof(uint16_t) * kRouteFusedTok * kFusedKChunk;
+  const int tok = fused_tok(M);
+  const int n_g = (M + tok - 1) / tok;
+  const int n_h = logits_in != nullptr ? 1 : (E + kFusedExperts - 1) / kFusedExperts;
+  const size_t x_bytes = logits_in != nullptr ? 0 : sizeof(uint16_t) * tok * kFusedKChunk;
   const size_t smem = std::max(x_bytes, align_smem_bytes(E));
   const dim3 grid(n_g, n_h);
   float4 *zb = reinterpret_cast<float4 *>(zero_buf);
   const long zn4 = zero_buf != nullptr ? zero_n / 4 : 0;
-#define MOE_FUSED_CASE(V)                                                                          \
-  do {                                                                                             \
-    cudaError_t err = ensure_smem_limit(reinterpret_cast<const void *>(k_route_fused<V>), smem);   \
-    if (err != cudaSuccess) return err;                                                            \
-    k_route_fused<V><<<grid, kFusedThreads, smem, s>>>(                                            \
-        x, w_router, bias, logits_in, M, E, H, top_k, renormalize, B, logits_ws, topk_ids, topk_w, \
-        sorted_ids, expert_ids, expert_offsets, n_post, counters, status, zb, zn4);                \
-  } while (0)
+#define MOE_FUSED_CASE(V)                                                                        \
+  return launch_fused_v<V>(tok, grid, smem, x, w_router, bias, logits_in, M, E, H, top_k,        \
+                           renormalize, B, logits_ws, topk_ids, topk_w, sorted_ids, expert_ids, \
+                           expert_offsets, n_post, counters, status, zb, zn4, s)
   switch (topk_vpl(E)) {
-    case 1: MOE_FUSED_CASE(1); break;
-    case 2: MOE_FUSED_CASE(2); break;
-    case 4: MOE_FUSED_CASE(4); break;
-    case 8: MOE_FUSED_CASE(8); break;
-    case 16: MOE_FUSED_CASE(16); break;
-    default: MOE_FUSED_CASE(32); break;
+    case 1: MOE_FUSED_CASE(1);
+    case 2: MOE_FUSED_CASE(2);
+    case 4: MOE_FUSED_CASE(4);
+    case 8: MOE_FUSED_CASE(8);
+    case 16: MOE_FUSED_CASE(16);
+    default: MOE_FUSED_CASE(32);
   }
 #undef MOE_FUSED_CASE
-  return cudaGetLastError();
 }
 
 }  // namespace moe

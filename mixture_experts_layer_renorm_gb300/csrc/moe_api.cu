@@ -214,10 +214,12 @@ moe_status_t run_gemm1(const uint16_t *x, const uint16_t *w13, const int32_t *so
   }
 }
 
+// early_weights: GEMM 2 directly follows GEMM 1 of the same layer (moe_forward),
+// so its weight loads may start before GEMM 1 has finished.
 moe_status_t run_gemm2(const uint16_t *a, const uint16_t *w2, const int32_t *sorted,
                        const int32_t *eids, const int32_t *npost, const float *wts, int M,
                        int top_k, int E, int H, int I, int B, float *yacc, int *status,
-                       cudaStream_t s) {
+                       bool early_weights, cudaStream_t s) {
   const long P = static_cast<long>(M) * top_k;
   const int cap = static_cast<int>(capacity(P, E, B));
   switch (pick_path(M, E, top_k, B)) {
@@ -225,7 +227,7 @@ moe_status_t run_gemm2(const uint16_t *a, const uint16_t *w2, const int32_t *sor
       const int ks = pick_ksplit(M, E, top_k, (H + 255) / 256, (I + 63) / 64);
       return cuda_status(moe::launch_tc_w2_combine(a, w2, sorted, eids, npost, wts,
                                                    static_cast<int>(P), top_k, E, H, I, B, cap,
-                                                   yacc, ks, status, s));
+                                                   yacc, ks, status, early_weights, s));
     }
     case GemmPath::kGemv:
     default:
@@ -373,7 +375,8 @@ moe_status_t moe_grouped_gemm_w2_combine(const moe_bf16_t *a, const moe_bf16_t *
   cudaError_t e = cudaMemsetAsync(yacc, 0, sizeof(float) * static_cast<size_t>(M) * H, stream);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   st = run_gemm2(a, w2, sorted_token_ids, expert_ids, num_tokens_post_padded, topk_weights, M,
-                 top_k, E, H, I, block_size_m, yacc, at<int>(ws, 0), stream);
+                 top_k, E, H, I, block_size_m, yacc, at<int>(ws, 0), /*early_weights=*/false,
+                 stream);
   if (st != MOE_OK) return st;
   return cuda_status(moe::launch_finalize(yacc, residual, M, H, y, stream));
 }
@@ -422,13 +425,15 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *w_router,
   if (st != MOE_OK) return st;
   uint16_t *a = at<uint16_t>(ws, L.a);
   const bool split_ok = zeroed && want_split;  // scratch reserved and cleared
+  // cleared before GEMM 1, so that GEMM 2 directly follows it in the stream
+  if (!zeroed && cudaMemsetAsync(yacc, 0, sizeof(float) * static_cast<size_t>(yn), stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
   st = run_gemm1(x, w13, sorted, eids, npost, M, top_k, E, H, I, B, a,
                  split_ok ? at<float>(ws, L.hacc) : nullptr,
                  split_ok ? at<int>(ws, L.tcnt) : nullptr, status, stream);
   if (st != MOE_OK) return st;
-  if (!zeroed && cudaMemsetAsync(yacc, 0, sizeof(float) * static_cast<size_t>(yn), stream) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  st = run_gemm2(a, w2, sorted, eids, npost, wts, M, top_k, E, H, I, B, yacc, status, stream);
+  st = run_gemm2(a, w2, sorted, eids, npost, wts, M, top_k, E, H, I, B, yacc, status,
+                 /*early_weights=*/true, stream);
   if (st != MOE_OK) return st;
   return cuda_status(moe::launch_finalize(yacc, residual, M, H, y, stream));
 }
@@ -544,7 +549,7 @@ extern "C" moe_status_t moe_grouped_gemm_w2_combine_noalloc(
   if (cudaMemsetAsync(acc, 0, sizeof(float) * static_cast<size_t>(M) * H, stream) != cudaSuccess)
     return MOE_ERR_CUDA;
   st = run_gemm2(a, w2, sorted_token_ids, expert_ids, num_tokens_post_padded, topk_weights, M,
-                 top_k, E, H, I, block_size_m, acc, lib_status(), stream);
+                 top_k, E, H, I, block_size_m, acc, lib_status(), /*early_weights=*/false, stream);
   if (st != MOE_OK) return st;
   return cuda_status(moe::launch_finalize(acc, residual, M, H, y, stream));
 }

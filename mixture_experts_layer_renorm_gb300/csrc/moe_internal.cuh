@@ -14,8 +14,35 @@ constexpr int kMaxTopK = 32;
 // fused routing kernel's completion counters from int kCountersOffset on.
 constexpr int kStatusBytes = 1024;
 constexpr int kCountersOffset = 64;
-constexpr int kRouteFusedTok = 8;          // tokens per CTA of the fused routing kernel
-constexpr int kRouteFusedMaxGroups = 64;   // so at most 512 tokens; one more counter for the align
+constexpr int kRouteFusedMaxGroups = 64;   // token groups (<= 8 tokens each); one more counter for the align
+
+// Programmatic dependent launch.  Every kernel of the library is launched with
+// launch_pdl, so it may become resident while the kernel before it in the
+// stream is still running.  It calls griddep_wait() before it touches
+// anything an earlier kernel writes (this waits for the whole earlier kernel
+// and makes its writes visible) and griddep_launch_dependents() to let the
+// next kernel start the same way.  Both are no-ops for a kernel launched
+// without the attribute or after a kernel that does not signal.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
 
 // Device status codes (same numbering as moe_status_t).
 constexpr int kStatusBadExpertId = 5;
@@ -102,7 +129,7 @@ cudaError_t launch_tc_w2_combine(const uint16_t *a, const uint16_t *w2, const in
                                  const int32_t *expert_ids, const int32_t *n_post,
                                  const float *topk_weights, int P, int top_k, int E, int H, int I,
                                  int B, int cap, float *y_acc, int ksplit, int *status,
-                                 cudaStream_t s);
+                                 bool early_weights, cudaStream_t s);
 
 // S0 on the tensor cores: logits [M,E] = bf16(x . w_router^T + bias), blocks of 128 tokens.
 cudaError_t launch_tc_router(const uint16_t *x, const uint16_t *w_router, const float *bias, int M,

@@ -261,6 +261,9 @@ int moe_pick_block_size(int M, int E, int top_k, int H, int I) {
   if (mean <= 24) return 16;
   if (mean <= 48) return 32;
   if (mean <= 96) return 64;
+  // 256-token tiles (one N = 256 MMA per K step) pay off once their padding is
+  // small next to the groups (prefill, about 1024 pairs per expert and more)
+  if (mean >= 1024) return 256;
   return 128;
 }
 

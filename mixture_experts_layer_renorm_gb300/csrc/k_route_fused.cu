@@ -43,7 +43,7 @@ k_route_fused(const uint16_t *__restrict__ x, const uint16_t *__restrict__ w_rou
               int32_t *__restrict__ sorted_ids, int32_t *__restrict__ expert_ids,
               int32_t *__restrict__ expert_offsets, int32_t *__restrict__ n_post,
               int *__restrict__ counters, int *status, float4 *__restrict__ zero_buf,
-              long zero_n4) {
+              long zero_n4, int skip_sort) {
   // the previous layer may still read the accumulator this kernel clears
   griddep_wait();
   griddep_launch_dependents();
@@ -166,6 +166,23 @@ k_route_fused(const uint16_t *__restrict__ x, const uint16_t *__restrict__ w_rou
   if (tid == 0) counters[kRouteFusedMaxGroups] = 0;
   __threadfence();
 
+  if (skip_sort) {
+    // ---- small batch (M * top_k * 4 <= E): no grouping; block p holds pair p
+    // alone and its expert is topk_ids[p] (vLLM blog, "Small batches skip the
+    // sort").  expert_offsets is not written: this layout has no groups.
+    const int P = M * top_k;
+    for (int i = tid; i < P * B; i += kFusedThreads) {
+      const int p = i / B, r = i - p * B;
+      sorted_ids[i] = r == 0 ? p : P;
+      if (r == 0) {
+        const int e = __ldcg(topk_ids + p);
+        if (e < 0 || e >= E) report_status(status, kStatusBadExpertId);
+        expert_ids[p] = e;
+      }
+    }
+    if (tid == 0) *n_post = P * B;
+    return;
+  }
   // ---- the align over every pair, in this one CTA
   align_one_cta<true>(reinterpret_cast<int *>(smem), topk_ids, M * top_k, E, B, sorted_ids,
                       expert_ids, expert_offsets, n_post, status);
@@ -180,13 +197,15 @@ cudaError_t launch_fused_vt(dim3 grid, size_t smem, const uint16_t *x, const uin
                             int top_k, int renormalize, int B, uint16_t *logits_ws,
                             int32_t *topk_ids, float *topk_w, int32_t *sorted_ids,
                             int32_t *expert_ids, int32_t *expert_offsets, int32_t *n_post,
-                            int *counters, int *status, float4 *zb, long zn4, cudaStream_t s) {
+                            int *counters, int *status, float4 *zb, long zn4, int skip_sort,
+                            cudaStream_t s) {
   const void *fn = reinterpret_cast<const void *>(k_route_fused<VPL, TOK>);
   cudaError_t err = ensure_smem_limit(fn, smem);
   if (err != cudaSuccess) return err;
   return launch_pdl(k_route_fused<VPL, TOK>, grid, dim3(kFusedThreads), smem, s, x, w_router, bias,
                     logits_in, M, E, H, top_k, renormalize, B, logits_ws, topk_ids, topk_w,
-                    sorted_ids, expert_ids, expert_offsets, n_post, counters, status, zb, zn4);
+                    sorted_ids, expert_ids, expert_offsets, n_post, counters, status, zb, zn4,
+                    skip_sort);
 }
 
 template <int VPL>
@@ -196,11 +215,12 @@ cudaError_t launch_fused_v(int tok, dim3 grid, size_t smem, const uint16_t *x,
                            uint16_t *logits_ws, int32_t *topk_ids, float *topk_w,
                            int32_t *sorted_ids, int32_t *expert_ids, int32_t *expert_offsets,
                            int32_t *n_post, int *counters, int *status, float4 *zb, long zn4,
-                           cudaStream_t s) {
+                           int skip_sort, cudaStream_t s) {
 #define MOE_FUSED_TOK(T)                                                                        \
   return launch_fused_vt<VPL, T>(grid, smem, x, w_router, bias, logits_in, M, E, H, top_k,      \
                                  renormalize, B, logits_ws, topk_ids, topk_w, sorted_ids,       \
-                                 expert_ids, expert_offsets, n_post, counters, status, zb, zn4, s)
+                                 expert_ids, expert_offsets, n_post, counters, status, zb, zn4, \
+                                 skip_sort, s)
   switch (tok) {
     case 1: MOE_FUSED_TOK(1);
     case 2: MOE_FUSED_TOK(2);
@@ -221,7 +241,8 @@ cudaError_t launch_route_fused(const uint16_t *x, const uint16_t *w_router, cons
                                int renormalize, int B, uint16_t *logits_ws, int32_t *topk_ids,
                                float *topk_w, int32_t *sorted_ids, int32_t *expert_ids,
                                int32_t *expert_offsets, int32_t *n_post, int *counters,
-                               int *status, float *zero_buf, long zero_n, cudaStream_t s) {
+                               int *status, float *zero_buf, long zero_n, bool skip_sort,
+                               cudaStream_t s) {
   const int tok = fused_tok(M);
   const int n_g = (M + tok - 1) / tok;
   const int n_h = logits_in != nullptr ? 1 : (E + kFusedExperts - 1) / kFusedExperts;
@@ -233,7 +254,7 @@ cudaError_t launch_route_fused(const uint16_t *x, const uint16_t *w_router, cons
 #define MOE_FUSED_CASE(V)                                                                        \
   return launch_fused_v<V>(tok, grid, smem, x, w_router, bias, logits_in, M, E, H, top_k,        \
                            renormalize, B, logits_ws, topk_ids, topk_w, sorted_ids, expert_ids, \
-                           expert_offsets, n_post, counters, status, zb, zn4, s)
+                           expert_offsets, n_post, counters, status, zb, zn4, skip_sort ? 1 : 0, s)
   switch (topk_vpl(E)) {
     case 1: MOE_FUSED_CASE(1);
     case 2: MOE_FUSED_CASE(2);

@@ -142,13 +142,16 @@ moe_status_t run_router(const uint16_t *x, const uint16_t *w_router, const float
 // S0 + S1 + S2.  Decode-sized batches take one fused launch (which also
 // clears zero_buf, the combine accumulator, when given); larger ones run the
 // router, top-k and align kernels.  *zeroed tells whether zero_buf was cleared.
+// skip_sort (only moe_forward asks, for M * top_k * 4 <= E): the fused launch
+// puts each pair in its own block instead of grouping by expert; the vLLM
+// blog, "Small batches skip the sort".
 constexpr int kFusedRouteMaxTokens = 256;
 
 moe_status_t run_route(const uint16_t *x, const uint16_t *w_router, const uint16_t *router_logits,
                        const float *bias, int M, int E, int top_k, int H, int renormalize, int B,
                        uint16_t *logits_ws, int32_t *ids, float *wts, int32_t *sorted,
                        int32_t *eids, int32_t *offs, int32_t *npost, int32_t *hist, int *control,
-                       float *zero_buf, long zero_n, bool *zeroed, cudaStream_t s) {
+                       float *zero_buf, long zero_n, bool *zeroed, bool skip_sort, cudaStream_t s) {
   const long P = static_cast<long>(M) * top_k;
   const int cap = static_cast<int>(capacity(P, E, B));
   *zeroed = false;
@@ -156,7 +159,8 @@ moe_status_t run_route(const uint16_t *x, const uint16_t *w_router, const uint16
     *zeroed = zero_buf != nullptr;
     return cuda_status(moe::launch_route_fused(
         x, w_router, bias, router_logits, M, E, H, top_k, renormalize, B, logits_ws, ids, wts,
-        sorted, eids, offs, npost, control + moe::kCountersOffset, control, zero_buf, zero_n, s));
+        sorted, eids, offs, npost, control + moe::kCountersOffset, control, zero_buf, zero_n,
+        skip_sort, s));
   }
   const uint16_t *logits = router_logits;
   if (w_router) {
@@ -424,7 +428,8 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *w_router,
   bool zeroed = false;
   st = run_route(x, w_router, router_logits, router_bias, M, E, top_k, H, renormalize, B,
                  at<uint16_t>(ws, L.logits), ids, wts, sorted, eids, offs, npost,
-                 at<int32_t>(ws, L.hist), status, yacc, zn, &zeroed, stream);
+                 at<int32_t>(ws, L.hist), status, yacc, zn, &zeroed,
+                 /*skip_sort=*/P * 4 <= E, stream);
   if (st != MOE_OK) return st;
   uint16_t *a = at<uint16_t>(ws, L.a);
   const bool split_ok = zeroed && want_split;  // scratch reserved and cleared
@@ -467,7 +472,8 @@ moe_status_t moe_route(const moe_bf16_t *x, const moe_bf16_t *w_router,
   return run_route(x, w_router, router_logits, router_bias, M, E, top_k, H, renormalize,
                    block_size_m, at<uint16_t>(ws, L.logits), topk_ids, topk_weights,
                    sorted_token_ids, expert_ids, expert_offsets, num_tokens_post_padded,
-                   at<int32_t>(ws, L.hist), at<int>(ws, 0), nullptr, 0, &zeroed, stream);
+                   at<int32_t>(ws, L.hist), at<int>(ws, 0), nullptr, 0, &zeroed,
+                   /*skip_sort=*/false, stream);
 }
 
 moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream) {

@@ -148,7 +148,8 @@ cudaError_t launch_route_fused(const uint16_t *x, const uint16_t *w_router, cons
                                int renormalize, int B, uint16_t *logits_ws, int32_t *topk_ids,
                                float *topk_w, int32_t *sorted_ids, int32_t *expert_ids,
                                int32_t *expert_offsets, int32_t *n_post, int *counters,
-                               int *status, float *zero_buf, long zero_n, cudaStream_t s);
+                               int *status, float *zero_buf, long zero_n, bool skip_sort,
+                               cudaStream_t s);
 
 int num_sms();
 

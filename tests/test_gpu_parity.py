@@ -477,3 +477,46 @@ def test_route_with_router_weights(cfg, M):
     if agree.all():
         rs, re_, ro, rn = oracle.align_block_size(rid, w.E, B)
         assert n == rn and np.array_equal(body, rs[:n]) and np.array_equal(out["o"], ro)
+
+
+# ----------------------------------------------------------------------------- small-batch sort skip
+
+@pytest.mark.parametrize("cfg,M", [(2, 1), (2, 4), (5, 1), (4, 1), (4, 8)])
+def test_forward_small_batch_skips_the_sort(cfg, M):
+    """M * top_k * 4 <= E: moe_forward puts each pair in its own block (vLLM blog,
+    "Small batches skip the sort").  Its y must match the always-sort path
+    through the step entry points, and both the oracle, on the same logits."""
+    w = synth.WORKLOADS[cfg]
+    assert M * w.top_k * 4 <= w.E
+    wt = synth.layer_weights(w, device=DEV)
+    inp = synth.layer_input(w, M, device=DEV)
+    x = inp["x"]
+    lg = inp["router_logits"]
+    if lg is None:  # route from fixed logits so both paths see the same ids
+        lg = torch.empty((M, w.E), dtype=torch.bfloat16, device=DEV)
+        moe.moe_router_logits(x, wt["w_router"], lg, router_bias=wt["router_bias"])
+    B = 16
+    y_skip, ids_skip, _ = run_forward(x, wt["w13"], wt["w2"], w.top_k, lg=lg, B=B, renorm=w.renormalize)
+    # the always-sort path
+    P = M * w.top_k
+    cap = moe.moe_align_capacity(M, w.top_k, w.E, B)
+    ids = torch.empty((M, w.top_k), dtype=torch.int32, device=DEV)
+    wts = torch.empty((M, w.top_k), dtype=torch.float32, device=DEV)
+    s = torch.empty(cap, dtype=torch.int32, device=DEV)
+    e = torch.empty(cap // B, dtype=torch.int32, device=DEV)
+    o = torch.empty(w.E + 1, dtype=torch.int32, device=DEV)
+    n = torch.empty(1, dtype=torch.int32, device=DEV)
+    ws = moe.Workspace(M, w.E, w.top_k, w.H, w.I, B)
+    moe.moe_topk_softmax(lg, w.top_k, ids, wts, renormalize=w.renormalize)
+    moe.moe_align_block_size(ids, w.E, B, s, e, o, n, ws)
+    a = torch.empty((P, w.I), dtype=torch.bfloat16, device=DEV)
+    y_sort = torch.empty((M, w.H), dtype=torch.bfloat16, device=DEV)
+    moe.moe_grouped_gemm_w13_act(x, wt["w13"], s, e, n, w.top_k, B, a)
+    moe.moe_grouped_gemm_w2_combine(a, wt["w2"], s, e, n, wts, w.top_k, B, y_sort, ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(ids_skip, ids.cpu().numpy())
+    assert_close_bf16(y_skip, bits(y_sort), "y skip vs sort")
+    ref = oracle.moe_forward(bits(x), bits(wt["w13"]), bits(wt["w2"]), w.top_k, router_logits=bits(lg),
+                             renormalize=w.renormalize)
+    assert np.array_equal(ids_skip, ref["topk_ids"])
+    assert_close_bf16(y_skip, ref["y"], "y")

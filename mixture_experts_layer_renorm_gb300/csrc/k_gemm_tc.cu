@@ -261,20 +261,45 @@ struct TcConfig {
 
 // Tile t of the persistent schedule: block b, weight tile c, and the K-stage
 // range [kb0, kb1) of split sp (ksplit splits; the splits of one tile are
-// neighbours in the schedule and run side by side).
+// neighbours in the schedule and run side by side).  With n_pass > 1 (GEMM 2
+// with a large combine accumulator) the weight tiles are cut into n_pass
+// ranges of ctp tiles, run one range after the other over every block: while
+// a range runs only its columns of y_acc are live, small enough to stay in L2
+// across the top_k additions each token receives.
 struct TileCoord {
   int b, c, kb0, kb1;
 };
-__device__ __forceinline__ TileCoord tile_coord(int t, int n_ctiles, int ksplit, int nk) {
-  const int per_b = n_ctiles * ksplit;
+struct TileSched {
+  int n_ctiles, ksplit, nk, n_pass, ctp, per_pass;
+};
+__device__ __forceinline__ TileSched make_sched(int n_ctiles, int ksplit, int nk, int n_blocks,
+                                                int n_pass) {
+  TileSched s;
+  s.n_ctiles = n_ctiles;
+  s.ksplit = ksplit;
+  s.nk = nk;
+  s.n_pass = max(1, n_pass);
+  s.ctp = (n_ctiles + s.n_pass - 1) / s.n_pass;
+  s.per_pass = n_blocks * s.ctp * ksplit;
+  return s;
+}
+__device__ __forceinline__ TileCoord tile_coord(int t, const TileSched &s) {
+  int p = 0, ct = s.n_ctiles;
+  if (s.n_pass > 1) {  // every range but the last holds ctp weight tiles
+    p = min(t / s.per_pass, s.n_pass - 1);
+    t -= p * s.per_pass;
+    ct = min(s.ctp, s.n_ctiles - p * s.ctp);
+  }
+  const int per_b = ct * s.ksplit;
   TileCoord tc;
   tc.b = t / per_b;
   const int r = t - tc.b * per_b;
-  tc.c = r / ksplit;
-  const int sp = r - tc.c * ksplit;
-  const int span = (nk + ksplit - 1) / ksplit;
-  tc.kb0 = min(nk, sp * span);
-  tc.kb1 = min(nk, tc.kb0 + span);
+  const int cl = r / s.ksplit;
+  tc.c = p * s.ctp + cl;
+  const int sp = r - cl * s.ksplit;
+  const int span = (s.nk + s.ksplit - 1) / s.ksplit;
+  tc.kb0 = min(s.nk, sp * span);
+  tc.kb1 = min(s.nk, tc.kb0 + span);
   return tc;
 }
 
@@ -327,7 +352,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
           const int32_t *__restrict__ n_post_ptr, const float *__restrict__ vec, int P, int top_k,
           int E, int K, int R_out, int a_rows, int B, int cap, int n_ctiles, int ksplit,
           float *__restrict__ h_acc, int *__restrict__ tile_cnt, uint16_t *__restrict__ out16,
-          float *__restrict__ y_acc, int H_out, int *status, int early_weights) {
+          float *__restrict__ y_acc, int H_out, int *status, int early_weights, int n_pass) {
   using Cfg = TcConfig<N, MODE>;
   constexpr int S = Cfg::kStages;
   // With early_weights (GEMM 2 right after GEMM 1 in one layer) only the row
@@ -393,6 +418,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int nk = (K + kBK - 1) / kBK;
+  const TileSched sched = make_sched(n_ctiles, ksplit, nk, n_blocks, MODE == 1 ? n_pass : 1);
 
   if (warp == 0) {
     // ------------------------------------------------------------ weight tiles (TMA)
@@ -403,13 +429,13 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
       int g = 0;
       bool stop = false;
       int t = blockIdx.x;
-      int e_next = MODE == 2 ? 0 : expert_ids[tile_coord(t, n_ctiles, ksplit, nk).b];
+      int e_next = MODE == 2 ? 0 : expert_ids[tile_coord(t, sched).b];
       for (; t < n_tiles && !stop; t += gridDim.x) {
-        const TileCoord tc = tile_coord(t, n_ctiles, ksplit, nk);
+        const TileCoord tc = tile_coord(t, sched);
         const int c = tc.c;
         const int e = e_next;
         const int tn = t + static_cast<int>(gridDim.x);
-        if (MODE != 2 && tn < n_tiles) e_next = expert_ids[tile_coord(tn, n_ctiles, ksplit, nk).b];
+        if (MODE != 2 && tn < n_tiles) e_next = expert_ids[tile_coord(tn, sched).b];
         // weight rows of the stage's tile(s); wide GEMM 1 loads 64 gate rows
         // and the matching 64 up rows as the two halves of one 128-row tile
         // (the map's box is then 64 rows high)
@@ -462,7 +488,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
     // Entries of sorted_token_ids (MODE 2: token ids) of this thread's rows in
     // tile t; the next tile's are loaded while this tile's rows are copied.
     auto fetch_ids = [&](int t, int (&ids)[Cfg::kChunksPerThread]) {
-      const int b = tile_coord(t, n_ctiles, ksplit, nk).b;
+      const int b = tile_coord(t, sched).b;
 #pragma unroll
       for (int u = 0; u < Cfg::kChunksPerThread; ++u) {
         const int r = (gt >> 3) + 16 * u;
@@ -475,7 +501,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
     int g = 0;
     bool stop = false;
     for (int t = blockIdx.x; t < n_tiles && !stop; t += gridDim.x) {
-      const TileCoord tc = tile_coord(t, n_ctiles, ksplit, nk);
+      const TileCoord tc = tile_coord(t, sched);
       int rowv[Cfg::kChunksPerThread];
 #pragma unroll
       for (int u = 0; u < Cfg::kChunksPerThread; ++u) {
@@ -517,7 +543,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
       int g = 0, i = 0;
       bool stop = false;
       for (int t = blockIdx.x; t < n_tiles && !stop; t += gridDim.x) {
-        const TileCoord tc = tile_coord(t, n_ctiles, ksplit, nk);
+        const TileCoord tc = tile_coord(t, sched);
         const bool two = !Cfg::kWide && (MODE == 0 || tc.c * 2 * kTileM + kTileM < a_rows);
         const int acc = i % Cfg::kAccBufs;
         const uint32_t use = i / Cfg::kAccBufs;
@@ -557,7 +583,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     int i = 0;
     for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
-      const TileCoord tc = tile_coord(t, n_ctiles, ksplit, nk);
+      const TileCoord tc = tile_coord(t, sched);
       const int b = tc.b, c = tc.c;
       // a block whose expert id lies outside [0, E) is computed (on zero
       // weights) but writes nothing
@@ -671,46 +697,61 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
         // adds; measured faster for 256-token tiles, slower for narrower ones)
         float *scr = reinterpret_cast<float *>(xchg) + (warp - 2) * (16 * 32);  // [16 tokens][32 ch]
         const int q4 = lane & 7, cg = lane >> 3;
-#pragma unroll 1
-        for (int item = half; item < (two ? 2 : 1) * n_chunks; item += 2) {
+        // one item: 16 columns of one 128-row half; a warp takes every second
+        // item and loads two before it waits, so one TMEM round trip serves two
+        auto process = [&](int item, const uint32_t (&o)[16]) {
           const int h = item / n_chunks, j0 = (item - h * n_chunks) * 16;
           const int n = c * Cfg::kRowsPerCTile + h * kTileM + q * 32 + lane;
-          uint32_t o[16];
-          tmem_ld_32x32b_x16(d0 + h * N + j0, o);
-          tmem_ld_wait();
           if (MODE == 1 && Cfg::kWide) {
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) scr[jj * 32 + lane] = __uint_as_float(o[jj]);
-            __syncwarp();
-            const int n4 = n - lane + 4 * q4;  // first of this thread's 4 channels
-            if (n4 < H_out) {                  // H_out is a multiple of 16: all 4 or none
+              for (int jj = 0; jj < 16; ++jj) scr[jj * 32 + lane] = __uint_as_float(o[jj]);
+              __syncwarp();
+              const int n4 = n - lane + 4 * q4;  // first of this thread's 4 channels
+              if (n4 < H_out) {                  // H_out is a multiple of 16: all 4 or none
 #pragma unroll
-              for (int jj = 0; jj < 4; ++jj) {
-                const int col = cg * 4 + jj;
-                const int d = dst_row[j0 + col];
-                if (d >= 0) {
-                  const float wgt = dst_w[j0 + col];
-                  const float4 v = *reinterpret_cast<const float4 *>(scr + col * 32 + 4 * q4);
-                  atomicAdd(reinterpret_cast<float4 *>(y_acc + (size_t)d * H_out + n4),
-                            make_float4(wgt * v.x, wgt * v.y, wgt * v.z, wgt * v.w));
+                for (int jj = 0; jj < 4; ++jj) {
+                  const int col = cg * 4 + jj;
+                  const int d = dst_row[j0 + col];
+                  if (d >= 0) {
+                    const float wgt = dst_w[j0 + col];
+                    const float4 v = *reinterpret_cast<const float4 *>(scr + col * 32 + 4 * q4);
+                    atomicAdd(reinterpret_cast<float4 *>(y_acc + (size_t)d * H_out + n4),
+                              make_float4(wgt * v.x, wgt * v.y, wgt * v.z, wgt * v.w));
+                  }
+                }
+              }
+              __syncwarp();  // the next item overwrites the staging rows
+            } else {
+              const bool valid = n < (MODE == 1 ? H_out : a_rows);
+              const float bias = (MODE == 2 && valid && vec != nullptr) ? vec[n] : 0.f;
+#pragma unroll
+              for (int jj = 0; jj < 16; ++jj) {
+                const int d = dst_row[j0 + jj];
+                if (valid && d >= 0) {
+                  if (MODE == 1)
+                    atomicAdd(y_acc + (size_t)d * H_out + n, dst_w[j0 + jj] * __uint_as_float(o[jj]));
+                  else
+                    out16[(size_t)d * a_rows + n] = float_to_bf16_bits(__uint_as_float(o[jj]) + bias);
                 }
               }
             }
-            __syncwarp();  // the next item overwrites the staging rows
-          } else {
-            const bool valid = n < (MODE == 1 ? H_out : a_rows);
-            const float bias = (MODE == 2 && valid && vec != nullptr) ? vec[n] : 0.f;
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
-              const int d = dst_row[j0 + jj];
-              if (valid && d >= 0) {
-                if (MODE == 1)
-                  atomicAdd(y_acc + (size_t)d * H_out + n, dst_w[j0 + jj] * __uint_as_float(o[jj]));
-                else
-                  out16[(size_t)d * a_rows + n] = float_to_bf16_bits(__uint_as_float(o[jj]) + bias);
-              }
-            }
+        };
+        const int n_items = (two ? 2 : 1) * n_chunks;
+#pragma unroll 1
+        for (int item = half; item < n_items; item += 4) {
+          const int item2 = item + 2;
+          uint32_t o[16], o2[16];
+          {
+            const int h = item / n_chunks, j0 = (item - h * n_chunks) * 16;
+            tmem_ld_32x32b_x16(d0 + h * N + j0, o);
           }
+          if (item2 < n_items) {
+            const int h = item2 / n_chunks, j0 = (item2 - h * n_chunks) * 16;
+            tmem_ld_32x32b_x16(d0 + h * N + j0, o2);
+          }
+          tmem_ld_wait();
+          process(item, o);
+          if (item2 < n_items) process(item2, o2);
         }
       }
       // this accumulator buffer may be overwritten once all epilogue warps are done with it
@@ -831,6 +872,7 @@ struct TcArgs {
   int *status;
   long max_blocks;  // host-side bound on the blocks (tiles = blocks * n_ctiles * ksplit)
   int early_weights;
+  int n_pass;  // GEMM 2: ranges of weight tiles run one after the other (1: none)
 };
 
 template <int N, int MODE>
@@ -846,7 +888,7 @@ cudaError_t launch_tc_n(const CUtensorMap &map_w, const TcArgs &a, cudaStream_t 
   return launch_pdl(kern, dim3(grid), dim3(kTcThreads), Cfg::kSmemBytes, s, map_w, a.src,
                     a.src_rows, a.sorted_ids, a.expert_ids, a.n_post, a.vec, a.P, a.top_k, a.E,
                     a.K, a.R_out, a.a_rows, a.B, a.cap, a.n_ctiles, a.ksplit, a.h_acc, a.tile_cnt,
-                    a.out16, a.y_acc, a.H_out, a.status, a.early_weights);
+                    a.out16, a.y_acc, a.H_out, a.status, a.early_weights, a.n_pass);
 }
 
 template <int MODE>
@@ -901,6 +943,17 @@ cudaError_t launch_tc_w13_act(const uint16_t *x, const uint16_t *w13, const int3
   return launch_tc<0>(B, map_w, args, s);
 }
 
+// Ranges of GEMM 2's weight tiles run one after the other so that the live
+// part of the fp32 combine accumulator (y_bytes in all) fits L2 beside the
+// weight and activation streams; each extra range reads the activation again.
+static int gemm2_passes(long y_bytes, int n_ctiles) {
+  constexpr long kLiveBytes = 48l << 20;
+  int n = static_cast<int>(std::min<long>((y_bytes + kLiveBytes - 1) / kLiveBytes, n_ctiles));
+  n = std::max(n, 1);
+  const int ctp = (n_ctiles + n - 1) / n;  // ranges actually needed with ctp tiles each
+  return (n_ctiles + ctp - 1) / ctp;
+}
+
 cudaError_t launch_tc_w2_combine(const uint16_t *a, const uint16_t *w2, const int32_t *sorted_ids,
                                  const int32_t *expert_ids, const int32_t *n_post,
                                  const float *topk_weights, int P, int top_k, int E, int H, int I,
@@ -933,6 +986,7 @@ cudaError_t launch_tc_w2_combine(const uint16_t *a, const uint16_t *w2, const in
   args.status = status;
   args.max_blocks = cap / B;
   args.early_weights = early_weights ? 1 : 0;
+  args.n_pass = gemm2_passes(static_cast<long>(P / top_k) * H * 4, args.n_ctiles);
   return launch_tc<1>(B, map_w, args, s);
 }
 

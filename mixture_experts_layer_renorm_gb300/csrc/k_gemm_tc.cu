@@ -575,8 +575,9 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
       }
     }
     __syncwarp();
-  } else {
+  } else if (warp >= 2 && warp < 2 + kEpiWarps) {
     // ------------------------------------------------------------ epilogue
+    // (exactly these warps meet the epilogue's named barriers)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int half = (warp - 2) >> 2;  // the two warps of a quarter split the column chunks
     const int et = threadIdx.x - 64;   // 0..255 over the epilogue warps
@@ -704,37 +705,37 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
           const int n = c * Cfg::kRowsPerCTile + h * kTileM + q * 32 + lane;
           if (MODE == 1 && Cfg::kWide) {
 #pragma unroll
-              for (int jj = 0; jj < 16; ++jj) scr[jj * 32 + lane] = __uint_as_float(o[jj]);
-              __syncwarp();
-              const int n4 = n - lane + 4 * q4;  // first of this thread's 4 channels
-              if (n4 < H_out) {                  // H_out is a multiple of 16: all 4 or none
+            for (int jj = 0; jj < 16; ++jj) scr[jj * 32 + lane] = __uint_as_float(o[jj]);
+            __syncwarp();
+            const int n4 = n - lane + 4 * q4;  // first of this thread's 4 channels
+            if (n4 < H_out) {                  // H_out is a multiple of 16: all 4 or none
 #pragma unroll
-                for (int jj = 0; jj < 4; ++jj) {
-                  const int col = cg * 4 + jj;
-                  const int d = dst_row[j0 + col];
-                  if (d >= 0) {
-                    const float wgt = dst_w[j0 + col];
-                    const float4 v = *reinterpret_cast<const float4 *>(scr + col * 32 + 4 * q4);
-                    atomicAdd(reinterpret_cast<float4 *>(y_acc + (size_t)d * H_out + n4),
-                              make_float4(wgt * v.x, wgt * v.y, wgt * v.z, wgt * v.w));
-                  }
-                }
-              }
-              __syncwarp();  // the next item overwrites the staging rows
-            } else {
-              const bool valid = n < (MODE == 1 ? H_out : a_rows);
-              const float bias = (MODE == 2 && valid && vec != nullptr) ? vec[n] : 0.f;
-#pragma unroll
-              for (int jj = 0; jj < 16; ++jj) {
-                const int d = dst_row[j0 + jj];
-                if (valid && d >= 0) {
-                  if (MODE == 1)
-                    atomicAdd(y_acc + (size_t)d * H_out + n, dst_w[j0 + jj] * __uint_as_float(o[jj]));
-                  else
-                    out16[(size_t)d * a_rows + n] = float_to_bf16_bits(__uint_as_float(o[jj]) + bias);
+              for (int jj = 0; jj < 4; ++jj) {
+                const int col = cg * 4 + jj;
+                const int d = dst_row[j0 + col];
+                if (d >= 0) {
+                  const float wgt = dst_w[j0 + col];
+                  const float4 v = *reinterpret_cast<const float4 *>(scr + col * 32 + 4 * q4);
+                  atomicAdd(reinterpret_cast<float4 *>(y_acc + (size_t)d * H_out + n4),
+                            make_float4(wgt * v.x, wgt * v.y, wgt * v.z, wgt * v.w));
                 }
               }
             }
+            __syncwarp();  // the next item overwrites the staging rows
+          } else {
+            const bool valid = n < (MODE == 1 ? H_out : a_rows);
+            const float bias = (MODE == 2 && valid && vec != nullptr) ? vec[n] : 0.f;
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+              const int d = dst_row[j0 + jj];
+              if (valid && d >= 0) {
+                if (MODE == 1)
+                  atomicAdd(y_acc + (size_t)d * H_out + n, dst_w[j0 + jj] * __uint_as_float(o[jj]));
+                else
+                  out16[(size_t)d * a_rows + n] = float_to_bf16_bits(__uint_as_float(o[jj]) + bias);
+              }
+            }
+          }
         };
         const int n_items = (two ? 2 : 1) * n_chunks;
 #pragma unroll 1

@@ -129,6 +129,11 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
+// Brings [src, src + bytes) into L2 (bytes a multiple of 16, src 16-byte aligned).
+__device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
                : "memory");
@@ -352,7 +357,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
           const int32_t *__restrict__ n_post_ptr, const float *__restrict__ vec, int P, int top_k,
           int E, int K, int R_out, int a_rows, int B, int cap, int n_ctiles, int ksplit,
           float *__restrict__ h_acc, int *__restrict__ tile_cnt, uint16_t *__restrict__ out16,
-          float *__restrict__ y_acc, int H_out, int *status, int early_weights, int n_pass) {
+          float *__restrict__ y_acc, int H_out, int *status, int early_weights, int n_pass,
+          const uint8_t *__restrict__ w_pf, long pf_bytes) {
   using Cfg = TcConfig<N, MODE>;
   constexpr int S = Cfg::kStages;
   // With early_weights (GEMM 2 right after GEMM 1 in one layer) only the row
@@ -360,6 +366,16 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
   // lists it reads were final before GEMM 1 started, so the weights stream
   // while GEMM 1 drains.
   const bool early = MODE == 1 && early_weights != 0;
+  // Decode GEMM 1 inside a layer: while routing still runs, the CTAs bring the
+  // weights their first tiles will most likely read (the lowest experts' W13,
+  // pf_bytes from w_pf) into L2; the host asks only when nearly every expert
+  // is routed to.  Weights never change, so this needs no wait.
+  if (MODE == 0 && pf_bytes > 0 && threadIdx.x == 0) {
+    const long slice = ((pf_bytes + gridDim.x - 1) / gridDim.x + 15) / 16 * 16;
+    const long begin = (long)blockIdx.x * slice;
+    const long end = min(pf_bytes, begin + slice);
+    for (long o = begin; o < end; o += 65536) prefetch_l2_bulk(w_pf + o, (uint32_t)min(65536l, end - o));
+  }
   if (!early) griddep_wait();
   griddep_launch_dependents();
   int n_blocks;
@@ -874,6 +890,8 @@ struct TcArgs {
   long max_blocks;  // host-side bound on the blocks (tiles = blocks * n_ctiles * ksplit)
   int early_weights;
   int n_pass;  // GEMM 2: ranges of weight tiles run one after the other (1: none)
+  const uint8_t *w_pf = nullptr;  // GEMM 1: weights to bring into L2 before the dependency wait
+  long pf_bytes = 0;
 };
 
 template <int N, int MODE>
@@ -889,7 +907,8 @@ cudaError_t launch_tc_n(const CUtensorMap &map_w, const TcArgs &a, cudaStream_t 
   return launch_pdl(kern, dim3(grid), dim3(kTcThreads), Cfg::kSmemBytes, s, map_w, a.src,
                     a.src_rows, a.sorted_ids, a.expert_ids, a.n_post, a.vec, a.P, a.top_k, a.E,
                     a.K, a.R_out, a.a_rows, a.B, a.cap, a.n_ctiles, a.ksplit, a.h_acc, a.tile_cnt,
-                    a.out16, a.y_acc, a.H_out, a.status, a.early_weights, a.n_pass);
+                    a.out16, a.y_acc, a.H_out, a.status, a.early_weights, a.n_pass, a.w_pf,
+                    a.pf_bytes);
 }
 
 template <int MODE>
@@ -911,7 +930,8 @@ bool tc_supports_block(int B) { return B == 16 || B == 32 || B == 64 || B == 128
 cudaError_t launch_tc_w13_act(const uint16_t *x, const uint16_t *w13, const int32_t *sorted_ids,
                               const int32_t *expert_ids, const int32_t *n_post, int P, int top_k,
                               int E, int H, int I, int B, int cap, uint16_t *a, int ksplit,
-                              float *h_acc, int *tile_cnt, int *status, cudaStream_t s) {
+                              float *h_acc, int *tile_cnt, int *status, int pf_experts,
+                              cudaStream_t s) {
   // wide tiles (B = 256): 64 gate rows over 64 up rows per weight tile, no K split
   const bool wide = B == 256;
   CUtensorMap map_w;
@@ -941,6 +961,15 @@ cudaError_t launch_tc_w13_act(const uint16_t *x, const uint16_t *w13, const int3
   args.out16 = a;
   args.status = status;
   args.max_blocks = cap / B;
+  if (pf_experts > 0) {
+    // the first wave's experts: ceil(SMs / tiles per block) blocks, one expert
+    // each at decode sizes, plus one for an expert without pairs among them
+    const long per_e = 2l * I * H * 2;
+    const int wave = (num_sms() + args.n_ctiles * ksplit - 1) / (args.n_ctiles * ksplit) + 1;
+    const int n_e = std::min(std::min(pf_experts, wave), E);
+    args.w_pf = reinterpret_cast<const uint8_t *>(w13);
+    args.pf_bytes = std::min<long>(n_e * per_e, 96l << 20);
+  }
   return launch_tc<0>(B, map_w, args, s);
 }
 

@@ -198,18 +198,22 @@ int pick_ksplit(int M, int E, int top_k, int n_ctiles, int nk) {
   return best;
 }
 
+// prefetch (moe_forward): GEMM 1 may bring the first wave's expert weights
+// into L2 while routing runs, when nearly every expert will be routed to.
 moe_status_t run_gemm1(const uint16_t *x, const uint16_t *w13, const int32_t *sorted,
                        const int32_t *eids, const int32_t *npost, int M, int top_k, int E, int H,
                        int I, int B, uint16_t *a, float *h_acc, int *tile_cnt, int *status,
-                       cudaStream_t s) {
+                       bool prefetch, cudaStream_t s) {
   const long P = static_cast<long>(M) * top_k;
   const int cap = static_cast<int>(capacity(P, E, B));
   switch (pick_path(M, E, top_k, B)) {
     case GemmPath::kTensorCore: {
       const int ks = h_acc != nullptr ? pick_ksplit(M, E, top_k, (I + 127) / 128, (H + 63) / 64) : 1;
+      const double D = E * (1.0 - std::pow(1.0 - static_cast<double>(top_k) / E, M));
+      const int pf_experts = (prefetch && D >= 0.9 * E) ? E : 0;
       return cuda_status(moe::launch_tc_w13_act(x, w13, sorted, eids, npost, static_cast<int>(P),
                                                 top_k, E, H, I, B, cap, a, ks, h_acc, tile_cnt,
-                                                status, s));
+                                                status, pf_experts, s));
     }
     case GemmPath::kGemv:
     default:
@@ -355,7 +359,7 @@ moe_status_t moe_grouped_gemm_w13_act(const moe_bf16_t *x, const moe_bf16_t *w13
     return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w13)) return MOE_ERR_INVALID_ARG;
   return run_gemm1(x, w13, sorted_token_ids, expert_ids, num_tokens_post_padded, M, top_k, E, H, I,
-                   block_size_m, a, nullptr, nullptr, lib_status(), stream);
+                   block_size_m, a, nullptr, nullptr, lib_status(), /*prefetch=*/false, stream);
 }
 
 moe_status_t moe_grouped_gemm_w2_combine(const moe_bf16_t *a, const moe_bf16_t *w2,
@@ -438,7 +442,7 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *w_router,
     return MOE_ERR_CUDA;
   st = run_gemm1(x, w13, sorted, eids, npost, M, top_k, E, H, I, B, a,
                  split_ok ? at<float>(ws, L.hacc) : nullptr,
-                 split_ok ? at<int>(ws, L.tcnt) : nullptr, status, stream);
+                 split_ok ? at<int>(ws, L.tcnt) : nullptr, status, /*prefetch=*/true, stream);
   if (st != MOE_OK) return st;
   st = run_gemm2(a, w2, sorted, eids, npost, wts, M, top_k, E, H, I, B, yacc, status,
                  /*early_weights=*/true, stream);

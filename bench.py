@@ -86,6 +86,20 @@ def load_peaks():
         return dict(FALLBACK_PEAKS, source="fallback")
 
 
+# ----------------------------------------------------------------------------- run metadata
+
+def gpu_info(device):
+    """Name and driver of the GPU the bench ran on."""
+    info = {"name": torch.cuda.get_device_name(device), "driver": None}
+    try:
+        out = subprocess.run(["nvidia-smi", "--query-gpu=driver_version", "--format=csv,noheader"],
+                             capture_output=True, text=True, timeout=20).stdout.split()
+        info["driver"] = out[0] if out else None
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return info
+
+
 # ----------------------------------------------------------------------------- profiled traffic
 
 PROFILES = os.path.join(ROOT, "profiles")
@@ -278,6 +292,13 @@ class Layer:
         stream.synchronize()
         return int(torch.unique(self.ids).numel())
 
+    def pairs_per_expert(self):
+        """Pairs per expert of the last routing this layer computed."""
+        n = torch.bincount(self.ids.reshape(-1).long(), minlength=self.w.E).cpu()
+        active = n[n > 0]
+        return {"max": int(n.max()), "mean_active": round(float(active.float().mean()), 2),
+                "experts_without_pairs": int((n == 0).sum())}
+
 
 def run_point(moe, w, M, steps, warmup, device, stream, flush, L=None):
     """Timed steps: moe_forward with CUDA events around each step only.  Then a
@@ -291,24 +312,30 @@ def run_point(moe, w, M, steps, warmup, device, stream, flush, L=None):
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(warmup + steps)]
     with torch.cuda.stream(stream):
+        torch.cuda.nvtx.range_push(f"warm-up M={M}")
         for i in range(warmup):
             flush.zero_()
             L.forward(moe, i, stream)
         stream.synchronize()
+        torch.cuda.nvtx.range_pop()
+        torch.cuda.nvtx.range_push(f"timed steps M={M}")
         for i in range(warmup, warmup + steps):
             flush.zero_()
             evs[i][0].record(stream)
             L.forward(moe, i, stream)
             evs[i][1].record(stream)
         stream.synchronize()
+        torch.cuda.nvtx.range_pop()
     step_ms = [evs[i][0].elapsed_time(evs[i][1]) for i in range(warmup, warmup + steps)]
     nb = min(steps, 10)
     bev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(nb)]
     with torch.cuda.stream(stream):
+        torch.cuda.nvtx.range_push(f"breakdown M={M}")
         for i in range(nb):
             flush.zero_()
             L.step(moe, warmup + i, stream, bev[i])
         stream.synchronize()
+        torch.cuda.nvtx.range_pop()
     per = [[bev[i][j].elapsed_time(bev[i][j + 1]) for j in range(3)] for i in range(nb)]
     D = [L.distinct_experts(moe, i, stream) for i in range(warmup, warmup + steps)]
     return L, per, step_ms, D
@@ -483,6 +510,7 @@ def ours_stack(args, moe, w, M, device, stream, flush, world, rank, peaks):
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
                      "traffic": None, "peak_source": peaks["source"], "algorithmic_bytes": int(sb)},
         "distinct_experts_per_layer": round(statistics.mean(D), 2),
+        "gpu": gpu_info(device),
         "e2e": None, "cpu_baseline": None,
         "gpu_launches": S.kernels_per_step() * args.steps,
         "clocks": clk.summary(),
@@ -589,6 +617,8 @@ def ours(args):
                            "tc_frac": round(lay_tflops / peaks["bf16_tflops"], 5),
                            "algorithmic_bytes": int(lay_bytes), "flops": int(flops),
                            "distinct_experts": round(D_mean, 2)},
+        "pairs_per_expert": L.pairs_per_expert(),
+        "gpu": gpu_info(device),
         "step_breakdown_ms": {k: round(statistics.mean(p[j] for p in per), 5) for j, k in
                               enumerate(["route", "gemm1_act", "gemm2_combine"])},
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,

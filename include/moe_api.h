@@ -222,6 +222,17 @@ moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream);
  * the workspace (MOE_OK if no kernel reported a problem) and clears it. */
 moe_status_t moe_get_device_status(void *ws, cudaStream_t stream);
 
+/* Self-test of the device failure path.  Launches one CTA that waits, with
+ * the bounded wait every kernel of the library uses, on an mbarrier that
+ * nothing completes; after about limit_ms milliseconds of SM clock (clamped to
+ * [1, 2000]) the wait gives up, records MOE_ERR_DEVICE_TIMEOUT in the
+ * workspace's status word and the kernel returns -- nothing traps, and the
+ * context stays usable.  Read the result with moe_get_device_status.
+ * Returns MOE_ERR_INVALID_ARG for a null or misaligned workspace or one
+ * smaller than its status block. */
+moe_status_t moe_selftest_device_timeout(void *ws, size_t ws_bytes, int limit_ms,
+                                         cudaStream_t stream);
+
 /* A static, human-readable name for a status code. */
 const char *moe_status_string(moe_status_t status);
 

@@ -26,7 +26,7 @@ __all__ = [
     "moe_pick_block_size", "moe_workspace_init", "moe_router_logits", "moe_topk_softmax",
     "moe_align_block_size", "moe_grouped_gemm_w13_act", "moe_grouped_gemm_w2_combine",
     "moe_forward", "moe_get_device_status", "moe_status_string", "Workspace",
-    "moe_grouped_gemm_w2_combine_noalloc", "moe_route",
+    "moe_grouped_gemm_w2_combine_noalloc", "moe_route", "moe_selftest_device_timeout",
 ]
 
 STATUS_NAMES = {
@@ -41,6 +41,7 @@ EXPORTED = (
     "moe_topk_softmax", "moe_align_block_size", "moe_grouped_gemm_w13_act",
     "moe_grouped_gemm_w2_combine", "moe_forward", "moe_workspace_init", "moe_get_device_status",
     "moe_status_string", "moe_grouped_gemm_w2_combine_noalloc", "moe_route",
+    "moe_selftest_device_timeout",
 )
 
 
@@ -84,6 +85,7 @@ def load_library(build_if_missing: bool = False):
         "moe_forward": ([P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, P, P, Z, P], I),
         "moe_workspace_init": ([P, Z, P], I),
         "moe_get_device_status": ([P, P], I),
+        "moe_selftest_device_timeout": ([P, Z, I, P], I),
         "moe_status_string": ([I], ctypes.c_char_p),
     }
     for name, (args, res) in sig.items():
@@ -170,6 +172,13 @@ def _ws(ws):
 def moe_workspace_init(ws, stream=None) -> None:
     ptr, n = _ws(ws)
     _ok(load_library().moe_workspace_init(ptr, n, _stream(stream)), "moe_workspace_init")
+
+
+def moe_selftest_device_timeout(ws, limit_ms: int = 100, stream=None) -> None:
+    """Runs the device timeout self-test; read the result with moe_get_device_status."""
+    ptr, n = _ws(ws)
+    _ok(load_library().moe_selftest_device_timeout(ptr, n, int(limit_ms), _stream(stream)),
+        "moe_selftest_device_timeout")
 
 
 def moe_get_device_status(ws, stream=None) -> int:

@@ -102,7 +102,8 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 
 // Waits for phase `parity` of the barrier; gives up after about 2 s of SM
 // clock (or when another role already gave up), recording the timeout.
-__device__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort, int *status) {
+__device__ bool wait_bounded_for(uint32_t bar, uint32_t parity, volatile int *abort, int *status,
+                                 long long limit_cycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
@@ -110,12 +111,30 @@ __device__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort,
     for (int i = 0; i < 16; ++i)
       if (mbar_try_wait_sleep(bar, parity)) return true;
     if (*abort) return false;
-    if (clock64() - t0 > kWaitLimitCycles) {
+    if (clock64() - t0 > limit_cycles) {
       *abort = 1;
       report_status(status, kStatusTimeout);
       return false;
     }
   }
+}
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort,
+                                             int *status) {
+  return wait_bounded_for(bar, parity, abort, status, kWaitLimitCycles);
+}
+
+// The failure path of wait_bounded, on its own: an mbarrier that nothing
+// completes, waited for limit_cycles.
+__global__ void k_selftest_timeout(int *status, long long limit_cycles) {
+  __shared__ uint64_t bar;
+  __shared__ volatile int abort;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) (void)wait_bounded_for(smem_u32(&bar), 0, &abort, status, limit_cycles);
 }
 
 // ---------------------------------------------------------------- copies
@@ -1018,6 +1037,16 @@ cudaError_t launch_tc_w2_combine(const uint16_t *a, const uint16_t *w2, const in
   args.early_weights = early_weights ? 1 : 0;
   args.n_pass = gemm2_passes(static_cast<long>(P / top_k) * H * 4, args.n_ctiles);
   return launch_tc<1>(B, map_w, args, s);
+}
+
+cudaError_t launch_selftest_timeout(int *status, int limit_ms, cudaStream_t s) {
+  int dev = 0, khz = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err == cudaSuccess) err = cudaDeviceGetAttribute(&khz, cudaDevAttrClockRate, dev);
+  if (err != cudaSuccess) return err;
+  const long long cycles = static_cast<long long>(std::max(1, std::min(limit_ms, 2000))) * khz;
+  k_selftest_timeout<<<1, 32, 0, s>>>(status, cycles);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_tc_router(const uint16_t *x, const uint16_t *w_router, const float *bias, int M,

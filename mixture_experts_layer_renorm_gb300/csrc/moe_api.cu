@@ -480,6 +480,13 @@ moe_status_t moe_route(const moe_bf16_t *x, const moe_bf16_t *w_router,
                    /*skip_sort=*/false, stream);
 }
 
+moe_status_t moe_selftest_device_timeout(void *ws, size_t ws_bytes, int limit_ms,
+                                         cudaStream_t stream) {
+  if (!ws || ws_bytes < static_cast<size_t>(moe::kStatusBytes)) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return MOE_ERR_INVALID_ARG;
+  return cuda_status(moe::launch_selftest_timeout(at<int>(ws, 0), limit_ms, stream));
+}
+
 moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream) {
   if (!ws || ws_bytes < static_cast<size_t>(moe::kStatusBytes)) return MOE_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return MOE_ERR_INVALID_ARG;

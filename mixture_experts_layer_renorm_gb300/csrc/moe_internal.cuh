@@ -133,6 +133,9 @@ cudaError_t launch_tc_w2_combine(const uint16_t *a, const uint16_t *w2, const in
                                  bool early_weights, cudaStream_t s);
 
 // S0 on the tensor cores: logits [M,E] = bf16(x . w_router^T + bias), blocks of 128 tokens.
+// One CTA whose bounded wait on an mbarrier nothing completes gives up after
+// about limit_ms ms and records the timeout status (self-test of that path).
+cudaError_t launch_selftest_timeout(int *status, int limit_ms, cudaStream_t s);
 cudaError_t launch_tc_router(const uint16_t *x, const uint16_t *w_router, const float *bias, int M,
                              int E, int H, uint16_t *logits, int *status, cudaStream_t s);
 

@@ -134,6 +134,9 @@ def test_step_argument_checks(lib):
     assert lib.moe_workspace_init(NULL, 1024, S) == INVALID
     assert lib.moe_workspace_init(FAKE_MIS, 1024, S) == INVALID
     assert lib.moe_get_device_status(NULL, S) == INVALID
+    assert lib.moe_selftest_device_timeout(NULL, 1 << 20, 10, S) == INVALID
+    assert lib.moe_selftest_device_timeout(FAKE_MIS, 1 << 20, 10, S) == INVALID
+    assert lib.moe_selftest_device_timeout(FAKE, 16, 10, S) == INVALID   # smaller than the status block
 
 
 def test_product_path_fails_loudly_without_the_library(monkeypatch, tmp_path):

@@ -520,3 +520,26 @@ def test_forward_small_batch_skips_the_sort(cfg, M):
                              renormalize=w.renormalize)
     assert np.array_equal(ids_skip, ref["topk_ids"])
     assert_close_bf16(y_skip, ref["y"], "y")
+
+
+# ----------------------------------------------------------------------------- failure path
+
+def test_device_wait_that_runs_out_reports_a_timeout_and_the_context_stays_usable():
+    """A bounded device wait whose mbarrier nothing completes gives up, records
+    MOE_ERR_DEVICE_TIMEOUT (6) in the workspace status word and returns; the next
+    layer on the same workspace runs normally and matches the oracle."""
+    w = synth.WORKLOADS[1]
+    ws = moe.Workspace(w.Ms[0], w.E, w.top_k, w.H, w.I, w.block_size_m)
+    moe.moe_selftest_device_timeout(ws, limit_ms=100)
+    assert moe.moe_get_device_status(ws) == 6
+    assert moe.moe_get_device_status(ws) == 0       # read clears it
+    M = w.Ms[0]
+    x, w13, w2, lg = layer_case(M, w.E, w.top_k, w.H, w.I, seed=5)
+    y = torch.empty((M, w.H), dtype=torch.bfloat16, device=DEV)
+    ids = torch.empty((M, w.top_k), dtype=torch.int32, device=DEV)
+    moe.moe_forward(x, w13, w2, w.top_k, y, ws, router_logits=lg.to(DEV), block_size_m=w.block_size_m,
+                    topk_ids_out=ids)
+    assert moe.moe_get_device_status(ws) == 0
+    ref = oracle.moe_forward(bits(x), bits(w13), bits(w2), w.top_k, router_logits=bits(lg))
+    assert np.array_equal(ids.cpu().numpy(), ref["topk_ids"])
+    assert_close_bf16(bits(y), ref["y"], "y")

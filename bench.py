@@ -106,23 +106,33 @@ PROFILES = os.path.join(ROOT, "profiles")
 CSRC = os.path.join(ROOT, "mixture_experts_layer_renorm_gb300", "csrc")
 
 
+def code_digest(path):
+    """sha256 of a C/CUDA source with its comments removed and whitespace
+    collapsed: it changes when the code changes, not when a comment does."""
+    text = open(path).read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return hashlib.sha256(" ".join(text.split()).encode()).hexdigest()
+
+
 def profiled_traffic(summary_name, block_size):
     """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
     dominant kernel, from the committed ncu summary `profiles/<summary_name>`,
-    or None when there is none for this block size or when a kernel source it
-    lists has changed since the counters were taken (sha256 per file)."""
+    or None when there is none for this block size or when the code of a
+    kernel source it lists has changed since the counters were taken
+    (code_digest per file)."""
     path = os.path.join(PROFILES, summary_name)
     if not os.path.exists(path):
         return None
     text = open(path).read()
     m = re.search(r"^\s*traffic_bytes_per_launch\s*=\s*(\d+)\s*$", text, re.M)
     b = re.search(r"^\s*block_size_m\s*=\s*(\d+)\s*$", text, re.M)
-    srcs = re.findall(r"^\s*source\s+(\S+)\s+sha256\s*=\s*([0-9a-f]{64})\s*$", text, re.M)
+    srcs = re.findall(r"^\s*source\s+(\S+)\s+code\s+sha256\s*=\s*([0-9a-f]{64})\s*$", text, re.M)
     if m is None or b is None or not srcs or int(b.group(1)) != block_size:
         return None
     for name, digest in srcs:
         f = os.path.join(CSRC, name)
-        if not os.path.exists(f) or hashlib.sha256(open(f, "rb").read()).hexdigest() != digest:
+        if not os.path.exists(f) or code_digest(f) != digest:
             return None
     return int(m.group(1))
 

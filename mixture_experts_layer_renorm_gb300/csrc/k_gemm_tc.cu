@@ -20,15 +20,27 @@
 //   GEMM 2: D_0/1 [128, B] = W2_e[n0 .. n0+255, :] . A_b^T
 //           epilogue: y_acc[t, n] += topk_weight[p] * D (fp32 red.add)
 //
-// Persistent CTAs (one per SM) walk the list of (block, weight tile) tiles.
+// 256-token blocks use one N = 256 MMA per K step on a single 128-row weight
+// tile (GEMM 1: 64 gate rows over the matching 64 up rows, whose results the
+// epilogue warp pairs trade through shared memory; GEMM 2: 128 rows of W2),
+// so that two accumulators still fit TMEM: a chain of N = 128 MMAs into one
+// accumulator leaves the tensor pipe idle between instructions.
+//
+// Persistent CTAs (one per SM) walk the list of (block, weight tile) tiles;
+// GEMM 2 with a large combine accumulator walks it in ranges of weight tiles
+// so the live part of the accumulator stays in L2.  Every launch is a
+// programmatic dependent launch: the CTAs wait (griddepcontrol.wait) only
+// where they read what an earlier kernel wrote -- in a layer, GEMM 2's weights
+// stream before GEMM 1 has finished, and decode GEMM 1 brings the first
+// wave's expert weights into L2 while routing runs.
 // Warp roles (448 threads): warp 0 -- one lane issues the TMA copies of the
 // two 128 x 64 weight tiles (128-byte swizzle); warps 10-13 gather the block's
 // rows with 16-byte cp.async into the same swizzled K-major layout (a TMA
 // instruction costs too much issue time per 512 bytes to gather with it);
 // warp 1 allocates TMEM and one lane issues tcgen05.mma; warps 2-9 are the
 // epilogue, two per TMEM lane quarter splitting its columns (tcgen05.ld
-// 32x32b).  Waiting threads sleep in mbarrier.try_wait rather than spin.  Two accumulator
-// buffers in TMEM (while 4B fp32 columns fit) let the epilogue of one tile
+// 32x32b).  Waiting threads sleep in mbarrier.try_wait rather than spin.  Two
+// accumulator buffers in TMEM let the epilogue of one tile
 // overlap the mainloop of the next.  A ring of shared-memory stages with
 // full/empty mbarriers connects the roles.  Every wait is bounded: after
 // about 2 s the kernel records MOE_ERR_DEVICE_TIMEOUT in the status word,
@@ -362,6 +374,9 @@ __device__ __forceinline__ void pair_bar_sync(int pair) {
 // (decode-sized GEMM 1 with too few tiles for the SMs) each split adds its
 // fp32 partial gate/up sums into h_acc [P, 2I] and the last split of the tile
 // forms a; h_acc and tile_cnt must be zero on entry and tile_cnt is left zero.
+// early_weights: only the row gathers wait for the previous kernel (GEMM 2 in
+// a layer); n_pass: ranges of weight tiles (GEMM 2); w_pf / pf_bytes: weights
+// GEMM 1 brings into L2 before its dependency wait.
 //
 // MODE 0: GEMM 1 + SiLU-and-mul   rows = x[p / top_k], A = W13_e gate | up tiles,
 //                                 a[p, i] = bf16(SiLU(bf16 gate) * bf16 up)

@@ -3,17 +3,21 @@
 
 Default workload: the Qwen3-30B-A3B-shaped decode layer (E=128, top_k=8,
 H=2048, I=768, bf16) at M=64 tokens, seeded synthetic weights and inputs
-already resident in HBM.  A step is one pass of the whole layer (router
-logits, softmax/top-k/renormalize, align, grouped GEMM 1 + SiLU-and-mul,
-grouped GEMM 2 + weighted combine) over one batch, timed with CUDA events on
-the launching stream; the L2 is flushed (a 512 MB write) between steps,
-outside the events, and each step routes a different x.
+already resident in HBM.  A step is one moe_forward call -- the whole layer
+(router logits, softmax/top-k/renormalize, align, grouped GEMM 1 +
+SiLU-and-mul, grouped GEMM 2 + weighted combine) over one batch -- timed with
+CUDA events around the call on the launching stream; the L2 is flushed (a
+512 MB write) between steps, outside the events, and each step routes a
+different x.
 
 Printed (rank 0, one JSON line): tokens/s, the roofline of the dominant
-kernel (grouped GEMM 1, HBM-bound in decode) measured live with CUDA events,
-the end-to-end figure through moe_forward with host buffers (copies inside
-the timed region), the CPU oracle timed on a bounded sample, SM clocks
-sampled during the timed region, and the other decode batch sizes.
+kernel (grouped GEMM 1: HBM-bound in decode, tensor-bound in large prefill),
+its duration taken with CUDA events in a breakdown pass through the step
+entry points right after the timed steps, its DRAM traffic from the committed
+ncu summary while the kernel code is unchanged, the end-to-end figure through
+moe_forward with host buffers (copies inside the timed region), the CPU
+oracle timed on a bounded sample, SM clocks sampled during the timed region,
+the GPU and driver, and the workload's other batch sizes.
 
 `--impl reference` times the CPU oracle instead (the slow reference arm).
 Under torchrun every rank runs its own replica (no collective on the data

@@ -204,7 +204,14 @@ moe_status_t moe_grouped_gemm_w2_combine_noalloc(const moe_bf16_t *a, const moe_
  * y [M, H] bf16 (output); topk_ids_out [M, top_k] int32 and
  * topk_weights_out [M, top_k] fp32 are optional copies of the routing.
  * block_size_m = 0 picks moe_pick_block_size(M, E, top_k, H, I).
- * ws_bytes >= moe_workspace_size(M, E, top_k, H, I, block_size_m). */
+ * ws_bytes >= moe_workspace_size(M, E, top_k, H, I, block_size_m).
+ * The workspace's intermediate lists are internal to this call: for
+ * M * top_k * 4 <= E it gives each pair its own block instead of grouping by
+ * expert (the vLLM blog, "Small batches skip the sort"); y is the same.  The
+ * kernels of the layer are programmatic dependent launches, so a layer may
+ * start while the previous kernel on `stream` is still finishing; it waits
+ * for that kernel before it reads anything the kernel writes (x, residual,
+ * router_logits). */
 moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *w_router,
                          const moe_bf16_t *router_logits, const float *router_bias,
                          const moe_bf16_t *w13, const moe_bf16_t *w2,

@@ -543,3 +543,29 @@ def test_device_wait_that_runs_out_reports_a_timeout_and_the_context_stays_usabl
     ref = oracle.moe_forward(bits(x), bits(w13), bits(w2), w.top_k, router_logits=bits(lg))
     assert np.array_equal(ids.cpu().numpy(), ref["topk_ids"])
     assert_close_bf16(bits(y), ref["y"], "y")
+
+
+def test_forward_back_to_back_on_one_workspace_with_changing_batches():
+    """One workspace (sized for the largest batch) serves layers of different
+    M in a row on one stream, switching between the fused routing launch
+    (M <= 256: completion counters, split-K scratch, small-batch skip) and the
+    separate routing kernels (M > 256); every layer matches the oracle."""
+    w = synth.WORKLOADS[2]
+    wt = synth.layer_weights(w, device=DEV)
+    Ms = (64, 1, 300, 8, 257, 3, 64)
+    ws = moe.Workspace(max(Ms), w.E, w.top_k, w.H, w.I, 16)
+    outs = []
+    for i, M in enumerate(Ms):
+        x = rand_bf16((M, w.H), 1.0, 900 + i)
+        lg = rand_bf16((M, w.E), 1.0, 950 + i)
+        y = torch.empty((M, w.H), dtype=torch.bfloat16, device=DEV)
+        ids = torch.empty((M, w.top_k), dtype=torch.int32, device=DEV)
+        moe.moe_forward(x, wt["w13"], wt["w2"], w.top_k, y, ws, router_logits=lg, block_size_m=16,
+                        topk_ids_out=ids)
+        outs.append((x, lg, y, ids))
+    assert moe.moe_get_device_status(ws) == 0
+    for x, lg, y, ids in outs:
+        ref = oracle.moe_forward(bits(x), bits(wt["w13"]), bits(wt["w2"]), w.top_k,
+                                 router_logits=bits(lg))
+        assert np.array_equal(ids.cpu().numpy(), ref["topk_ids"])
+        assert_close_bf16(bits(y), ref["y"], "y")

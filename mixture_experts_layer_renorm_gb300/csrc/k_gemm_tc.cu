@@ -26,20 +26,29 @@
 // so that two accumulators still fit TMEM: a chain of N = 128 MMAs into one
 // accumulator leaves the tensor pipe idle between instructions.
 //
-// Persistent CTAs (one per SM) walk the list of (block, weight tile) tiles;
+// 2-SM tiles: where the weight tiles of a 256-token GEMM come in an even
+// number, CTAs run in clusters of two on neighbouring weight tiles of the same
+// block and the even CTA issues M = 256 MMAs (tcgen05 cta_group::2) over both
+// CTAs' shared memory.  Each CTA gathers only its half of the block's rows
+// (stages of 32 KB instead of 48, so six fit); the odd CTA's relay warp tells
+// the even CTA's MMA lane when its half of a stage has landed, the MMA
+// completions release both CTAs' stages (multicast commits), and each CTA's
+// epilogue writes its own 128 rows from its own tensor memory.
+//
+// Persistent CTAs (one per SM, or pairs) walk the list of (block, weight tile) tiles;
 // GEMM 2 with a large combine accumulator walks it in ranges of weight tiles
 // so the live part of the accumulator stays in L2.  Every launch is a
 // programmatic dependent launch: the CTAs wait (griddepcontrol.wait) only
 // where they read what an earlier kernel wrote -- in a layer, GEMM 2's weights
 // stream before GEMM 1 has finished, and decode GEMM 1 brings the first
 // wave's expert weights into L2 while routing runs.
-// Warp roles (448 threads): warp 0 -- one lane issues the TMA copies of the
+// Warp roles (480 threads): warp 0 -- one lane issues the TMA copies of the
 // two 128 x 64 weight tiles (128-byte swizzle); warps 10-13 gather the block's
 // rows with 16-byte cp.async into the same swizzled K-major layout (a TMA
 // instruction costs too much issue time per 512 bytes to gather with it);
 // warp 1 allocates TMEM and one lane issues tcgen05.mma; warps 2-9 are the
 // epilogue, two per TMEM lane quarter splitting its columns (tcgen05.ld
-// 32x32b).  Waiting threads sleep in mbarrier.try_wait rather than spin.  Two
+// 32x32b); warp 14 relays stage completion in 2-SM tiles.  Waiting threads sleep in mbarrier.try_wait rather than spin.  Two
 // accumulator buffers in TMEM let the epilogue of one tile
 // overlap the mainloop of the next.  A ring of shared-memory stages with
 // full/empty mbarriers connects the roles.  Every wait is bounded: after
@@ -60,8 +69,13 @@ namespace {
 constexpr int kEpiWarps = 8;                         // warps 2..9: two per TMEM lane quarter
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kGatherWarp0 = 2 + kEpiWarps;          // warps 10..13 gather the block's rows
-constexpr int kGatherThreads = 128;
-constexpr int kTcThreads = 64 + kEpiThreads + kGatherThreads;
+constexpr int kGatherWarps = 4;
+constexpr int kGatherThreads = kGatherWarps * 32;
+constexpr int kRelayWarp = kGatherWarp0 + kGatherWarps;  // warp 14: 2-SM tiles, second CTA
+constexpr int kTcThreads = 64 + kEpiThreads + kGatherThreads + 32;
+// 2-SM tiles: accumulator buffers per CTA
+constexpr int kPairAccBufs = 2;
+constexpr bool kPairTiles = true;  // 256-token tiles run as 2-SM tiles where they can
 constexpr int kBK = 64;                              // K per stage: one 128-byte swizzle row
 constexpr int kTileM = 128;                          // weight rows per MMA
 constexpr uint32_t kATileBytes = kTileM * kBK * 2;   // 16 KB
@@ -223,6 +237,70 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
       : "memory");
 }
 
+// The same for a pair of CTAs (cta_group::2): an M = 256 MMA whose A rows
+// 0-127 and B rows 0..N/2-1 come from the even CTA's shared memory and A rows
+// 128-255 and B rows N/2..N-1 from the odd CTA's, at the same offsets; each
+// CTA's tensor memory receives its 128 rows of D.  Issued by the even CTA.
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrives once on the barrier at this offset in both CTAs of the pair when
+// every pair MMA this thread issued has completed.
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
+  const uint16_t both = 3;
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar), "h"(both)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+// ---------------------------------------------------------------- clusters
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA of the cluster.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+// Address in CTA `rank` of the cluster of the shared variable at saddr here.
+__device__ __forceinline__ uint32_t map_to_cta(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+// One arrival on a barrier of another CTA of the cluster (address from
+// map_to_cta).  Relaxed: what an arrival announces here has already completed
+// where the other CTA reads it -- rows landed in this CTA's shared memory
+// (seen through its own barrier, then the proxy fence) or tensor-memory loads
+// waited for -- and this thread wrote nothing the other CTA reads.  A
+// cluster-scope release cost about 0.8 us per arrival, which held the 2-SM
+// mainloop at one stage per 0.8 us.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
@@ -253,7 +331,7 @@ __host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N) {
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-template <int N, int MODE>
+template <int N, int MODE, bool P2 = false>
 struct TcConfig {
   // Wide tiles (N = 256 token columns, GEMMs 1 and 2): ONE 128-row weight tile
   // per stage -- for GEMM 1 its 64 gate rows over the matching 64 up rows -- so
@@ -264,7 +342,9 @@ struct TcConfig {
   static constexpr bool kWide = N == 256 && MODE != 2;
   static constexpr int kATiles = kWide ? 1 : 2;               // 128-row weight tiles per stage
   static constexpr int kRowsPerCTile = kWide && MODE == 0 ? 64 : kATiles * kTileM;  // output rows
-  static constexpr uint32_t kBStageBytes = N * kBK * 2;
+  // 2-SM tiles (P2): each CTA of the pair holds half of the block's rows
+  static constexpr int kBRows = P2 ? N / 2 : N;
+  static constexpr uint32_t kBStageBytes = kBRows * kBK * 2;
   static constexpr uint32_t kStageBytes = kATiles * kATileBytes + kBStageBytes;
   // wide GEMM 1: gate and up of a channel sit in different TMEM lane quarters;
   // each pair of epilogue warps trades half of its bf16 values through a
@@ -279,19 +359,20 @@ struct TcConfig {
   // accumulator buffers in TMEM: two (epilogue of one tile overlaps the
   // mainloop of the next) while both fit the 512 columns
   static constexpr uint32_t kAccCols = kATiles * N;
-  static constexpr int kAccBufs = (2 * kAccCols <= 512) ? 2 : 1;
+  static constexpr int kAccBufs = P2 ? kPairAccBufs : (2 * kAccCols <= 512) ? 2 : 1;
   static constexpr uint32_t kTmemCols = (kAccBufs * kAccCols <= 32) ? 32
                                         : (kAccBufs * kAccCols <= 64) ? 64
                                         : (kAccBufs * kAccCols <= 128) ? 128
                                         : (kAccBufs * kAccCols <= 256) ? 256 : 512;
   // 16-byte chunks of one stage's gathered rows per gather thread
-  static constexpr int kChunksPerThread = N * 8 / kGatherThreads;
+  static constexpr int kChunksPerThread = kBRows * 8 / kGatherThreads;
   // barriers: full[S], empty[S], acc_full[2], acc_empty[2]; tmem address,
   // abort flag; epilogue destination rows[N], weights[N]
   static constexpr uint32_t kCtlBytes = 8 * (2 * kStages + 4) + 16 + 8 * N;
   static constexpr uint32_t kSmemBytes = 1024 + kStages * kStageBytes + kXchgBytes + kCtlBytes;
   static_assert(kStages >= 3, "pipeline needs at least three stages");
-  static_assert(N * 8 % kGatherThreads == 0, "gather threads split a stage evenly");
+  static_assert(kBRows * 8 % kGatherThreads == 0, "gather threads split a stage evenly");
+  static_assert(!P2 || kWide, "2-SM tiles are 256-token tiles");
   static_assert(kAccBufs * kAccCols <= 512, "accumulators fit TMEM");
 };
 
@@ -384,7 +465,7 @@ __device__ __forceinline__ void pair_bar_sync(int pair) {
 //                                 y_acc[p / top_k, n] += topk_w[p] * o
 // MODE 2: router logits           rows = x[t] (blocks of N consecutive tokens),
 //                                 A = W_r rows e0..e0+255, logits[t, e] = bf16(D + bias[e])
-template <int N, int MODE>
+template <int N, int MODE, bool P2>
 __global__ void __launch_bounds__(kTcThreads, 1)
 k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict__ src,
           int src_rows, const int32_t *__restrict__ sorted_ids, const int32_t *__restrict__ expert_ids,
@@ -393,7 +474,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
           float *__restrict__ h_acc, int *__restrict__ tile_cnt, uint16_t *__restrict__ out16,
           float *__restrict__ y_acc, int H_out, int *status, int early_weights, int n_pass,
           const uint8_t *__restrict__ w_pf, long pf_bytes) {
-  using Cfg = TcConfig<N, MODE>;
+  using Cfg = TcConfig<N, MODE, P2>;
   constexpr int S = Cfg::kStages;
   // With early_weights (GEMM 2 right after GEMM 1 in one layer) only the row
   // gathers wait for the previous kernel: the weight tiles and the routing
@@ -419,8 +500,17 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
     const int n_post = min(max(*n_post_ptr, 0), cap);
     n_blocks = n_post / B;
   }
-  const int n_tiles = n_blocks * n_ctiles * ksplit;
-  if (static_cast<int>(blockIdx.x) >= n_tiles) {
+  // 2-SM tiles (P2, clusters of two): the pair's tile t covers weight tiles
+  // c = 2 c2 (even CTA) and 2 c2 + 1 (odd CTA) of one block; the even CTA
+  // issues M = 256 MMAs over both CTAs' shared memory, each CTA gathers half of
+  // the block's rows and loads its own weight tile, and each CTA's epilogue
+  // writes its own 128 rows.
+  const int rank = P2 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int t0 = P2 ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int tstride = P2 ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  const int n_cunits = P2 ? n_ctiles / 2 : n_ctiles;
+  const int n_tiles = n_blocks * n_cunits * ksplit;
+  if (t0 >= n_tiles) {  // (both CTAs of a pair leave here together)
     // this kernel must not finish before the one it follows has: the next
     // kernels count on that when they reuse what it read
     if (early) griddep_wait();
@@ -448,27 +538,40 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       // the weight lane's expect_tx + one cp.async-completion arrival per gather thread
-      mbar_init(smem_u32(&full[s]), 1 + kGatherThreads);
+      // (2-SM tiles, even CTA: plus the odd CTA's relay arrival)
+      mbar_init(smem_u32(&full[s]), 1 + kGatherThreads + (P2 && rank == 0 ? 1 : 0));
       mbar_init(smem_u32(&empty[s]), 1);      // one tcgen05.commit
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&acc_full[a]), 1);   // one tcgen05.commit
-      mbar_init(smem_u32(&acc_empty[a]), kEpiWarps);  // one arrive per epilogue warp
+      // one arrive per epilogue warp (2-SM tiles, even CTA: of both CTAs)
+      mbar_init(smem_u32(&acc_empty[a]), (P2 && rank == 0 ? 2 : 1) * kEpiWarps);
     }
     *abort = 0;
     *epi_stop = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
-    tmem_relinquish();
+    if constexpr (P2) {
+      tmem_alloc_pair(smem_u32(tmem_slot), Cfg::kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if constexpr (P2) cluster_sync();  // the other CTA's barriers exist before any arrival
   const uint32_t tmem = *tmem_slot;
   const int nk = (K + kBK - 1) / kBK;
-  const TileSched sched = make_sched(n_ctiles, ksplit, nk, n_blocks, MODE == 1 ? n_pass : 1);
+  const TileSched sched = make_sched(n_cunits, ksplit, nk, n_blocks, MODE == 1 ? n_pass : 1);
+  auto coord = [&](int t) {
+    TileCoord tc = tile_coord(t, sched);
+    if (P2) tc.c = 2 * tc.c + rank;
+    return tc;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ weight tiles (TMA)
@@ -478,14 +581,14 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
     if (lane == 0) {
       int g = 0;
       bool stop = false;
-      int t = blockIdx.x;
-      int e_next = MODE == 2 ? 0 : expert_ids[tile_coord(t, sched).b];
-      for (; t < n_tiles && !stop; t += gridDim.x) {
-        const TileCoord tc = tile_coord(t, sched);
+      int t = t0;
+      int e_next = MODE == 2 ? 0 : expert_ids[coord(t).b];
+      for (; t < n_tiles && !stop; t += tstride) {
+        const TileCoord tc = coord(t);
         const int c = tc.c;
         const int e = e_next;
-        const int tn = t + static_cast<int>(gridDim.x);
-        if (MODE != 2 && tn < n_tiles) e_next = expert_ids[tile_coord(tn, sched).b];
+        const int tn = t + tstride;
+        if (MODE != 2 && tn < n_tiles) e_next = expert_ids[coord(tn).b];
         // weight rows of the stage's tile(s); wide GEMM 1 loads 64 gate rows
         // and the matching 64 up rows as the two halves of one 128-row tile
         // (the map's box is then 64 rows high)
@@ -515,6 +618,12 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
           if (two) tma_load_3d(a_s + second, &tmap_w, kb * kBK, row1, e, fb);
         }
       }
+      if constexpr (P2) {
+        // the even CTA's MMAs release this CTA's stages with multicast
+        // commits: wait for the last of them before leaving
+        for (int g2 = g; g2 < g + S; ++g2)
+          (void)wait_bounded(smem_u32(&empty[g2 % S]), ((g2 / S) & 1) ^ 1, abort, status);
+      }
       // after an abort: let the copies already issued land before exit
       if (*abort) {
         for (int g2 = (g > S ? g - S : 0); g2 < g; ++g2) {
@@ -522,6 +631,27 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
           while (!mbar_try_wait(smem_u32(&full[g2 % S]), (g2 / S) & 1) &&
                  clock64() - t0 < kWaitLimitCycles) {
           }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == kRelayWarp) {
+    // ------------------------------------------------------------ relay (2-SM tiles, odd CTA)
+    // Once a stage of this CTA (its weight tile and its half of the rows) is
+    // complete, one arrival on the even CTA's full barrier for that stage.
+    if (P2 && rank == 1 && lane == 0) {
+      int g = 0;
+      bool stop = false;
+      for (int t = t0; t < n_tiles && !stop; t += tstride) {
+        const TileCoord tc = coord(t);
+        for (int kb = tc.kb0; kb < tc.kb1; ++kb, ++g) {
+          const int sf = g % S;
+          if (!wait_bounded(smem_u32(&full[sf]), (g / S) & 1, abort, status)) {
+            stop = true;
+            break;
+          }
+          fence_proxy_async_smem();  // the rows were written by cp.async
+          mbar_arrive_cluster(map_to_cta(smem_u32(&full[sf]), 0));
         }
       }
     }
@@ -537,21 +667,23 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
     if (early) griddep_wait();  // the gathered rows are the previous kernel's output
     // Entries of sorted_token_ids (MODE 2: token ids) of this thread's rows in
     // tile t; the next tile's are loaded while this tile's rows are copied.
+    // (2-SM tiles: this CTA's rows are the block's rows rank * N/2 + r)
+    const int rbase = P2 ? rank * Cfg::kBRows : 0;
     auto fetch_ids = [&](int t, int (&ids)[Cfg::kChunksPerThread]) {
-      const int b = tile_coord(t, sched).b;
+      const int b = coord(t).b;
 #pragma unroll
       for (int u = 0; u < Cfg::kChunksPerThread; ++u) {
-        const int r = (gt >> 3) + 16 * u;
+        const int r = rbase + (gt >> 3) + 16 * u;
         if (MODE == 2) ids[u] = b * N + r;
         else ids[u] = r < B ? sorted_ids[(size_t)b * B + r] : -1;
       }
     };
     int ids_next[Cfg::kChunksPerThread];
-    fetch_ids(blockIdx.x, ids_next);
+    fetch_ids(t0, ids_next);
     int g = 0;
     bool stop = false;
-    for (int t = blockIdx.x; t < n_tiles && !stop; t += gridDim.x) {
-      const TileCoord tc = tile_coord(t, sched);
+    for (int t = t0; t < n_tiles && !stop; t += tstride) {
+      const TileCoord tc = coord(t);
       int rowv[Cfg::kChunksPerThread];
 #pragma unroll
       for (int u = 0; u < Cfg::kChunksPerThread; ++u) {
@@ -564,7 +696,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
         }
         rowv[u] = row;
       }
-      const int tn = t + static_cast<int>(gridDim.x);
+      const int tn = t + tstride;
       if (tn < n_tiles) fetch_ids(tn, ids_next);
       for (int kb = tc.kb0; kb < tc.kb1; ++kb, ++g) {
         const int s = g % S;
@@ -588,12 +720,12 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
     cp_async_wait<0>();  // nothing of ours still in flight at exit
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA
-    if (lane == 0) {
-      constexpr uint32_t idesc = umma_idesc_bf16(kTileM, N);
+    if (lane == 0 && (!P2 || rank == 0)) {
+      constexpr uint32_t idesc = umma_idesc_bf16(P2 ? 2 * kTileM : kTileM, N);
       int g = 0, i = 0;
       bool stop = false;
-      for (int t = blockIdx.x; t < n_tiles && !stop; t += gridDim.x) {
-        const TileCoord tc = tile_coord(t, sched);
+      for (int t = t0; t < n_tiles && !stop; t += tstride) {
+        const TileCoord tc = coord(t);
         const bool two = !Cfg::kWide && (MODE == 0 || tc.c * 2 * kTileM + kTileM < a_rows);
         const int acc = i % Cfg::kAccBufs;
         const uint32_t use = i / Cfg::kAccBufs;
@@ -616,12 +748,18 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint32_t accumulate = (kb > tc.kb0 || kk > 0) ? 1u : 0u;
             const uint64_t bd = sw128_kmajor_desc(bt + kk * 32);
-            umma_bf16(d0, sw128_kmajor_desc(a0 + kk * 32), bd, idesc, accumulate);
-            if (two) umma_bf16(d0 + N, sw128_kmajor_desc(a1 + kk * 32), bd, idesc, accumulate);
+            if constexpr (P2) {
+              umma_bf16_pair(d0, sw128_kmajor_desc(a0 + kk * 32), bd, idesc, accumulate);
+            } else {
+              umma_bf16(d0, sw128_kmajor_desc(a0 + kk * 32), bd, idesc, accumulate);
+              if (two) umma_bf16(d0 + N, sw128_kmajor_desc(a1 + kk * 32), bd, idesc, accumulate);
+            }
           }
-          umma_commit(smem_u32(&empty[s]));
+          if constexpr (P2) umma_commit_pair(smem_u32(&empty[s]));
+          else umma_commit(smem_u32(&empty[s]));
         }
-        umma_commit(smem_u32(&acc_full[acc]));
+        if constexpr (P2) umma_commit_pair(smem_u32(&acc_full[acc]));
+        else umma_commit(smem_u32(&acc_full[acc]));
       }
     }
     __syncwarp();
@@ -633,8 +771,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
     const int et = threadIdx.x - 64;   // 0..255 over the epilogue warps
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     int i = 0;
-    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
-      const TileCoord tc = tile_coord(t, sched);
+    for (int t = t0; t < n_tiles; t += tstride) {
+      const TileCoord tc = coord(t);
       const int b = tc.b, c = tc.c;
       // a block whose expert id lies outside [0, E) is computed (on zero
       // weights) but writes nothing
@@ -808,7 +946,11 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
       // this accumulator buffer may be overwritten once all epilogue warps are done with it
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&acc_empty[acc]));
+      if (lane == 0) {
+        // (2-SM tiles: the MMAs are the even CTA's, so is the barrier)
+        if (P2 && rank == 1) mbar_arrive_cluster(map_to_cta(smem_u32(&acc_empty[acc]), 0));
+        else mbar_arrive(smem_u32(&acc_empty[acc]));
+      }
       if (MODE == 0 && ksplit > 1) {
         // The last split of this tile to finish (an atomic count after a fence;
         // nobody waits) reads the summed h back and writes a.
@@ -835,7 +977,12 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) tmem_dealloc(tmem, Cfg::kTmemCols);
+  if constexpr (P2) {
+    cluster_sync();  // neither CTA leaves while the other may still signal it
+    if (warp == 1) tmem_dealloc_pair(tmem, Cfg::kTmemCols);
+  } else {
+    if (warp == 1) tmem_dealloc(tmem, Cfg::kTmemCols);
+  }
 }
 
 // ---------------------------------------------------------------- host side
@@ -928,11 +1075,65 @@ struct TcArgs {
   long pf_bytes = 0;
 };
 
+// Clusters of two CTAs of the 2-SM kernel that can be resident at once (0: none).
+template <int N, int MODE>
+int max_pair_clusters() {
+  static int cached[64];
+  static bool known[64];
+  static std::mutex m;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(m);
+  if (!known[dev]) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_sms() / 2 * 2);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = TcConfig<N, MODE, true>::kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, k_gemm_tc<N, MODE, true>, &cfg) != cudaSuccess) {
+      (void)cudaGetLastError();
+      n = 0;
+    }
+    cached[dev] = n;
+    known[dev] = true;
+  }
+  return cached[dev];
+}
+
 template <int N, int MODE>
 cudaError_t launch_tc_n(const CUtensorMap &map_w, const TcArgs &a, cudaStream_t s) {
   using Cfg = TcConfig<N, MODE>;
-  auto kern = k_gemm_tc<N, MODE>;
-  cudaError_t err = ensure_smem_limit(reinterpret_cast<const void *>(kern), Cfg::kSmemBytes);
+  cudaError_t err;
+  if constexpr (Cfg::kWide) {
+    // 256-token tiles with an even number of weight tiles: 2-SM tiles, as many
+    // pairs of CTAs as can be resident at once
+    if (kPairTiles && a.ksplit == 1 && a.n_ctiles % 2 == 0) {
+      auto kern2 = k_gemm_tc<N, MODE, true>;
+      err = ensure_smem_limit(reinterpret_cast<const void *>(kern2), TcConfig<N, MODE, true>::kSmemBytes);
+      if (err != cudaSuccess) return err;
+      const int units_max = max_pair_clusters<N, MODE>();
+      if (units_max > 0) {
+        const int units =
+            static_cast<int>(std::min<long>(a.max_blocks * (a.n_ctiles / 2), units_max));
+        if (units <= 0) return cudaSuccess;
+        return launch_pdl_cluster(kern2, dim3(2 * units), dim3(kTcThreads),
+                                  TcConfig<N, MODE, true>::kSmemBytes, s, 2, map_w, a.src,
+                                  a.src_rows, a.sorted_ids, a.expert_ids, a.n_post, a.vec, a.P,
+                                  a.top_k, a.E, a.K, a.R_out, a.a_rows, a.B, a.cap, a.n_ctiles,
+                                  a.ksplit, a.h_acc, a.tile_cnt, a.out16, a.y_acc, a.H_out,
+                                  a.status, a.early_weights, a.n_pass, a.w_pf, a.pf_bytes);
+      }
+    }
+  }
+  auto kern = k_gemm_tc<N, MODE, false>;
+  err = ensure_smem_limit(reinterpret_cast<const void *>(kern), Cfg::kSmemBytes);
   if (err != cudaSuccess) return err;
   // persistent: one CTA per SM at most, each walking the tile list with stride gridDim.x
   const int grid = static_cast<int>(

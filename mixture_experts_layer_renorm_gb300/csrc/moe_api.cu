@@ -263,15 +263,17 @@ const char *moe_status_string(moe_status_t st) {
 }
 
 int moe_pick_block_size(int M, int E, int top_k, int H, int I) {
-  (void)H; (void)I;
   if (M <= 0 || E <= 0 || top_k <= 0) return 16;
   const double mean = static_cast<double>(M) * top_k / E;  // mean pairs per expert
   if (mean <= 24) return 16;
   if (mean <= 48) return 32;
   if (mean <= 96) return 64;
   // 256-token tiles (one N = 256 MMA per K step) pay off once their padding is
-  // small next to the groups (prefill, about 1024 pairs per expert and more)
-  if (mean >= 1024) return 256;
+  // small next to the groups: from about 256 pairs per expert when both GEMMs
+  // run them as 2-SM tiles (an even number of weight tiles: ceil(I/64) for
+  // GEMM 1, ceil(H/128) for GEMM 2), else from about 1024
+  const bool pairs = ((I + 63) / 64) % 2 == 0 && ((H + 127) / 128) % 2 == 0;
+  if (mean >= (pairs ? 256 : 1024)) return 256;
   return 128;
 }
 

@@ -473,7 +473,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
           int E, int K, int R_out, int a_rows, int B, int cap, int n_ctiles, int ksplit,
           float *__restrict__ h_acc, int *__restrict__ tile_cnt, uint16_t *__restrict__ out16,
           float *__restrict__ y_acc, int H_out, int *status, int early_weights, int n_pass,
-          const uint8_t *__restrict__ w_pf, long pf_bytes) {
+          const uint8_t *__restrict__ w_pf, long pf_bytes, float4 *__restrict__ zero_dst,
+          long zero_n4) {
   using Cfg = TcConfig<N, MODE, P2>;
   constexpr int S = Cfg::kStages;
   // With early_weights (GEMM 2 right after GEMM 1 in one layer) only the row
@@ -510,10 +511,21 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
   const int tstride = P2 ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
   const int n_cunits = P2 ? n_ctiles / 2 : n_ctiles;
   const int n_tiles = n_blocks * n_cunits * ksplit;
+  // GEMM 1 inside a layer clears the combine accumulator that GEMM 2 adds
+  // into (zero_n4 float4s at zero_dst): each CTA its slice, the epilogue warps
+  // while the first tile's mainloop runs (GEMM 2 reads it only after this
+  // kernel has completed).
+  auto zero_slice = [&](int tid, int nthreads) {
+    const long slice = (zero_n4 + gridDim.x - 1) / gridDim.x;
+    const long begin = static_cast<long>(blockIdx.x) * slice;
+    const long end = min(zero_n4, begin + slice);
+    for (long i = begin + tid; i < end; i += nthreads) zero_dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  };
   if (t0 >= n_tiles) {  // (both CTAs of a pair leave here together)
     // this kernel must not finish before the one it follows has: the next
     // kernels count on that when they reuse what it read
     if (early) griddep_wait();
+    if (MODE == 0 && zero_n4 > 0) zero_slice(threadIdx.x, blockDim.x);
     return;
   }
 
@@ -770,6 +782,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
     const int half = (warp - 2) >> 2;  // the two warps of a quarter split the column chunks
     const int et = threadIdx.x - 64;   // 0..255 over the epilogue warps
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    if (MODE == 0 && zero_n4 > 0) zero_slice(et, kEpiThreads);
     int i = 0;
     for (int t = t0; t < n_tiles; t += tstride) {
       const TileCoord tc = coord(t);
@@ -1073,6 +1086,8 @@ struct TcArgs {
   int n_pass;  // GEMM 2: ranges of weight tiles run one after the other (1: none)
   const uint8_t *w_pf = nullptr;  // GEMM 1: weights to bring into L2 before the dependency wait
   long pf_bytes = 0;
+  float *zero_dst = nullptr;  // GEMM 1: fp32 buffer to clear (zero_n floats, a multiple of 4)
+  long zero_n = 0;
 };
 
 // Clusters of two CTAs of the 2-SM kernel that can be resident at once (0: none).
@@ -1128,7 +1143,8 @@ cudaError_t launch_tc_n(const CUtensorMap &map_w, const TcArgs &a, cudaStream_t 
                                   a.src_rows, a.sorted_ids, a.expert_ids, a.n_post, a.vec, a.P,
                                   a.top_k, a.E, a.K, a.R_out, a.a_rows, a.B, a.cap, a.n_ctiles,
                                   a.ksplit, a.h_acc, a.tile_cnt, a.out16, a.y_acc, a.H_out,
-                                  a.status, a.early_weights, a.n_pass, a.w_pf, a.pf_bytes);
+                                  a.status, a.early_weights, a.n_pass, a.w_pf, a.pf_bytes,
+                                  reinterpret_cast<float4 *>(a.zero_dst), a.zero_n / 4);
       }
     }
   }
@@ -1143,7 +1159,7 @@ cudaError_t launch_tc_n(const CUtensorMap &map_w, const TcArgs &a, cudaStream_t 
                     a.src_rows, a.sorted_ids, a.expert_ids, a.n_post, a.vec, a.P, a.top_k, a.E,
                     a.K, a.R_out, a.a_rows, a.B, a.cap, a.n_ctiles, a.ksplit, a.h_acc, a.tile_cnt,
                     a.out16, a.y_acc, a.H_out, a.status, a.early_weights, a.n_pass, a.w_pf,
-                    a.pf_bytes);
+                    a.pf_bytes, reinterpret_cast<float4 *>(a.zero_dst), a.zero_n / 4);
 }
 
 template <int MODE>
@@ -1166,7 +1182,7 @@ cudaError_t launch_tc_w13_act(const uint16_t *x, const uint16_t *w13, const int3
                               const int32_t *expert_ids, const int32_t *n_post, int P, int top_k,
                               int E, int H, int I, int B, int cap, uint16_t *a, int ksplit,
                               float *h_acc, int *tile_cnt, int *status, int pf_experts,
-                              cudaStream_t s) {
+                              float *zero_dst, long zero_n, cudaStream_t s) {
   // wide tiles (B = 256): 64 gate rows over 64 up rows per weight tile, no K split
   const bool wide = B == 256;
   CUtensorMap map_w;
@@ -1196,6 +1212,8 @@ cudaError_t launch_tc_w13_act(const uint16_t *x, const uint16_t *w13, const int3
   args.out16 = a;
   args.status = status;
   args.max_blocks = cap / B;
+  args.zero_dst = zero_dst;
+  args.zero_n = zero_dst != nullptr ? zero_n : 0;
   if (pf_experts > 0) {
     // the first wave's experts: ceil(SMs / tiles per block) blocks, one expert
     // each at decode sizes, plus one for an expert without pairs among them

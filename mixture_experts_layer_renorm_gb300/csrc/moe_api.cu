@@ -203,7 +203,7 @@ int pick_ksplit(int M, int E, int top_k, int n_ctiles, int nk) {
 moe_status_t run_gemm1(const uint16_t *x, const uint16_t *w13, const int32_t *sorted,
                        const int32_t *eids, const int32_t *npost, int M, int top_k, int E, int H,
                        int I, int B, uint16_t *a, float *h_acc, int *tile_cnt, int *status,
-                       bool prefetch, cudaStream_t s) {
+                       bool prefetch, float *zero_dst, long zero_n, cudaStream_t s) {
   const long P = static_cast<long>(M) * top_k;
   const int cap = static_cast<int>(capacity(P, E, B));
   switch (pick_path(M, E, top_k, B)) {
@@ -213,10 +213,13 @@ moe_status_t run_gemm1(const uint16_t *x, const uint16_t *w13, const int32_t *so
       const int pf_experts = (prefetch && D >= 0.9 * E) ? E : 0;
       return cuda_status(moe::launch_tc_w13_act(x, w13, sorted, eids, npost, static_cast<int>(P),
                                                 top_k, E, H, I, B, cap, a, ks, h_acc, tile_cnt,
-                                                status, pf_experts, s));
+                                                status, pf_experts, zero_dst, zero_n, s));
     }
     case GemmPath::kGemv:
     default:
+      if (zero_dst != nullptr &&
+          cudaMemsetAsync(zero_dst, 0, sizeof(float) * static_cast<size_t>(zero_n), s) != cudaSuccess)
+        return MOE_ERR_CUDA;
       return cuda_status(moe::launch_gemv_w13_act(x, w13, sorted, eids, npost, static_cast<int>(P),
                                                   top_k, E, H, I, B, cap, a, s));
   }
@@ -361,7 +364,8 @@ moe_status_t moe_grouped_gemm_w13_act(const moe_bf16_t *x, const moe_bf16_t *w13
     return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w13)) return MOE_ERR_INVALID_ARG;
   return run_gemm1(x, w13, sorted_token_ids, expert_ids, num_tokens_post_padded, M, top_k, E, H, I,
-                   block_size_m, a, nullptr, nullptr, lib_status(), /*prefetch=*/false, stream);
+                   block_size_m, a, nullptr, nullptr, lib_status(), /*prefetch=*/false,
+                   /*zero_dst=*/nullptr, 0, stream);
 }
 
 moe_status_t moe_grouped_gemm_w2_combine(const moe_bf16_t *a, const moe_bf16_t *w2,
@@ -439,12 +443,12 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *w_router,
   if (st != MOE_OK) return st;
   uint16_t *a = at<uint16_t>(ws, L.a);
   const bool split_ok = zeroed && want_split;  // scratch reserved and cleared
-  // cleared before GEMM 1, so that GEMM 2 directly follows it in the stream
-  if (!zeroed && cudaMemsetAsync(yacc, 0, sizeof(float) * static_cast<size_t>(yn), stream) != cudaSuccess)
-    return MOE_ERR_CUDA;
+  // not cleared by the routing kernel: GEMM 1 clears it on the way (GEMM 2
+  // reads it only after GEMM 1 has completed)
   st = run_gemm1(x, w13, sorted, eids, npost, M, top_k, E, H, I, B, a,
                  split_ok ? at<float>(ws, L.hacc) : nullptr,
-                 split_ok ? at<int>(ws, L.tcnt) : nullptr, status, /*prefetch=*/true, stream);
+                 split_ok ? at<int>(ws, L.tcnt) : nullptr, status, /*prefetch=*/true,
+                 zeroed ? nullptr : yacc, yn, stream);
   if (st != MOE_OK) return st;
   st = run_gemm2(a, w2, sorted, eids, npost, wts, M, top_k, E, H, I, B, yacc, status,
                  /*early_weights=*/true, stream);

@@ -143,7 +143,9 @@ cudaError_t launch_tc_w13_act(const uint16_t *x, const uint16_t *w13, const int3
                               const int32_t *expert_ids, const int32_t *n_post, int P, int top_k,
                               int E, int H, int I, int B, int cap, uint16_t *a, int ksplit,
                               float *h_acc, int *tile_cnt, int *status, int pf_experts,
-                              cudaStream_t s);
+                              float *zero_dst, long zero_n, cudaStream_t s);
+// zero_dst / zero_n: an fp32 buffer (zero_n a multiple of 4, 16-byte aligned)
+// GEMM 1 clears on the way, or null.
 // ksplit > 1 splits each tile's K range across CTAs (GEMM 1: partial sums go
 // through h_acc [P, 2I] fp32 and tile_cnt [cap/B * ceil(I/128)] ints, both zero
 // on entry; GEMM 2 adds its partial sums into y_acc directly).

@@ -130,7 +130,10 @@ moe_status_t moe_align_block_size(const int32_t *topk_ids, int M, int top_k, int
  * Exactly one of w_router [E, H] and router_logits [M, E] is non-NULL
  * (router_bias only with w_router; H is ignored with router_logits).
  * Outputs as for moe_topk_softmax and moe_align_block_size (block_size_m
- * explicit).  ws/ws_bytes: a workspace of at least moe_workspace_size(M, E,
+ * explicit).  router_logits_out [M, E] bf16 or NULL: with w_router, the
+ * logits the routing was decided on are written there (they equal what
+ * moe_router_logits gives up to the order of the fp32 sums); not written
+ * when router_logits is given.  ws/ws_bytes: a workspace of at least moe_workspace_size(M, E,
  * top_k, 16, 16, block_size_m) bytes, initialised once with moe_workspace_init
  * (its control block holds counters that must start at zero; each call leaves
  * them at zero); calls sharing a workspace must not overlap on the GPU. */
@@ -138,8 +141,9 @@ moe_status_t moe_route(const moe_bf16_t *x, const moe_bf16_t *w_router,
                        const moe_bf16_t *router_logits, const float *router_bias, int M, int E,
                        int top_k, int H, int renormalize, int block_size_m, int32_t *topk_ids,
                        float *topk_weights, int32_t *sorted_token_ids, int32_t *expert_ids,
-                       int32_t *expert_offsets, int32_t *num_tokens_post_padded, void *ws,
-                       size_t ws_bytes, cudaStream_t stream);
+                       int32_t *expert_offsets, int32_t *num_tokens_post_padded,
+                       moe_bf16_t *router_logits_out, void *ws, size_t ws_bytes,
+                       cudaStream_t stream);
 
 /* S3. Grouped GEMM 1 with SiLU-and-mul.  [vLLM] "One GEMM 1 program, step by
  * step" and "The rest of the layer stays in pair order": for every real pair
@@ -202,7 +206,9 @@ moe_status_t moe_grouped_gemm_w2_combine_noalloc(const moe_bf16_t *a, const moe_
  * Exactly one of w_router [E, H] and router_logits [M, E] is non-NULL.
  * router_bias [E] fp32 or NULL (only with w_router); residual [M, H] or NULL.
  * y [M, H] bf16 (output); topk_ids_out [M, top_k] int32 and
- * topk_weights_out [M, top_k] fp32 are optional copies of the routing.
+ * topk_weights_out [M, top_k] fp32 are optional copies of the routing;
+ * router_logits_out [M, E] bf16 (optional, with w_router only) receives the
+ * logits the routing was decided on.
  * block_size_m = 0 picks moe_pick_block_size(M, E, top_k, H, I).
  * ws_bytes >= moe_workspace_size(M, E, top_k, H, I, block_size_m).
  * The workspace's intermediate lists are internal to this call: for
@@ -217,8 +223,9 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *w_router,
                          const moe_bf16_t *w13, const moe_bf16_t *w2,
                          const moe_bf16_t *residual, int M, int E, int top_k, int H, int I,
                          int renormalize, int block_size_m, moe_bf16_t *y,
-                         int32_t *topk_ids_out, float *topk_weights_out, void *ws,
-                         size_t ws_bytes, cudaStream_t stream);
+                         int32_t *topk_ids_out, float *topk_weights_out,
+                         moe_bf16_t *router_logits_out, void *ws, size_t ws_bytes,
+                         cudaStream_t stream);
 
 /* Clears the whole workspace (asynchronously on `stream`).  Call it once on a
  * freshly allocated workspace before its first use: the status word at its
@@ -226,7 +233,13 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *w_router,
 moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /* Synchronises `stream`, returns the device status word kept at the start of
- * the workspace (MOE_OK if no kernel reported a problem) and clears it. */
+ * the workspace (MOE_OK if no kernel reported a problem) and clears it.  The
+ * entry points that take no workspace (moe_router_logits,
+ * moe_grouped_gemm_w13_act, moe_grouped_gemm_w2_combine_noalloc) report into
+ * one library-wide word per device instead; it is read (and cleared) here as
+ * well, and on its own when ws is NULL -- the way a caller without a
+ * workspace learns that one of those calls gave up on a bounded wait.  With
+ * ws NULL and no usable CUDA device the result is MOE_ERR_CUDA. */
 moe_status_t moe_get_device_status(void *ws, cudaStream_t stream);
 
 /* Self-test of the device failure path.  Launches one CTA that waits, with

@@ -79,10 +79,10 @@ def load_library(build_if_missing: bool = False):
         "moe_topk_softmax": ([P, I, I, I, I, P, P, P], I),
         "moe_align_block_size": ([P, I, I, I, I, P, P, P, P, P, Z, P], I),
         "moe_grouped_gemm_w13_act": ([P, P, P, P, P, I, I, I, I, I, I, P, P], I),
-        "moe_route": ([P, P, P, P, I, I, I, I, I, I, P, P, P, P, P, P, P, Z, P], I),
+        "moe_route": ([P, P, P, P, I, I, I, I, I, I, P, P, P, P, P, P, P, P, Z, P], I),
         "moe_grouped_gemm_w2_combine": ([P, P, P, P, P, P, P, I, I, I, I, I, I, P, P, Z, P], I),
         "moe_grouped_gemm_w2_combine_noalloc": ([P, P, P, P, P, P, P, I, I, I, I, I, I, P, P], I),
-        "moe_forward": ([P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, P, P, Z, P], I),
+        "moe_forward": ([P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, P, P, P, Z, P], I),
         "moe_workspace_init": ([P, Z, P], I),
         "moe_get_device_status": ([P, P], I),
         "moe_selftest_device_timeout": ([P, Z, I, P], I),
@@ -182,8 +182,10 @@ def moe_selftest_device_timeout(ws, limit_ms: int = 100, stream=None) -> None:
 
 
 def moe_get_device_status(ws, stream=None) -> int:
-    """Synchronises the stream; returns and clears the device status word."""
-    ptr, _ = _ws(ws)
+    """Synchronises the stream; returns and clears the device status word.
+    ws=None reads only the library-wide word of the entry points that take no
+    workspace."""
+    ptr = None if ws is None else _ws(ws)[0]
     return int(load_library().moe_get_device_status(ptr, _stream(stream)))
 
 
@@ -224,13 +226,16 @@ def moe_align_block_size(topk_ids, E: int, block_size_m: int, sorted_token_ids, 
 
 def moe_route(top_k: int, block_size_m: int, topk_ids, topk_weights, sorted_token_ids,
               expert_ids, expert_offsets, num_tokens_post_padded, ws, *, x=None, w_router=None,
-              router_logits=None, router_bias=None, renormalize: bool = True, stream=None) -> None:
-    """Router logits (or the given logits), top-k and align in as few launches as the shape allows."""
+              router_logits=None, router_bias=None, renormalize: bool = True,
+              router_logits_out=None, stream=None) -> None:
+    """Router logits (or the given logits), top-k and align in as few launches as the shape allows.
+    router_logits_out [M, E] bf16 (with w_router) receives the logits the routing used."""
     for t, n in ((x, "x"), (w_router, "w_router"), (router_logits, "router_logits")):
         _check_dtype(t, torch.bfloat16, n)
     _check_dtype(router_bias, torch.float32, "router_bias")
     _check_dtype(topk_ids, torch.int32, "topk_ids")
     _check_dtype(topk_weights, torch.float32, "topk_weights")
+    _check_dtype(router_logits_out, torch.bfloat16, "router_logits_out")
     if w_router is not None:
         M, H = x.shape
         E = w_router.shape[0]
@@ -241,8 +246,8 @@ def moe_route(top_k: int, block_size_m: int, topk_ids, topk_weights, sorted_toke
     _ok(load_library().moe_route(_p(x), _p(w_router), _p(router_logits), _p(router_bias), M, E,
                                  top_k, H, int(bool(renormalize)), block_size_m, _p(topk_ids),
                                  _p(topk_weights), _p(sorted_token_ids), _p(expert_ids),
-                                 _p(expert_offsets), _p(num_tokens_post_padded), ptr, n,
-                                 _stream(stream)), "moe_route")
+                                 _p(expert_offsets), _p(num_tokens_post_padded),
+                                 _p(router_logits_out), ptr, n, _stream(stream)), "moe_route")
 
 
 def moe_grouped_gemm_w13_act(x, w13, sorted_token_ids, expert_ids, num_tokens_post_padded,
@@ -298,9 +303,11 @@ def moe_grouped_gemm_w2_combine_noalloc(a, w2, sorted_token_ids, expert_ids,
 
 def moe_forward(x, w13, w2, top_k: int, y, ws, *, w_router=None, router_logits=None,
                 router_bias=None, residual=None, renormalize: bool = True, block_size_m: int = 0,
-                topk_ids_out=None, topk_weights_out=None, stream=None) -> None:
+                topk_ids_out=None, topk_weights_out=None, router_logits_out=None,
+                stream=None) -> None:
     for t, n in ((x, "x"), (w13, "w13"), (w2, "w2"), (y, "y"), (w_router, "w_router"),
-                 (router_logits, "router_logits"), (residual, "residual")):
+                 (router_logits, "router_logits"), (residual, "residual"),
+                 (router_logits_out, "router_logits_out")):
         _check_dtype(t, torch.bfloat16, n)
     _check_dtype(router_bias, torch.float32, "router_bias")
     _check_dtype(topk_ids_out, torch.int32, "topk_ids_out")
@@ -311,4 +318,5 @@ def moe_forward(x, w13, w2, top_k: int, y, ws, *, w_router=None, router_logits=N
     _ok(load_library().moe_forward(_p(x), _p(w_router), _p(router_logits), _p(router_bias),
                                    _p(w13), _p(w2), _p(residual), M, E, top_k, H, twoI // 2,
                                    int(bool(renormalize)), block_size_m, _p(y), _p(topk_ids_out),
-                                   _p(topk_weights_out), ptr, n, _stream(stream)), "moe_forward")
+                                   _p(topk_weights_out), _p(router_logits_out), ptr, n,
+                                   _stream(stream)), "moe_forward")

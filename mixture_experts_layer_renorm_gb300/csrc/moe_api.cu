@@ -402,8 +402,9 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *w_router,
                          const moe_bf16_t *router_logits, const float *router_bias,
                          const moe_bf16_t *w13, const moe_bf16_t *w2, const moe_bf16_t *residual,
                          int M, int E, int top_k, int H, int I, int renormalize, int block_size_m,
-                         moe_bf16_t *y, int32_t *topk_ids_out, float *topk_weights_out, void *ws,
-                         size_t ws_bytes, cudaStream_t stream) {
+                         moe_bf16_t *y, int32_t *topk_ids_out, float *topk_weights_out,
+                         moe_bf16_t *router_logits_out, void *ws, size_t ws_bytes,
+                         cudaStream_t stream) {
   moe_status_t st = check_shapes(M, E, top_k, H, I);
   if (st != MOE_OK) return st;
   if (block_size_m != 0 && !valid_block_size(block_size_m)) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -436,8 +437,9 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *w_router,
                           pick_ksplit(M, E, top_k, (I + 127) / 128, (H + 63) / 64) > 1;
   const long zn = want_split ? static_cast<long>((L.total - L.yacc) / sizeof(float)) : yn;
   bool zeroed = false;
+  uint16_t *logits_ws = router_logits_out ? router_logits_out : at<uint16_t>(ws, L.logits);
   st = run_route(x, w_router, router_logits, router_bias, M, E, top_k, H, renormalize, B,
-                 at<uint16_t>(ws, L.logits), ids, wts, sorted, eids, offs, npost,
+                 logits_ws, ids, wts, sorted, eids, offs, npost,
                  at<int32_t>(ws, L.hist), status, yacc, zn, &zeroed,
                  /*skip_sort=*/P * 4 <= E, stream);
   if (st != MOE_OK) return st;
@@ -460,8 +462,9 @@ moe_status_t moe_route(const moe_bf16_t *x, const moe_bf16_t *w_router,
                        const moe_bf16_t *router_logits, const float *router_bias, int M, int E,
                        int top_k, int H, int renormalize, int block_size_m, int32_t *topk_ids,
                        float *topk_weights, int32_t *sorted_token_ids, int32_t *expert_ids,
-                       int32_t *expert_offsets, int32_t *num_tokens_post_padded, void *ws,
-                       size_t ws_bytes, cudaStream_t stream) {
+                       int32_t *expert_offsets, int32_t *num_tokens_post_padded,
+                       moe_bf16_t *router_logits_out, void *ws, size_t ws_bytes,
+                       cudaStream_t stream) {
   if (M < 0) return MOE_ERR_INVALID_ARG;
   if (E < 1 || E > kMaxExperts || top_k < 1 || top_k > std::min(E, kMaxTopK) ||
       !valid_block_size(block_size_m))
@@ -479,8 +482,9 @@ moe_status_t moe_route(const moe_bf16_t *x, const moe_bf16_t *w_router,
   const WsLayout L = ws_layout(M, E, top_k, 16, 16, block_size_m);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   bool zeroed = false;
+  uint16_t *logits_ws = router_logits_out ? router_logits_out : at<uint16_t>(ws, L.logits);
   return run_route(x, w_router, router_logits, router_bias, M, E, top_k, H, renormalize,
-                   block_size_m, at<uint16_t>(ws, L.logits), topk_ids, topk_weights,
+                   block_size_m, logits_ws, topk_ids, topk_weights,
                    sorted_token_ids, expert_ids, expert_offsets, num_tokens_post_padded,
                    at<int32_t>(ws, L.hist), at<int>(ws, 0), nullptr, 0, &zeroed,
                    /*skip_sort=*/false, stream);
@@ -500,10 +504,13 @@ moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream) 
 }
 
 moe_status_t moe_get_device_status(void *ws, cudaStream_t stream) {
-  if (!ws) return MOE_ERR_INVALID_ARG;
+  // ws == NULL: only the library-wide word, which the entry points without a
+  // workspace (moe_router_logits, moe_grouped_gemm_w13_act, the _noalloc
+  // combine) report into
   int host[2] = {0, 0};
   int *lib = lib_status();
-  if (cudaMemcpyAsync(&host[0], ws, sizeof(int), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+  if (!ws && !lib) return MOE_ERR_CUDA;
+  if (ws && cudaMemcpyAsync(&host[0], ws, sizeof(int), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (lib && cudaMemcpyAsync(&host[1], lib, sizeof(int), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
     return MOE_ERR_CUDA;

@@ -89,13 +89,13 @@ def test_forward_argument_checks(lib):
     f = lib.moe_forward
     big = 1 << 40
     args = dict(x=FAKE, wr=FAKE, lg=NULL, bias=NULL, w13=FAKE, w2=FAKE, res=NULL, M=4, E=8, k=2,
-                H=64, I=32, renorm=1, B=16, y=FAKE, ids=NULL, wts=NULL, ws=FAKE, wsb=big)
+                H=64, I=32, renorm=1, B=16, y=FAKE, ids=NULL, wts=NULL, lgo=NULL, ws=FAKE, wsb=big)
 
     def call(**kw):
         a = dict(args, **kw)
         return f(a["x"], a["wr"], a["lg"], a["bias"], a["w13"], a["w2"], a["res"], a["M"], a["E"],
-                 a["k"], a["H"], a["I"], a["renorm"], a["B"], a["y"], a["ids"], a["wts"], a["ws"],
-                 a["wsb"], S)
+                 a["k"], a["H"], a["I"], a["renorm"], a["B"], a["y"], a["ids"], a["wts"], a["lgo"],
+                 a["ws"], a["wsb"], S)
 
     assert call(M=0) == OK                      # M == 0 is a no-op
     assert call(M=-1) == INVALID
@@ -140,7 +140,8 @@ def test_step_argument_checks(lib):
                                            16, FAKE, FAKE, 1 << 30, S) == INVALID
     assert lib.moe_workspace_init(NULL, 1024, S) == INVALID
     assert lib.moe_workspace_init(FAKE_MIS, 1024, S) == INVALID
-    assert lib.moe_get_device_status(NULL, S) == INVALID
+    # no workspace: only the library-wide word, which needs a device to read
+    assert lib.moe_get_device_status(NULL, S) == 4  # MOE_ERR_CUDA
     assert lib.moe_selftest_device_timeout(NULL, 1 << 20, 10, S) == INVALID
     assert lib.moe_selftest_device_timeout(FAKE_MIS, 1 << 20, 10, S) == INVALID
     assert lib.moe_selftest_device_timeout(FAKE, 16, 10, S) == INVALID   # smaller than the status block

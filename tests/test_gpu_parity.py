@@ -1,15 +1,19 @@
 """Parity of every C-ABI entry point against the CPU oracle, on the GPU.
 
 The CUDA path and the oracle get the same seeded inputs (module `synth`);
-nothing the CUDA path produces is fed to the oracle.  Routing outputs must
-match bit for bit; y (and the activation a) within the output tolerance
-(tests/_util.py); router weights within 1e-6.
-
-Where the two sides round a router logit differently (an fp32 sum and an
-fp64 sum can land on either side of a bf16 rounding midpoint), the test
-checks that the GPU logit is the rounding of a value within the fp32
-summation error bound of the exact dot product, and then compares the layer
-outputs only on tokens whose routing agrees.
+nothing the CUDA path produces is fed to the oracle except, where a test says
+so, the router logits the GPU decided on: those are first checked on their
+own (each must be the bf16 rounding of a value within the fp32 summation
+error bound of the exact dot product), then the GPU's routing must equal the
+oracle's top-k of those very logits bit for bit, and the layer output must
+match the oracle run on them -- on every token, at the output tolerance
+(tests/_util.py).  Where the oracle's own logits (fp64 sums) round a value to
+the other side of a bf16 midpoint and that flips a near-tie at the k-th
+logit, the GPU's routing may differ from the oracle's own: every such token
+must have logits that differ between the two sides, and every expert chosen
+by one side only must sit within a few bf16 steps of the k-th largest logit.
+Routing outputs given identical logits match bit for bit; router weights
+within 1e-6.
 """
 import math
 
@@ -248,19 +252,24 @@ def test_grouped_gemm_w2_combine(M, E, k, H, I, B, with_residual, gemm_path):
 
 # ----------------------------------------------------------------------------- the layer
 
-def run_forward(x, w13, w2, k, *, lg=None, wr=None, bias=None, res=None, B=0, renorm=True):
+def run_forward(x, w13, w2, k, *, lg=None, wr=None, bias=None, res=None, B=0, renorm=True,
+                want_logits=False):
     M, H = x.shape
     E, twoI, _ = w13.shape
     y = torch.empty((M, H), dtype=torch.bfloat16, device=DEV)
     ids = torch.empty((M, k), dtype=torch.int32, device=DEV)
     wts = torch.empty((M, k), dtype=torch.float32, device=DEV)
+    lgo = torch.empty((M, E), dtype=torch.bfloat16, device=DEV) if wr is not None else None
     ws = moe.Workspace(M, E, k, H, twoI // 2, B)
     moe.moe_forward(x, w13, w2, k, y, ws, w_router=wr, router_logits=lg, router_bias=bias,
                     residual=res, renormalize=renorm, block_size_m=B, topk_ids_out=ids,
-                    topk_weights_out=wts)
+                    topk_weights_out=wts, router_logits_out=lgo)
     torch.cuda.synchronize()
     assert moe.moe_get_device_status(ws) == 0
-    return bits(y), ids.cpu().numpy(), wts.cpu().numpy()
+    out = (bits(y), ids.cpu().numpy(), wts.cpu().numpy())
+    if want_logits:
+        out = out + (None if lgo is None else bits(lgo),)
+    return out
 
 
 @pytest.mark.parametrize("M,E,k,H,I,B", [(3, 4, 2, 128, 64, 16), (1, 60, 4, 2048, 1408, 0),
@@ -276,20 +285,46 @@ def test_forward_given_logits(M, E, k, H, I, B, renorm):
     assert_close_bf16(yb, ref["y"], "y")
 
 
-def compare_routed_layer(yb, ids, ref, x, wr, bias):
-    """y compared on tokens whose routing agrees; disagreeing tokens must have a
-    logit that the two sides round differently."""
-    agree = (ids == ref["topk_ids"]).all(axis=1)
-    if not agree.all():
-        lg = torch.empty((x.shape[0], wr.shape[0]), dtype=torch.bfloat16, device=DEV)
-        moe.moe_router_logits(x, wr, lg, router_bias=bias)
-        torch.cuda.synchronize()
-        lgb = bits(lg)
-        check_logits(lgb, x, wr, bias)
-        for t in np.nonzero(~agree)[0]:
-            assert (lgb[t] != ref["logits"][t]).any(), f"token {t}: routing differs, logits equal"
-        assert (~agree).sum() <= max(1, 0.02 * len(agree))
-    assert_close_bf16(yb[agree], ref["y"][agree], "y")
+def ordered_bf16(bits_):
+    """bf16 bit patterns -> integers in the order of the values (+0 and -0 equal)."""
+    b = np.asarray(bits_, dtype=np.int64)
+    return np.where(b & 0x8000, -(b & 0x7FFF), b)
+
+
+def assert_routing_explained(g_lg, g_ids, o_lg, o_ids, k, what="routing", max_steps=8):
+    """g_ids must be the oracle's top-k of the GPU logits g_lg (bit for bit); a
+    token routed differently by the oracle from its own logits o_lg must have
+    logits that differ, and every expert chosen by one side only must lie
+    within max_steps bf16 steps of the oracle's k-th largest logit (a near-tie
+    that the two roundings decide differently).  Returns the number of such
+    tokens."""
+    want_ids, _ = oracle.topk_softmax(g_lg, k)
+    assert np.array_equal(g_ids, want_ids), f"{what}: GPU ids are not the top-k of its own logits"
+    differ = ~(g_ids == o_ids).all(axis=1)
+    for t in np.nonzero(differ)[0]:
+        assert (g_lg[t] != o_lg[t]).any(), f"{what}: token {t} routed differently on equal logits"
+        kth = ordered_bf16(o_lg[t][o_ids[t][-1]])
+        odd = np.setxor1d(o_ids[t], g_ids[t])
+        assert (np.abs(ordered_bf16(o_lg[t][odd]) - kth) <= max_steps).all(), \
+            f"{what}: token {t} routed differently away from a near-tie"
+    return int(differ.sum())
+
+
+def compare_routed_layer(yb, ids, g_lg, x, wr, bias, w13, w2, k, res=None, renorm=True):
+    """A layer routed by router weights: the GPU logits within the fp32 bound,
+    the GPU's routing the top-k of its logits, any difference from the
+    oracle's own routing a near-tie, and y equal to the oracle's layer on the
+    GPU logits for every token."""
+    check_logits(g_lg, x, wr, bias)
+    xb = bits(x)
+    o_lg = oracle.router_logits(xb, bits(wr), None if bias is None else bias.cpu().numpy())
+    o_ids, _ = oracle.topk_softmax(o_lg, k, renormalize=renorm)
+    n = assert_routing_explained(g_lg, ids, o_lg, o_ids, k)
+    assert n <= max(1, 0.02 * len(ids)), f"{n} of {len(ids)} tokens routed differently"
+    ref = oracle.moe_forward(xb, bits(w13), bits(w2), k, router_logits=g_lg,
+                             residual=None if res is None else bits(res), renormalize=renorm)
+    assert np.array_equal(ids, ref["topk_ids"])
+    assert_close_bf16(yb, ref["y"], "y")
 
 
 @pytest.mark.parametrize("cfg,M", [(1, 3), (2, 1), (2, 8), (2, 32), (2, 64), (4, 16), (4, 128)])
@@ -299,12 +334,9 @@ def test_forward_with_router_on_workloads(cfg, M):
     inp = synth.layer_input(w, M, device=DEV)
     x = inp["x"]
     res = x if w.residual else None
-    yb, ids, _ = run_forward(x, wt["w13"], wt["w2"], w.top_k, wr=wt["w_router"], res=res,
-                             B=w.block_size_m)
-    ref = oracle.moe_forward(bits(x), bits(wt["w13"]), bits(wt["w2"]), w.top_k,
-                             w_router=bits(wt["w_router"]),
-                             residual=None if res is None else bits(res))
-    compare_routed_layer(yb, ids, ref, x, wt["w_router"], None)
+    yb, ids, _, g_lg = run_forward(x, wt["w13"], wt["w2"], w.top_k, wr=wt["w_router"], res=res,
+                                   B=w.block_size_m, want_logits=True)
+    compare_routed_layer(yb, ids, g_lg, x, wt["w_router"], None, wt["w13"], wt["w2"], w.top_k, res)
 
 
 @pytest.mark.parametrize("cfg,M", [(3, 512), (3, 4096), (3, 16384), (5, 8192), (5, 1)])
@@ -315,21 +347,19 @@ def test_forward_full_size_sampled(cfg, M):
     inp = synth.layer_input(w, M, device=DEV)
     x = inp["x"]
     lg = inp["router_logits"]
-    yb, ids, _ = run_forward(x, wt["w13"], wt["w2"], w.top_k, wr=wt["w_router"], lg=lg,
-                             bias=wt["router_bias"])
+    yb, ids, _, g_lg = run_forward(x, wt["w13"], wt["w2"], w.top_k, wr=wt["w_router"], lg=lg,
+                                   bias=wt["router_bias"], want_logits=True)
     g = torch.Generator().manual_seed(M)
     sample = torch.randperm(M, generator=g)[: min(M, 48)].sort().values.numpy()
-    ref = oracle.moe_forward(
-        bits(x)[sample], bits(wt["w13"]), bits(wt["w2"]), w.top_k,
-        w_router=None if wt["w_router"] is None else bits(wt["w_router"]),
-        router_logits=None if lg is None else bits(lg)[sample],
-        router_bias=None if wt["router_bias"] is None else wt["router_bias"].cpu().numpy())
     if wt["w_router"] is None:
+        ref = oracle.moe_forward(bits(x)[sample], bits(wt["w13"]), bits(wt["w2"]), w.top_k,
+                                 router_logits=bits(lg)[sample])
         assert np.array_equal(ids[sample], ref["topk_ids"])
         assert_close_bf16(yb[sample], ref["y"], "y")
     else:
-        compare_routed_layer(yb[sample], ids[sample], ref, x[torch.from_numpy(sample).to(DEV)],
-                             wt["w_router"], wt["router_bias"])
+        compare_routed_layer(yb[sample], ids[sample], g_lg[sample],
+                             x[torch.from_numpy(sample).to(DEV)], wt["w_router"], wt["router_bias"],
+                             wt["w13"], wt["w2"], w.top_k)
     # routing is complete: every token has top_k distinct experts
     assert (np.sort(ids, axis=1)[:, 1:] != np.sort(ids, axis=1)[:, :-1]).all()
 
@@ -338,22 +368,21 @@ def test_forward_full_size_sampled(cfg, M):
 
 def test_stack_chain_against_the_oracle_on_sampled_tokens():
     """The 256-expert, 64-layer decode stack: layer l+1 reads y_l computed with
-    residual x_l.  The GPU runs all M=16 tokens through every layer; the oracle
-    chains 3 sampled tokens through the same layers on its own (each token is
-    independent), copying only the experts it routes to.  Each sampled token
-    must route identically and match y layer by layer until its first routing
-    difference, which must come at a near-tie of the k-th logit.  Such a
-    difference is expected within tens of layers: each layer's y is rounded to
-    bf16 on both sides from differently ordered sums, the residual carries the
-    difference forward, and with 256 experts a near-tie at the k-th logit
-    somewhere along the chain is likely.  So every sampled token must agree on
-    its first layers, and a tenth of the (token, layer) pairs at least are
-    compared."""
+    residual x_l.  The GPU runs all M=16 tokens through every layer.  Two
+    checks per layer on 5 sampled tokens:
 
-    def ordered(bits_):
-        b = np.asarray(bits_, dtype=np.int64)
-        return np.where(b & 0x8000, -(b & 0x7FFF), b)
+    same input (the parity check): the oracle gets the very x_l the GPU layer
+    received and the router logits the GPU decided on.  At every depth the
+    GPU logits must lie within the fp32 bound, the GPU routing must be the
+    top-k of them, any difference from the oracle's own routing of x_l must
+    be a near-tie, and y_l must match at the unscaled output tolerance.
 
+    chained drift (an extra): the oracle also chains the sampled tokens
+    through the layers on its own.  Each layer's y is rounded to bf16 on both
+    sides from differently ordered sums and the residual carries the
+    difference forward, so the chains drift apart like a random walk; they
+    are compared while their routing agrees, with a tolerance growing as
+    sqrt(1 + l/4), and the first routing difference must be a near-tie."""
     w = synth.WORKLOADS[4]
     M, sample = 16, [0, 3, 7, 10, 13]
     x0 = synth.layer_input(w, M, device=DEV)["x"]
@@ -368,20 +397,34 @@ def test_stack_chain_against_the_oracle_on_sampled_tokens():
         y = torch.empty_like(cur)
         ids = torch.empty((M, w.top_k), dtype=torch.int32, device=DEV)
         lg = torch.empty((M, w.E), dtype=torch.bfloat16, device=DEV)
-        moe.moe_router_logits(cur, wt["w_router"], lg)
         moe.moe_forward(cur, wt["w13"], wt["w2"], w.top_k, y, ws, w_router=wt["w_router"],
-                        residual=cur, topk_ids_out=ids)
+                        residual=cur, topk_ids_out=ids, router_logits_out=lg)
         torch.cuda.synchronize()
+        gx = bits(cur)[sample]
         g_y, g_ids, g_lg = bits(y)[sample], ids.cpu().numpy()[sample], bits(lg)[sample]
+        wr_b = bits(wt["w_router"])
         # the oracle's own chain for the sampled tokens
-        o_lg = oracle.router_logits(ox, bits(wt["w_router"]))
+        o_lg = oracle.router_logits(ox, wr_b)
         o_ids, o_w = oracle.topk_softmax(o_lg, w.top_k)
-        used = np.unique(o_ids)
+        # copy only the experts either check routes to
+        used = np.unique(np.concatenate([o_ids.ravel(), g_ids.ravel()]))
         idx = torch.from_numpy(used.astype(np.int64)).to(DEV)
         w13 = np.zeros((w.E, 2 * w.I, w.H), np.uint16)
         w2 = np.zeros((w.E, w.H, w.I), np.uint16)
         w13[used] = bits(wt["w13"].index_select(0, idx))
         w2[used] = bits(wt["w2"].index_select(0, idx))
+
+        # same input: x_l as the GPU layer received it, the GPU's logits
+        sub = torch.from_numpy(np.array(sample)).to(DEV)
+        check_logits(g_lg, cur.index_select(0, sub), wt["w_router"], None)
+        s_lg = oracle.router_logits(gx, wr_b)
+        s_ids, _ = oracle.topk_softmax(s_lg, w.top_k)
+        assert_routing_explained(g_lg, g_ids, s_lg, s_ids, w.top_k, f"layer {l}")
+        ref = oracle.moe_forward(gx, w13, w2, w.top_k, router_logits=g_lg, residual=gx)
+        assert np.array_equal(g_ids, ref["topk_ids"])
+        assert_close_bf16(g_y, ref["y"], f"y layer {l} (same input)")
+
+        # chained drift
         a = oracle.expert_act(ox, w13, o_ids)
         oy = oracle.expert_down_combine(a, w2, o_ids, o_w, residual=ox)
         for s_i in range(len(sample)):
@@ -391,16 +434,13 @@ def test_stack_chain_against_the_oracle_on_sampled_tokens():
                 # a near-tie: every expert chosen by one side only sits within a few
                 # bf16 steps of the oracle's k-th largest logit
                 assert (o_lg[s_i] != g_lg[s_i]).any(), f"layer {l}: routing differs, logits equal"
-                kth = ordered(o_lg[s_i][o_ids[s_i][-1]])
+                kth = ordered_bf16(o_lg[s_i][o_ids[s_i][-1]])
                 odd = np.setxor1d(o_ids[s_i], g_ids[s_i])
-                assert (np.abs(ordered(o_lg[s_i][odd]) - kth) <= 8).all(), \
+                assert (np.abs(ordered_bf16(o_lg[s_i][odd]) - kth) <= 8).all(), \
                     f"layer {l} token {sample[s_i]}: routing differs away from a near-tie"
                 live[s_i] = False
                 first_diff[s_i] = l
                 continue
-            # each side rounds every layer's y to bf16 from its own input; the
-            # residual carries those differences forward, so they add up like
-            # a random walk: the tolerance grows with sqrt(depth) from layer 0's
             grow = math.sqrt(1.0 + l / 4.0)
             assert_close_bf16(g_y[s_i:s_i + 1], oy[s_i:s_i + 1], f"y layer {l} token {sample[s_i]}",
                               max_rel=Y_MAX_REL * grow, mean_rel=Y_MEAN_REL * grow)
@@ -414,7 +454,7 @@ def test_stack_chain_against_the_oracle_on_sampled_tokens():
 
 # ----------------------------------------------------------------------------- S0 + S1 + S2 together
 
-def run_route(M, E, k, B, *, lg=None, x=None, wr=None, bias=None, ws=None, renorm=True):
+def run_route(M, E, k, B, *, lg=None, x=None, wr=None, bias=None, ws=None, renorm=True, lg_out=None):
     cap = moe.moe_align_capacity(M, k, E, B)
     out = dict(ids=torch.empty((M, k), dtype=torch.int32, device=DEV),
                w=torch.empty((M, k), dtype=torch.float32, device=DEV),
@@ -424,7 +464,8 @@ def run_route(M, E, k, B, *, lg=None, x=None, wr=None, bias=None, ws=None, renor
                n=torch.empty((1,), dtype=torch.int32, device=DEV))
     ws = ws or moe.Workspace(M, E, k, 16, 16, B)
     moe.moe_route(k, B, out["ids"], out["w"], out["s"], out["e"], out["o"], out["n"], ws, x=x,
-                  w_router=wr, router_logits=lg, router_bias=bias, renormalize=renorm)
+                  w_router=wr, router_logits=lg, router_bias=bias, renormalize=renorm,
+                  router_logits_out=lg_out)
     torch.cuda.synchronize()
     assert moe.moe_get_device_status(ws) == 0
     return {kk: v.cpu().numpy() for kk, v in out.items()}, ws
@@ -454,29 +495,34 @@ def test_route_given_logits_matches_the_steps(M, E, k, B):
 
 @pytest.mark.parametrize("cfg,M", [(2, 1), (2, 64), (4, 128), (3, 512)])
 def test_route_with_router_weights(cfg, M):
+    """Routing from router weights: the logits the routing used (router_logits_out)
+    lie within the fp32 bound of the exact products, the ids and weights are
+    the oracle's top-k of those logits, the lists are the oracle's align of
+    those ids (all bit for bit), and every token the oracle routes differently
+    from its own logits is a near-tie."""
     w = synth.WORKLOADS[cfg]
     wt = synth.layer_weights(w, device=DEV)
     x = synth.layer_input(w, M, device=DEV)["x"]
     B = 16
-    out, _ = run_route(M, w.E, w.top_k, B, x=x, wr=wt["w_router"], bias=wt["router_bias"])
+    g_lg = torch.empty((M, w.E), dtype=torch.bfloat16, device=DEV)
+    out, _ = run_route(M, w.E, w.top_k, B, x=x, wr=wt["w_router"], bias=wt["router_bias"],
+                       lg_out=g_lg)
+    g_lg = bits(g_lg)
+    check_logits(g_lg, x, wt["w_router"], wt["router_bias"])
     bias_np = None if wt["router_bias"] is None else wt["router_bias"].cpu().numpy()
     o_lg = oracle.router_logits(bits(x), bits(wt["w_router"]), bias_np)
-    rid, _ = oracle.topk_softmax(o_lg, w.top_k)
-    agree = (out["ids"] == rid).all(axis=1)
-    assert agree.mean() >= 0.98
-    # whatever the routing, the lists group exactly the routed pairs
-    ids = out["ids"]
-    P = ids.size
-    n = int(out["n"][0])
-    body = out["s"][:n]
-    real = body[body < P]
-    assert np.array_equal(real, np.argsort(ids.reshape(-1), kind="stable"))
-    for b, e in enumerate(out["e"][: n // B]):
-        seg = body[b * B:(b + 1) * B]
-        assert (ids.reshape(-1)[seg[seg < P]] == e).all()
-    if agree.all():
-        rs, re_, ro, rn = oracle.align_block_size(rid, w.E, B)
-        assert n == rn and np.array_equal(body, rs[:n]) and np.array_equal(out["o"], ro)
+    o_ids, _ = oracle.topk_softmax(o_lg, w.top_k)
+    n = assert_routing_explained(g_lg, out["ids"], o_lg, o_ids, w.top_k)
+    assert n <= max(1, 0.02 * M), f"{n} of {M} tokens routed differently"
+    rid, rw = oracle.topk_softmax(g_lg, w.top_k)
+    assert np.array_equal(out["ids"], rid)
+    assert np.abs(out["w"].astype(np.float64) - rw).max() <= W_ABS
+    rs, re_, ro, rn = oracle.align_block_size(rid, w.E, B)
+    nn = int(out["n"][0])
+    assert nn == rn
+    assert np.array_equal(out["s"][:nn], rs[:nn])
+    assert np.array_equal(out["e"][: nn // B], re_[: nn // B])
+    assert np.array_equal(out["o"], ro)
 
 
 # ----------------------------------------------------------------------------- small-batch sort skip

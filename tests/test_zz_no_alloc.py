@@ -5,8 +5,11 @@ device allocations, latency-critical code that may not call cudaMalloc).
 It keeps its fp32 accumulator in an array built into the library instead of
 a caller workspace.  This test calls it through the C ABI twice in a row, on
 different inputs (the second call must not see the first call's sums), and
-compares each result with the workspace entry point moe_grouped_gemm_w2_combine
-within the output tolerance.  The file is named to be collected last.
+compares each result with the oracle's GEMM 2 + combine and with the
+workspace entry point moe_grouped_gemm_w2_combine, within the output
+tolerance.  Without a workspace a caller learns of a device-side problem
+through the library-wide status word (moe_get_device_status(NULL)); it must
+read MOE_OK after every call.  The file is named to be collected last.
 """
 import pytest
 import torch
@@ -37,28 +40,33 @@ def _case(M, E, k, H, I, B, seed, residual):
     w2 = synth.normal_bf16((E, H, I), 0.02, seed + 2, DEV)
     lg = synth.normal_bf16((M, E), 1.0, seed + 3, "cpu")
     ids, w = oracle.topk_softmax(bits(lg), k)
+    a_bits = oracle.expert_act(bits(x), bits(w13), ids)
     s, e, _, n = oracle.align_block_size(ids, E, B)
     s, e = torch.from_numpy(s).to(DEV), torch.from_numpy(e).to(DEV)
     n = torch.tensor([n], dtype=torch.int32, device=DEV)
     wts = torch.from_numpy(w).to(DEV)
-    a = torch.empty((M * k, I), dtype=torch.bfloat16, device=DEV)
-    moe.moe_grouped_gemm_w13_act(x, w13, s, e, n, k, B, a)
+    a = synth.from_bits(a_bits, DEV)    # the oracle's activation as the input
     res = synth.normal_bf16((M, H), 1.0, seed + 4, DEV) if residual else None
-    return a, w2, s, e, n, wts, res
+    ref = oracle.expert_down_combine(a_bits, bits(w2), ids, w, None if res is None else bits(res))
+    return a, w2, s, e, n, wts, res, ref
 
 
 @pytest.mark.parametrize("shape", [(64, 128, 8, 2048, 768, 16), (3, 4, 2, 128, 64, 16)])
-def test_noalloc_matches_workspace_entry_point_on_two_calls(shape):
+def test_noalloc_matches_the_oracle_and_the_workspace_entry_point_on_two_calls(shape):
     M, E, k, H, I, B = shape
+    assert moe.moe_get_device_status(None) == 0
     for call, (seed, residual) in enumerate([(501, False), (907, True)]):
-        a, w2, s, e, n, wts, res = _case(M, E, k, H, I, B, seed + M, residual)
+        a, w2, s, e, n, wts, res, ref = _case(M, E, k, H, I, B, seed + M, residual)
         y_ws = torch.empty((M, H), dtype=torch.bfloat16, device=DEV)
         ws = moe.Workspace(M, E, k, H, I, B)
         moe.moe_grouped_gemm_w2_combine(a, w2, s, e, n, wts, k, B, y_ws, ws, residual=res)
         y_na = torch.full((M, H), float("nan"), dtype=torch.bfloat16, device=DEV)
         moe.moe_grouped_gemm_w2_combine_noalloc(a, w2, s, e, n, wts, k, B, y_na, residual=res)
         torch.cuda.synchronize()
-        assert_close_bf16(bits(y_na), bits(y_ws), f"y (call {call + 1})")
+        assert moe.moe_get_device_status(None) == 0
+        assert moe.moe_get_device_status(ws) == 0
+        assert_close_bf16(bits(y_na), ref, f"y against the oracle (call {call + 1})")
+        assert_close_bf16(bits(y_na), bits(y_ws), f"y against the workspace path (call {call + 1})")
 
 
 def test_noalloc_rejects_sizes_beyond_its_accumulator():

@@ -498,14 +498,15 @@ class Stack:
         self.ids = [torch.empty((M, w.top_k), dtype=torch.int32, device=device)
                     for _ in range(w.layers)]
 
-    def kernels_per_step(self):
+    @staticmethod
+    def kernels_for(w, M):
         """moe_forward per layer: routing (one fused launch up to 256 tokens, else
         router + top-k + align), GEMM 1, GEMM 2 and the output pass."""
-        if self.M <= 256 and self.M * self.w.top_k <= 16384:
+        if M <= 256 and M * w.top_k <= 16384:
             route = 1
         else:
-            route = 2 + (1 if self.M * self.w.top_k <= 16384 else 2)
-        return self.w.layers * (route + 3)
+            route = 2 + (1 if M * w.top_k <= 16384 else 2)
+        return w.layers * (route + 3)
 
     def step(self, moe, x, stream, keep_ids=False):
         """x (held in buf[0]) through every layer; returns the output buffer."""
@@ -569,6 +570,20 @@ def run_stack(moe, args, w, M, device, stream, flush, world):
 
 def ours_stack(args, moe, w, M, device, stream, flush, world, rank, peaks):
     S, step_ms, D, clk = run_stack(moe, args, w, M, device, stream, flush, world)
+    block_size = S.B
+    one_kernel = None
+    if M <= 16 and not args.no_points:
+        # the same step with the one-kernel decode layer (opt-in), for comparison
+        del S
+        os.environ["MOE_DECODE_LAYER"] = "on"
+        try:
+            _, k_ms, _, _ = run_stack(moe, args, w, M, device, stream, flush, world)
+        finally:
+            os.environ.pop("MOE_DECODE_LAYER", None)
+        k_total = max_over_ranks(sum(k_ms), world, device)
+        one_kernel = {"ms_per_step": round(k_total / args.steps, 5),
+                      "tokens_per_s": round(world * M * args.steps / (k_total / 1e3), 2)}
+        S = None
     total_ms = max_over_ranks(sum(step_ms), world, device)
     ms_per_step = total_ms / args.steps
     value = world * M * args.steps / (total_ms / 1e3)
@@ -582,7 +597,7 @@ def ours_stack(args, moe, w, M, device, stream, flush, world, rank, peaks):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic: seeded x ~ N(0,1), 64 layers of weights ~ N(0,0.02), bf16; new x every step",
         "config": {"workload": f"{w.name}_m{M}", "M": M, "E": w.E, "top_k": w.top_k, "H": w.H,
-                   "I": w.I, "layers": w.layers, "block_size_m": S.B, "residual": True,
+                   "I": w.I, "layers": w.layers, "block_size_m": block_size, "residual": True,
                    "cuda_graph": bool(args.graph),
                    "l2": f"flushed between steps ({args.flush_mb} MB write, outside the events)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
@@ -592,8 +607,9 @@ def ours_stack(args, moe, w, M, device, stream, flush, world, rank, peaks):
         "distinct_experts_per_layer": round(statistics.mean(D), 2),
         "gpu": gpu_info(device),
         "e2e": None, "cpu_baseline": None,
-        "gpu_launches": S.kernels_per_step() * args.steps,
+        "gpu_launches": Stack.kernels_for(w, M) * args.steps,
         "clocks": clk.summary(),
+        "one_kernel_layer": one_kernel,
     }
     print(json.dumps(line), flush=True)
 
@@ -678,6 +694,23 @@ def ours(args):
                            "gemm2_ms": round(statistics.mean(p[2] for p in p_per), 5),
                            "distinct_experts": round(statistics.mean(p_D), 2)})
 
+    # the one-kernel decode layer (opt-in) beside the default path, at the
+    # decode sizes it serves
+    one_kernel = []
+    if not args.no_points:
+        for m in sorted(set(w.Ms) | {M}):
+            if m > 16:
+                continue
+            os.environ["MOE_DECODE_LAYER"] = "on"
+            try:
+                _, _, k_ms, _ = run_point(moe, w, m, max(5, args.steps // 2), args.warmup, device,
+                                          stream, flush)
+            finally:
+                os.environ.pop("MOE_DECODE_LAYER", None)
+            ms = statistics.mean(k_ms)
+            one_kernel.append({"M": m, "ms_per_layer": round(ms, 5),
+                               "tokens_per_s": round(m / (ms / 1e3), 1)})
+
     if rank != 0:
         return
     cpu = None if (world > 1 or args.no_cpu_baseline) else cpu_baseline(w, L)
@@ -716,6 +749,7 @@ def ours(args):
         "gpu_launches": kernels * args.steps,
         "clocks": clk.summary(),
         "points": points,
+        "one_kernel_layer": one_kernel,
     }
     print(json.dumps(line), flush=True)
 

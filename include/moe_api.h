@@ -213,7 +213,14 @@ moe_status_t moe_grouped_gemm_w2_combine_noalloc(const moe_bf16_t *a, const moe_
  * ws_bytes >= moe_workspace_size(M, E, top_k, H, I, block_size_m).
  * The workspace's intermediate lists are internal to this call: for
  * M * top_k * 4 <= E it gives each pair its own block instead of grouping by
- * expert (the vLLM blog, "Small batches skip the sort"); y is the same.  The
+ * expert (the vLLM blog, "Small batches skip the sort"); y is the same.
+ * With the environment variable MOE_DECODE_LAYER=on, decode-sized calls
+ * (M * top_k <= 512, I <= 1536, the shapes fitting one CTA's shared memory)
+ * run the whole layer as one persistent cooperative kernel (router, top-k,
+ * grouping, both GEMMs and the combine; the MoE execution analysis page,
+ * "Per-decode-step kernel launches"); same arguments, same results within
+ * the output tolerance.  It is off by default: on this GPU it measured no
+ * faster than the kernel chain.   The
  * kernels of the layer are programmatic dependent launches, so a layer may
  * start while the previous kernel on `stream` is still finishing; it waits
  * for that kernel before it reads anything the kernel writes (x, residual,

@@ -105,6 +105,18 @@ int forced_path() {
   return 0;
 }
 
+// The whole layer as one persistent kernel (k_decode_layer), for decode-sized
+// batches.  Measured against the kernel chain below it does not win on this
+// GPU (a tie at one token, slower from about eight tokens on, where its
+// CUDA-core arithmetic and its three grid barriers outweigh the saved
+// launches), so it runs only when MOE_DECODE_LAYER=on asks for it and the
+// shape fits its shared-memory plan.
+bool use_decode_layer(int M, int E, int top_k, int H, int I) {
+  const char *v = std::getenv("MOE_DECODE_LAYER");
+  if (v == nullptr || std::strcmp(v, "on") != 0) return false;
+  return forced_path() == 0 && moe::decode_layer_supports(M, E, top_k, H, I);
+}
+
 GemmPath pick_path(int M, int E, int top_k, int B) {
   (void)M; (void)E; (void)top_k;
   if (!moe::tc_supports_block(B)) return GemmPath::kGemv;
@@ -425,6 +437,12 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *w_router,
   int *status = at<int>(ws, L.status);
   int32_t *ids = topk_ids_out ? topk_ids_out : at<int32_t>(ws, L.ids);
   float *wts = topk_weights_out ? topk_weights_out : at<float>(ws, L.wts);
+  uint16_t *logits_ws = router_logits_out ? router_logits_out : at<uint16_t>(ws, L.logits);
+  if (use_decode_layer(M, E, top_k, H, I))
+    return cuda_status(moe::launch_decode_layer(
+        x, w_router, router_logits, router_bias, w13, w2, residual, M, E, top_k, H, I,
+        renormalize, y, ids, wts, logits_ws, at<uint16_t>(ws, L.a), at<float>(ws, L.yacc),
+        status + moe::kDecodeCtlOffset, status, stream));
   int32_t *sorted = at<int32_t>(ws, L.sorted);
   int32_t *eids = at<int32_t>(ws, L.eids);
   int32_t *offs = at<int32_t>(ws, L.offsets);
@@ -437,7 +455,6 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *w_router,
                           pick_ksplit(M, E, top_k, (I + 127) / 128, (H + 63) / 64) > 1;
   const long zn = want_split ? static_cast<long>((L.total - L.yacc) / sizeof(float)) : yn;
   bool zeroed = false;
-  uint16_t *logits_ws = router_logits_out ? router_logits_out : at<uint16_t>(ws, L.logits);
   st = run_route(x, w_router, router_logits, router_bias, M, E, top_k, H, renormalize, B,
                  logits_ws, ids, wts, sorted, eids, offs, npost,
                  at<int32_t>(ws, L.hist), status, yacc, zn, &zeroed,

@@ -15,6 +15,7 @@ constexpr int kMaxTopK = 32;
 constexpr int kStatusBytes = 1024;
 constexpr int kCountersOffset = 64;
 constexpr int kRouteFusedMaxGroups = 64;   // token groups (<= 8 tokens each); one more counter for the align
+constexpr int kDecodeCtlOffset = 192;     // the decode-layer kernel's grid-barrier counters (3 ints)
 
 // Programmatic dependent launch.  Every kernel of the library is launched with
 // launch_pdl, so it may become resident while the kernel before it in the
@@ -177,6 +178,20 @@ cudaError_t launch_route_fused(const uint16_t *x, const uint16_t *w_router, cons
                                int32_t *expert_offsets, int32_t *n_post, int *counters,
                                int *status, float *zero_buf, long zero_n, bool skip_sort,
                                cudaStream_t s);
+
+// The whole layer in one persistent kernel (decode-sized batches): router
+// (or the given logits), top-k, grouping, GEMM 1 + SiLU-and-mul, GEMM 2 +
+// combine, y written as bf16.  ctl: 3 ints in the workspace control block,
+// zero between calls.  logits_buf [M, E], a_buf [M * top_k, I] and y_acc
+// [M, H] fp32 are scratch (logits_buf receives the router's logits).
+bool decode_layer_supports(int M, int E, int top_k, int H, int I);
+cudaError_t launch_decode_layer(const uint16_t *x, const uint16_t *w_router,
+                                const uint16_t *logits_in, const float *bias,
+                                const uint16_t *w13, const uint16_t *w2,
+                                const uint16_t *residual, int M, int E, int top_k, int H, int I,
+                                int renormalize, uint16_t *y, int32_t *ids_out, float *wts_out,
+                                uint16_t *logits_buf, uint16_t *a_buf, float *y_acc, int *ctl,
+                                int *status, cudaStream_t s);
 
 int num_sms();
 

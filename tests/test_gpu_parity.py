@@ -615,3 +615,69 @@ def test_forward_back_to_back_on_one_workspace_with_changing_batches():
                                  router_logits=bits(lg))
         assert np.array_equal(ids.cpu().numpy(), ref["topk_ids"])
         assert_close_bf16(bits(y), ref["y"], "y")
+
+
+# ----------------------------------------------------------------------------- one-kernel decode layer
+
+@pytest.mark.parametrize("M,E,k,H,I,mode", [
+    (1, 128, 8, 2048, 768, "router"),      # decode, one token
+    (8, 128, 8, 2048, 768, "router"),
+    (16, 256, 8, 2048, 512, "residual"),   # a stack layer
+    (1, 60, 4, 2048, 1408, "logits"),      # tail: I = 1408 spans two K slices of GEMM 2
+    (3, 4, 2, 128, 64, "router"),          # toy: fewer channels than CTAs
+    (2, 1024, 32, 256, 64, "bias"),        # the largest E and top_k
+    (5, 33, 3, 80, 48, "residual"),        # ragged everything
+    (16, 8, 8, 2304, 96, "logits"),        # every expert chosen by every token; H beyond one K slice
+])
+def test_decode_layer_kernel_matches_the_oracle(M, E, k, H, I, mode, monkeypatch):
+    """moe_forward with the whole layer in one persistent kernel (forced on):
+    routing, both GEMMs and the combine against the oracle, twice in a row on
+    one workspace (its grid-barrier counters must be back at zero)."""
+    monkeypatch.setenv("MOE_DECODE_LAYER", "on")
+    ws = moe.Workspace(M, E, k, H, I, 0)
+    for rep in range(2):
+        x, w13, w2, lg = layer_case(M, E, k, H, I, seed=7 * M + E + H + 100 * rep)
+        wr = rand_bf16((E, H), 0.02, 3 + E + rep) if mode != "logits" else None
+        bias = synth.zipf_router_bias(E, 1.1).to(DEV) if mode == "bias" else None
+        res = rand_bf16((M, H), 1.0, 9 + rep) if mode == "residual" else None
+        y = torch.full((M, H), float("nan"), dtype=torch.bfloat16, device=DEV)
+        ids = torch.empty((M, k), dtype=torch.int32, device=DEV)
+        wts = torch.empty((M, k), dtype=torch.float32, device=DEV)
+        lgo = torch.empty((M, E), dtype=torch.bfloat16, device=DEV) if wr is not None else None
+        moe.moe_forward(x, w13, w2, k, y, ws, w_router=wr,
+                        router_logits=lg.to(DEV) if wr is None else None, router_bias=bias,
+                        residual=res, topk_ids_out=ids, topk_weights_out=wts, router_logits_out=lgo)
+        torch.cuda.synchronize()
+        assert moe.moe_get_device_status(ws) == 0
+        if wr is None:
+            ref = oracle.moe_forward(bits(x), bits(w13), bits(w2), k, router_logits=bits(lg),
+                                     residual=None if res is None else bits(res))
+            assert np.array_equal(ids.cpu().numpy(), ref["topk_ids"])
+            assert np.abs(wts.cpu().numpy().astype(np.float64) - ref["topk_weights"]).max() <= W_ABS
+            assert_close_bf16(bits(y), ref["y"], "y")
+        else:
+            compare_routed_layer(bits(y), ids.cpu().numpy(), bits(lgo), x, wr, bias, w13, w2, k, res)
+            _, rw = oracle.topk_softmax(bits(lgo), k)
+            assert np.abs(wts.cpu().numpy().astype(np.float64) - rw).max() <= W_ABS
+
+
+@pytest.mark.parametrize("cfg,M", [(2, 1), (2, 8), (4, 16), (5, 1)])
+def test_decode_layer_kernel_agrees_with_the_multi_kernel_layer(cfg, M, monkeypatch):
+    """The same layer through the one-kernel path and through the routing +
+    grouped-GEMM kernels, on the same logits: identical routing, y within the
+    output tolerance of each other."""
+    w = synth.WORKLOADS[cfg]
+    wt = synth.layer_weights(w, device=DEV)
+    inp = synth.layer_input(w, M, device=DEV)
+    lg = inp["router_logits"]
+    if lg is None:
+        lg = torch.empty((M, w.E), dtype=torch.bfloat16, device=DEV)
+        moe.moe_router_logits(inp["x"], wt["w_router"], lg, router_bias=wt["router_bias"])
+    res = inp["x"] if w.residual else None
+    outs = {}
+    for path in ("on", "off"):
+        monkeypatch.setenv("MOE_DECODE_LAYER", path)
+        outs[path] = run_forward(inp["x"], wt["w13"], wt["w2"], w.top_k, lg=lg, res=res)
+    assert np.array_equal(outs["on"][1], outs["off"][1])
+    assert np.abs(outs["on"][2] - outs["off"][2]).max() <= W_ABS
+    assert_close_bf16(outs["on"][0], outs["off"][0], "y one kernel vs several")

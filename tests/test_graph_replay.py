@@ -38,8 +38,13 @@ def _built():
 
 # decode M = 1 (small-batch skip of the sort), 8 and 64 (grouped, split K);
 # the 256-expert stack layer with its residual; the 60-expert tail from given logits
-@pytest.mark.parametrize("cfg,M", [(2, 1), (2, 8), (2, 64), (4, 16), (5, 64)])
-def test_forward_replayed_from_a_cuda_graph(cfg, M):
+@pytest.mark.parametrize("cfg,M,one_kernel", [(2, 1, False), (2, 8, False), (2, 64, False),
+                                              (4, 16, False), (5, 64, False),
+                                              # the whole layer as one persistent kernel: its
+                                              # grid-barrier counters must reset for each replay
+                                              (2, 1, True), (2, 8, True), (4, 16, True), (5, 1, True)])
+def test_forward_replayed_from_a_cuda_graph(cfg, M, one_kernel, monkeypatch):
+    monkeypatch.setenv("MOE_DECODE_LAYER", "on" if one_kernel else "off")
     w = synth.WORKLOADS[cfg]
     wt = synth.layer_weights(w, device=DEV)
     x_in = torch.empty((M, w.H), dtype=torch.bfloat16, device=DEV)

@@ -615,6 +615,46 @@ def ours_stack(args, moe, w, M, device, stream, flush, world, rank, peaks):
 
 
 
+def prefill_point(moe, args, device, stream, flush, peaks, world):
+    """The prefill layer (Qwen3-30B-A3B shape, Zipf(1.1) router skew) at
+    M = 16384: tokens/s, the layer's fraction of the bf16 tensor-core peak and
+    the roofline of its dominant kernel, grouped GEMM 1 (tensor-bound there),
+    from the breakdown pass after the timed steps."""
+    w = synth.WORKLOADS[WORKLOAD_CFG["prefill"]]
+    M = max(w.Ms)
+    steps = max(5, args.steps // 2)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(device) as clk:
+        L, per, step_ms, D = run_point(moe, w, M, steps, args.warmup, device, stream, flush)
+    total = max_over_ranks(sum(step_ms), world, device)
+    ms = total / steps
+    gemm1_ms = statistics.mean(p[1] for p in per)
+    g1_tflops = gemm1_flops(w, M) / (gemm1_ms / 1e3) / 1e12
+    lay_tflops = layer_flops(w, M) / (ms / 1e3) / 1e12
+    lay_bytes = statistics.mean(layer_bytes(w, M, d) for d in D)
+    out = {
+        "workload": f"{w.name}_m{M}", "M": M, "block_size_m": L.B,
+        "value": round(world * M / (ms / 1e3), 1), "unit": UNIT, "ms_per_layer": round(ms, 5),
+        "layer_tc_frac": round(lay_tflops / peaks["bf16_tflops"], 4),
+        "layer_hbm_frac": round(lay_bytes / (ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+        "roofline": {"kernel": "grouped GEMM 1 + SiLU-and-mul", "bound": "tensor",
+                     "achieved": round(g1_tflops, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": round(g1_tflops / peaks["bf16_tflops"], 4),
+                     "algorithmic_flops": int(gemm1_flops(w, M)), "ms": round(gemm1_ms, 5),
+                     "traffic": profiled_traffic(f"k_gemm_tc_gemm1_{w.name}_m{M}.md", L.B),
+                     "peak_source": peaks["source"]},
+        "step_breakdown_ms": {k: round(statistics.mean(p[j] for p in per), 5) for j, k in
+                              enumerate(["route", "gemm1_act", "gemm2_combine"])},
+        "distinct_experts": round(statistics.mean(D), 2),
+        "steps": steps, "warmup": args.warmup,
+        "gpu_launches": L.kernels_per_step() * steps,
+        "clocks": clk.summary(),
+    }
+    del L
+    return out
+
+
 def ours(args):
     import mixture_experts_layer_renorm_gb300 as moe
     world, rank, local = dist_env()
@@ -711,6 +751,12 @@ def ours(args):
             one_kernel.append({"M": m, "ms_per_layer": round(ms, 5),
                                "tokens_per_s": round(m / (ms / 1e3), 1)})
 
+    # the prefill half of the metric (% of bf16 tensor-core peak), timed in the
+    # same run: the Zipf-skewed prefill layer at its largest batch
+    prefill = None
+    if args.workload == "decode" and not args.no_prefill:
+        prefill = prefill_point(moe, args, device, stream, flush, peaks, world)
+
     if rank != 0:
         return
     cpu = None if (world > 1 or args.no_cpu_baseline) else cpu_baseline(w, L)
@@ -750,6 +796,7 @@ def ours(args):
         "clocks": clk.summary(),
         "points": points,
         "one_kernel_layer": one_kernel,
+        "prefill": prefill,
     }
     print(json.dumps(line), flush=True)
 
@@ -817,6 +864,8 @@ def main(argv=None):
     ap.add_argument("--flush-mb", type=int, default=512)
     ap.add_argument("--no-points", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="decode workload: skip the prefill point (M = 16384) in the same run")
     ap.add_argument("--ref-tokens", type=int, default=64)
     ap.add_argument("--block-size", type=int, default=0,
                     help="block_size_m of the align and the grouped GEMMs (default: the library's pick)")

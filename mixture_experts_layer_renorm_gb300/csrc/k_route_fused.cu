@@ -158,13 +158,19 @@ k_route_fused(const uint16_t *__restrict__ x, const uint16_t *__restrict__ w_rou
     topk_softmax_warp<VPL, true>(lg + (size_t)t * E, E, top_k, renormalize,
                                  topk_ids + (size_t)t * top_k, topk_w + (size_t)t * top_k, lane);
   }
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) last = atomicAdd(&counters[kRouteFusedMaxGroups], 1) == n_g - 1;
-  __syncthreads();
-  if (!last) return;
-  if (tid == 0) counters[kRouteFusedMaxGroups] = 0;
-  __threadfence();
+  // with one token group this CTA holds every token's ids already (its own
+  // warps wrote them); with several, the last group's CTA goes on
+  if (n_g > 1) {
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) last = atomicAdd(&counters[kRouteFusedMaxGroups], 1) == n_g - 1;
+    __syncthreads();
+    if (!last) return;
+    if (tid == 0) counters[kRouteFusedMaxGroups] = 0;
+    __threadfence();
+  } else {
+    __syncthreads();
+  }
 
   if (skip_sort) {
     // ---- small batch (M * top_k * 4 <= E): no grouping; block p holds pair p

@@ -18,7 +18,10 @@
  * Arithmetic: every sum and product is taken in IEEE double; values are
  * rounded to bfloat16 (round to nearest, ties to even) at the four points the
  * layer stores in bf16: router logits, the GEMM-1 output h, the activation a
- * and the layer output y.  The GEMM-2 output o is not rounded.  Top-k is
+ * and the layer output y.  The pages fix no accumulation precision; a double
+ * sum of products of bf16 values is the exact sum up to 2^-53 relative in any
+ * order, so this oracle does not depend on how a device orders or splits its
+ * sums, and a comparison measures the device's own rounding alone.  The GEMM-2 output o is not rounded.  Top-k is
  * decided on the bf16 logits themselves (softmax is monotone), ties going to
  * the lower expert id.
  *

@@ -54,6 +54,9 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
         return LIB_PATH
     nvcc = _nvcc()
     flags = ARCH_FLAGS + NVCC_FLAGS + list(extra_flags or [])
+    if os.environ.get("MOE_STRICT_CLUSTER_ORDER") == "1":
+        # 2-SM tiles: release semantics on every per-stage hand-off (slower)
+        flags.append("-DMOE_STRICT_CLUSTER_ORDER")
     headers = glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h"))
 
     def compile_one(src):

@@ -58,6 +58,8 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "moe_internal.cuh"
@@ -71,8 +73,9 @@ constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kGatherWarp0 = 2 + kEpiWarps;          // warps 10..13 gather the block's rows
 constexpr int kGatherWarps = 4;
 constexpr int kGatherThreads = kGatherWarps * 32;
-constexpr int kRelayWarp = kGatherWarp0 + kGatherWarps;  // warp 14: 2-SM tiles, second CTA
-constexpr int kTcThreads = 64 + kEpiThreads + kGatherThreads + 32;
+constexpr int kRelayWarp = kGatherWarp0 + kGatherWarps;  // warps 14, 15: 2-SM tiles, second CTA
+constexpr int kRelayWarps = 2;                           // stage g is relayed by warp 14 + g % 2
+constexpr int kTcThreads = 64 + kEpiThreads + kGatherThreads + 32 * kRelayWarps;
 // 2-SM tiles: accumulator buffers per CTA
 constexpr int kPairAccBufs = 2;
 constexpr bool kPairTiles = true;  // 256-token tiles run as 2-SM tiles where they can
@@ -126,16 +129,33 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
   return ok != 0;
 }
 
+// The same wait with cluster-scope acquire semantics: the phase's arrivals
+// from the other CTA of a pair, made with release semantics at cluster scope,
+// happen-before everything this thread does after the wait returns.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "n"(kSuspendHintNs)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for phase `parity` of the barrier; gives up after about 2 s of SM
 // clock (or when another role already gave up), recording the timeout.
+// cluster_acquire: the barrier collects arrivals from the other CTA of a pair.
 __device__ bool wait_bounded_for(uint32_t bar, uint32_t parity, volatile int *abort, int *status,
-                                 long long limit_cycles) {
-  if (mbar_try_wait(bar, parity)) return true;
+                                 long long limit_cycles, bool cluster_acquire = false) {
+  if (cluster_acquire ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 16; ++i)
-      if (mbar_try_wait_sleep(bar, parity)) return true;
+      if (cluster_acquire ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait_sleep(bar, parity))
+        return true;
     if (*abort) return false;
     if (clock64() - t0 > limit_cycles) {
       *abort = 1;
@@ -145,8 +165,8 @@ __device__ bool wait_bounded_for(uint32_t bar, uint32_t parity, volatile int *ab
   }
 }
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort,
-                                             int *status) {
-  return wait_bounded_for(bar, parity, abort, status, kWaitLimitCycles);
+                                             int *status, bool cluster_acquire = false) {
+  return wait_bounded_for(bar, parity, abort, status, kWaitLimitCycles, cluster_acquire);
 }
 
 // The failure path of wait_bounded, on its own: an mbarrier that nothing
@@ -291,14 +311,32 @@ __device__ __forceinline__ uint32_t map_to_cta(uint32_t saddr, uint32_t rank) {
   return r;
 }
 // One arrival on a barrier of another CTA of the cluster (address from
-// map_to_cta).  Relaxed: what an arrival announces here has already completed
-// where the other CTA reads it -- rows landed in this CTA's shared memory
-// (seen through its own barrier, then the proxy fence) or tensor-memory loads
-// waited for -- and this thread wrote nothing the other CTA reads.  A
-// cluster-scope release cost about 0.8 us per arrival, which held the 2-SM
-// mainloop at one stage per 0.8 us.
+// map_to_cta), with release semantics at cluster scope: what this thread has
+// observed before the arrival (tensor-memory loads it waited for) happens-
+// before whatever the other CTA does after its cluster-scope acquire of the
+// phase (every wait of the MMA lane on a barrier the other CTA arrives on).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// The per-stage hand-off of the second CTA's rows to the first CTA's MMA.
+// Its arrival is relaxed unless the library is built with
+// -DMOE_STRICT_CLUSTER_ORDER: a release at cluster scope drains this SM's
+// outstanding memory requests (the row gathers of the following stages among
+// them) and measured 45 % slower GEMM 1 at M = 4096 and 16384 (one arrival per
+// stage).  Without it the ordering rests on the hardware, not on the PTX
+// memory model: the relaying thread has seen the stage's rows land in this
+// CTA's own shared memory (its acquire of this CTA's barrier) and has made
+// them visible to this CTA's tensor-core proxy (fence.proxy.async) before it
+// issues the arrival; the first CTA issues the MMA only after the arrival
+// reaches it, and this CTA's tensor core reads its half of the operands from
+// its own shared memory.
+__device__ __forceinline__ void mbar_arrive_stage_relay(uint32_t bar) {
+#ifdef MOE_STRICT_CLUSTER_ORDER
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+#else
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+#endif
 }
 
 __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
@@ -647,23 +685,27 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
       }
     }
     __syncwarp();
-  } else if (warp == kRelayWarp) {
+  } else if (warp >= kRelayWarp) {
     // ------------------------------------------------------------ relay (2-SM tiles, odd CTA)
     // Once a stage of this CTA (its weight tile and its half of the rows) is
     // complete, one arrival on the even CTA's full barrier for that stage.
+    // Stage g is relayed by warp kRelayWarp + g % kRelayWarps, so that the
+    // arrivals' release of one stage overlaps the wait for the next.
+    const int rw = warp - kRelayWarp;
     if (P2 && rank == 1 && lane == 0) {
       int g = 0;
       bool stop = false;
       for (int t = t0; t < n_tiles && !stop; t += tstride) {
         const TileCoord tc = coord(t);
         for (int kb = tc.kb0; kb < tc.kb1; ++kb, ++g) {
+          if (g % kRelayWarps != rw) continue;
           const int sf = g % S;
           if (!wait_bounded(smem_u32(&full[sf]), (g / S) & 1, abort, status)) {
             stop = true;
             break;
           }
           fence_proxy_async_smem();  // the rows were written by cp.async
-          mbar_arrive_cluster(map_to_cta(smem_u32(&full[sf]), 0));
+          mbar_arrive_stage_relay(map_to_cta(smem_u32(&full[sf]), 0));
         }
       }
     }
@@ -742,12 +784,12 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
         const int acc = i % Cfg::kAccBufs;
         const uint32_t use = i / Cfg::kAccBufs;
         ++i;
-        if (!wait_bounded(smem_u32(&acc_empty[acc]), (use & 1) ^ 1, abort, status)) break;
+        if (!wait_bounded(smem_u32(&acc_empty[acc]), (use & 1) ^ 1, abort, status, P2)) break;
         tc_fence_after();
         const uint32_t d0 = tmem + acc * Cfg::kAccCols;
         for (int kb = tc.kb0; kb < tc.kb1; ++kb, ++g) {
           const int s = g % S;
-          if (!wait_bounded(smem_u32(&full[s]), (g / S) & 1, abort, status)) {
+          if (!wait_bounded(smem_u32(&full[s]), (g / S) & 1, abort, status, P2)) {
             stop = true;
             break;
           }
@@ -1129,7 +1171,10 @@ cudaError_t launch_tc_n(const CUtensorMap &map_w, const TcArgs &a, cudaStream_t 
   if constexpr (Cfg::kWide) {
     // 256-token tiles with an even number of weight tiles: 2-SM tiles, as many
     // pairs of CTAs as can be resident at once
-    if (kPairTiles && a.ksplit == 1 && a.n_ctiles % 2 == 0) {
+    // (MOE_FORCE_PATH=tc1 keeps one CTA per tile, for comparisons)
+    const char *force = std::getenv("MOE_FORCE_PATH");
+    const bool no_pairs = force != nullptr && std::strcmp(force, "tc1") == 0;
+    if (kPairTiles && !no_pairs && a.ksplit == 1 && a.n_ctiles % 2 == 0) {
       auto kern2 = k_gemm_tc<N, MODE, true>;
       err = ensure_smem_limit(reinterpret_cast<const void *>(kern2), TcConfig<N, MODE, true>::kSmemBytes);
       if (err != cudaSuccess) return err;

@@ -93,15 +93,16 @@ moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE
 
 // Which grouped-GEMM implementation runs: the tcgen05 kernels for block sizes
 // they tile (16, 32, 64, 128, 256), the CUDA-core weight-streaming kernels for
-// any other block size.  MOE_FORCE_PATH=gemv|tc overrides the choice (for
-// measurements); "tc" falls back to gemv where the block size is not tiled.
+// any other block size.  MOE_FORCE_PATH=gemv|tc|tc1 overrides the choice (for
+// measurements and tests); "tc" falls back to gemv where the block size is
+// not tiled; "tc1" is "tc" without 2-SM tiles (k_gemm_tc.cu reads it).
 enum class GemmPath { kGemv, kTensorCore };
 
 int forced_path() {
   const char *v = std::getenv("MOE_FORCE_PATH");
   if (v == nullptr) return 0;
   if (std::strcmp(v, "gemv") == 0) return 1;
-  if (std::strcmp(v, "tc") == 0) return 2;
+  if (std::strcmp(v, "tc") == 0 || std::strcmp(v, "tc1") == 0) return 2;
   return 0;
 }
 

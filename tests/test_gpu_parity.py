@@ -681,3 +681,42 @@ def test_decode_layer_kernel_agrees_with_the_multi_kernel_layer(cfg, M, monkeypa
     assert np.array_equal(outs["on"][1], outs["off"][1])
     assert np.abs(outs["on"][2] - outs["off"][2]).max() <= W_ABS
     assert_close_bf16(outs["on"][0], outs["off"][0], "y one kernel vs several")
+
+
+# ----------------------------------------------------------------------------- 2-SM tiles
+
+def test_two_sm_gemm1_is_stable_and_equals_one_cta_tiles(monkeypatch):
+    """Grouped GEMM 1 with 256-token 2-SM tiles (a pair of CTAs, one M = 256
+    MMA over both CTAs' shared memory; the odd CTA hands each stage to the
+    even CTA's MMA with a release arrival that the even CTA acquires): 20 runs
+    at the Zipf prefill shape M = 4096 (no K split, so a is deterministic) must
+    equal, bit for bit, the same GEMM with one CTA per 256-token tile, and
+    match the oracle on a sample of pairs."""
+    w = synth.WORKLOADS[3]
+    M, B = 4096, 256
+    wt = synth.layer_weights(w, device=DEV)
+    x = synth.layer_input(w, M, device=DEV)["x"]
+    out, _ = run_route(M, w.E, w.top_k, B, x=x, wr=wt["w_router"], bias=wt["router_bias"])
+    s = torch.from_numpy(out["s"]).to(DEV)
+    e = torch.from_numpy(out["e"]).to(DEV)
+    n = torch.from_numpy(out["n"]).to(DEV)
+    P = M * w.top_k
+    monkeypatch.setenv("MOE_FORCE_PATH", "tc1")
+    a_one = torch.empty((P, w.I), dtype=torch.bfloat16, device=DEV)
+    moe.moe_grouped_gemm_w13_act(x, wt["w13"], s, e, n, w.top_k, B, a_one)
+    torch.cuda.synchronize()
+    ref_bits = bits(a_one)
+    monkeypatch.setenv("MOE_FORCE_PATH", "tc")
+    a_two = torch.empty_like(a_one)
+    for run in range(20):
+        a_two.fill_(float("nan"))
+        moe.moe_grouped_gemm_w13_act(x, wt["w13"], s, e, n, w.top_k, B, a_two)
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(a_two), ref_bits), f"run {run}: 2-SM tiles differ from one-CTA tiles"
+    assert moe.moe_get_device_status(None) == 0
+    g = torch.Generator().manual_seed(4096)
+    tok = torch.randperm(M, generator=g)[:24].sort().values.numpy()
+    ids = out["ids"][tok]
+    ref = oracle.expert_act(bits(x)[tok], bits(wt["w13"]), ids)
+    pairs = (tok[:, None] * w.top_k + np.arange(w.top_k)[None, :]).reshape(-1)
+    assert_close_bf16(ref_bits[pairs], ref, "a (sampled pairs)")

@@ -82,6 +82,18 @@ def _load():
     lib.oracle_expert_down_combine.restype = None
     lib.oracle_moe_forward.argtypes = [P, P, P, P, P, P, P, i, i, i, i, i, i, P, P, P, P]
     lib.oracle_moe_forward.restype = i
+    lib.oracle_e4m3_round_array.argtypes = [P, ctypes.c_long, P]
+    lib.oracle_e4m3_round_array.restype = None
+    lib.oracle_e4m3_to_double_array.argtypes = [P, ctypes.c_long, P]
+    lib.oracle_e4m3_to_double_array.restype = None
+    lib.oracle_quant_rows.argtypes = [P, i, i, P, P]
+    lib.oracle_quant_rows.restype = None
+    lib.oracle_expert_act_fp8.argtypes = [P, P, P, P, P, i, i, i, i, i, P]
+    lib.oracle_expert_act_fp8.restype = None
+    lib.oracle_expert_down_combine_fp8.argtypes = [P, P, P, P, P, P, P, i, i, i, i, i, P]
+    lib.oracle_expert_down_combine_fp8.restype = None
+    lib.oracle_moe_forward_fp8.argtypes = [P, P, P, P, P, P, P, P, P, i, i, i, i, i, i, P, P, P, P]
+    lib.oracle_moe_forward_fp8.restype = i
     _lib = lib
     return lib
 
@@ -217,4 +229,91 @@ def moe_forward(x, w13, w2, top_k: int, *, w_router=None, router_logits=None,
                                     int(bool(renormalize)), _ptr(y), _ptr(ids), _ptr(w), _ptr(lg))
     if rc != 0:
         raise ValueError("oracle_moe_forward: bad arguments")
+    return {"y": y, "topk_ids": ids, "topk_weights": w, "logits": lg}
+
+
+# ----------------------------------------------------------------------------- FP8 (E4M3)
+
+def e4m3_round(values) -> np.ndarray:
+    """float64 values -> E4M3 codes (uint8): nearest, ties to even, saturating at +-448."""
+    v = np.ascontiguousarray(values, dtype=np.float64)
+    out = np.empty(v.shape, np.uint8)
+    _load().oracle_e4m3_round_array(_ptr(v), v.size, _ptr(out))
+    return out
+
+
+def e4m3_to_f64(codes) -> np.ndarray:
+    """E4M3 codes (uint8) -> float64, exactly."""
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.empty(c.shape, np.float64)
+    _load().oracle_e4m3_to_double_array(_ptr(c), c.size, _ptr(out))
+    return out
+
+
+def quant_rows(src):
+    """Per-row dynamic E4M3 quantization of bf16 bits [R, K]: (codes uint8 [R, K], scales f32 [R])."""
+    src = _c(src, np.uint16)
+    R, K = src.shape
+    q = np.empty((R, K), np.uint8)
+    s = np.empty(R, np.float32)
+    _load().oracle_quant_rows(_ptr(src), R, K, _ptr(q), _ptr(s))
+    return q, s
+
+
+def expert_act_fp8(qx, sx, qw13, sw13, topk_ids):
+    """a [M*k, I] (bf16 bits) from E4M3 x codes/scales and E4M3 W13 codes/row scales."""
+    qx, sx = _c(qx, np.uint8), _c(sx, np.float32)
+    qw13, sw13 = _c(qw13, np.uint8), _c(sw13, np.float32)
+    ids = _c(topk_ids, np.int32)
+    M, H = qx.shape
+    E, twoI, H2 = qw13.shape
+    assert H2 == H and sw13.shape == (E, twoI) and sx.shape == (M,)
+    I = twoI // 2
+    k = ids.shape[1]
+    a = np.empty((M * k, I), np.uint16)
+    _load().oracle_expert_act_fp8(_ptr(qx), _ptr(sx), _ptr(qw13), _ptr(sw13), _ptr(ids), M, k, E,
+                                  H, I, _ptr(a))
+    return a
+
+
+def expert_down_combine_fp8(qa, sa, qw2, sw2, topk_ids, topk_weights, residual=None):
+    """y [M, H] (bf16 bits) from E4M3 activation codes/scales and E4M3 W2 codes/row scales."""
+    qa, sa = _c(qa, np.uint8), _c(sa, np.float32)
+    qw2, sw2 = _c(qw2, np.uint8), _c(sw2, np.float32)
+    ids = _c(topk_ids, np.int32)
+    w = _c(topk_weights, np.float32)
+    residual = _c(residual, np.uint16)
+    M, k = ids.shape
+    E, H, I = qw2.shape
+    assert qa.shape == (M * k, I) and sa.shape == (M * k,) and sw2.shape == (E, H)
+    y = np.empty((M, H), np.uint16)
+    _load().oracle_expert_down_combine_fp8(_ptr(qa), _ptr(sa), _ptr(qw2), _ptr(sw2), _ptr(ids),
+                                           _ptr(w), _ptr(residual), M, k, E, H, I, _ptr(y))
+    return y
+
+
+def moe_forward_fp8(x, qw13, sw13, qw2, sw2, top_k: int, *, w_router=None, router_logits=None,
+                    router_bias=None, residual=None, renormalize: bool = True):
+    """Whole layer with E4M3 expert weights.  Returns dict(y, topk_ids, topk_weights, logits)."""
+    x = _c(x, np.uint16)
+    qw13, sw13 = _c(qw13, np.uint8), _c(sw13, np.float32)
+    qw2, sw2 = _c(qw2, np.uint8), _c(sw2, np.float32)
+    w_router = _c(w_router, np.uint16)
+    router_logits = _c(router_logits, np.uint16)
+    router_bias = _c(router_bias, np.float32)
+    residual = _c(residual, np.uint16)
+    M, H = x.shape
+    E, twoI, _ = qw13.shape
+    I = twoI // 2
+    y = np.empty((M, H), np.uint16)
+    ids = np.empty((M, top_k), np.int32)
+    w = np.empty((M, top_k), np.float32)
+    lg = np.empty((M, E), np.uint16)
+    rc = _load().oracle_moe_forward_fp8(_ptr(x), _ptr(w_router), _ptr(router_logits),
+                                        _ptr(router_bias), _ptr(qw13), _ptr(sw13), _ptr(qw2),
+                                        _ptr(sw2), _ptr(residual), M, E, top_k, H, I,
+                                        int(bool(renormalize)), _ptr(y), _ptr(ids), _ptr(w),
+                                        _ptr(lg))
+    if rc != 0:
+        raise ValueError("oracle_moe_forward_fp8: bad arguments")
     return {"y": y, "topk_ids": ids, "topk_weights": w, "logits": lg}

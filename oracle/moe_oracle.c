@@ -369,3 +369,223 @@ int oracle_moe_forward(const bf16_t *x, const bf16_t *w_router, const bf16_t *ro
     free(logits); free(ids); free(w); free(a);
     return 0;
 }
+
+
+/* ------------------------------------------------------ FP8 (E4M3) path -- */
+
+/* [MoE-vLLM] "fused_experts_impl": for FP8 models the GEMM-1 input is the
+ * quantized copy of x (qhidden_states), and one kernel serves bf16 and FP8
+ * weights.  The page gives no format details; the readings taken here (the
+ * same on the device):
+ *   - FP8 is E4M3 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; no
+ *     infinities; 0x7F / 0xFF are NaN; largest finite 448), converted from a
+ *     value by rounding to nearest, ties to even, saturating at +-448;
+ *   - weights are stored as E4M3 codes with one fp32 scale per output row
+ *     (per output channel): W[e][n][k] ~ s_w[e][n] * q_w[e][n][k];
+ *   - activations are quantized per row (per token for x, per pair for the
+ *     GEMM-1 output a) with a dynamic scale s = amax / 448 (1 for an all-zero
+ *     row) and codes q = e4m3(v / s); amax, the scale and v / s are taken in
+ *     fp32 with correctly rounded division, the precision the device uses,
+ *     so that both sides decide every code the same way;
+ *   - dequantization happens after the sums:
+ *       h[n] = bf16( s_x[t] * s_w[e][n] * sum_k e4m3(q_x[t,k]) e4m3(q_w[e][n,k]) )
+ *       o[n] =       s_a[p] * s_w2[e][n] * sum_i e4m3(q_a[p,i]) e4m3(q_w2[e][n,i])
+ *     with the bf16 rounding points of the bf16 layer (h, a, y).  */
+
+/* Value of an E4M3 code. */
+double oracle_e4m3_to_double(uint8_t c)
+{
+    const int neg = (c >> 7) & 1, ex = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (ex == 15 && m == 7)
+        return NAN;
+    if (ex == 0)
+        v = ldexp((double)m, -9);               /* subnormal: m/8 * 2^-6 */
+    else
+        v = ldexp(8.0 + m, ex - 7 - 3);         /* (1 + m/8) * 2^(ex-7) */
+    return neg ? -v : v;
+}
+
+/* The E4M3 code nearest to v (ties to the even code), saturating at +-448. */
+uint8_t oracle_e4m3_round(double v)
+{
+    if (isnan(v))
+        return 0x7F;
+    const int neg = signbit(v) ? 1 : 0;
+    double a = fabs(v);
+    uint8_t code;
+    if (a >= 448.0) {
+        code = 0x7E;                            /* 448 = 1.75 * 2^8 */
+    } else if (a < ldexp(1.0, -6)) {
+        const double m = nearbyint(ldexp(a, 9)); /* steps of 2^-9 below 2^-6 */
+        code = (uint8_t)m;                      /* m = 8 is 2^-6, the first normal code */
+    } else {
+        int ex;
+        (void)frexp(a, &ex);                    /* a in [2^(ex-1), 2^ex) */
+        const int e = ex - 1;                   /* a in [2^e, 2^(e+1)), -6 <= e <= 8 */
+        double m = nearbyint(ldexp(a, 3 - e));  /* 8 .. 16 in steps of one code */
+        int E = e + 7;
+        if (m >= 16.0) {                        /* rounded up into the next binade */
+            m = 8.0;
+            E += 1;
+        }
+        if (E > 15 || (E == 15 && m > 14.0))    /* above 448 after rounding */
+            code = 0x7E;
+        else
+            code = (uint8_t)((E << 3) | ((int)m - 8));
+    }
+    return (uint8_t)(code | (neg ? 0x80 : 0));
+}
+
+/* Element-wise oracle_e4m3_round / oracle_e4m3_to_double over arrays. */
+void oracle_e4m3_round_array(const double *v, long n, uint8_t *out)
+{
+    for (long i = 0; i < n; ++i)
+        out[i] = oracle_e4m3_round(v[i]);
+}
+
+void oracle_e4m3_to_double_array(const uint8_t *c, long n, double *out)
+{
+    for (long i = 0; i < n; ++i)
+        out[i] = oracle_e4m3_to_double(c[i]);
+}
+
+/* Per-row dynamic E4M3 quantization of a bf16 matrix [R, K]:
+ *   amax = max_k |src[r, k]|;  s[r] = amax / 448 (fp32; 1 if amax == 0)
+ *   q[r, k] = e4m3( float(src[r, k]) / s[r] )   (fp32 division)         */
+void oracle_quant_rows(const bf16_t *src, int R, int K, uint8_t *q, float *s)
+{
+#pragma omp parallel for schedule(static)
+    for (int r = 0; r < R; ++r) {
+        float amax = 0.0f;
+        for (int k = 0; k < K; ++k) {
+            const float v = (float)fabs(bf(src[(size_t)r * K + k]));
+            if (v > amax)
+                amax = v;
+        }
+        const float sc = amax > 0.0f ? amax / 448.0f : 1.0f;
+        s[r] = sc;
+        for (int k = 0; k < K; ++k) {
+            const float v = (float)bf(src[(size_t)r * K + k]) / sc;
+            q[(size_t)r * K + k] = oracle_e4m3_round((double)v);
+        }
+    }
+}
+
+static double f8(uint8_t c) { return oracle_e4m3_to_double(c); }
+
+/* oracle_expert_act on E4M3 operands: for every pair p = t * top_k + j with
+ * e = topk_ids[p]
+ *   h[n] = bf16( s_x[t] * s_w13[e][n] * sum_k q_x[t,k] q_w13[e][n][k] )   n < 2I
+ *   a[p, i] = bf16( SiLU(h[i]) * h[I + i] )
+ * q_x [M, H], s_x [M]; q_w13 [E, 2I, H], s_w13 [E, 2I]; a [M * top_k, I]. */
+void oracle_expert_act_fp8(const uint8_t *qx, const float *sx, const uint8_t *qw13,
+                           const float *sw13, const int32_t *topk_ids, int M, int top_k,
+                           int E, int H, int I, bf16_t *a)
+{
+    (void)E;
+#pragma omp parallel
+    {
+        double *h = (double *)malloc(sizeof(double) * 2 * (size_t)I);
+#pragma omp for schedule(static)
+        for (long p = 0; p < (long)M * top_k; ++p) {
+            const long t = p / top_k;
+            const int e = topk_ids[p];
+            const uint8_t *W = qw13 + (size_t)e * 2 * I * H;
+            for (int n = 0; n < 2 * I; ++n) {
+                double acc = 0.0;
+                for (int k = 0; k < H; ++k)
+                    acc += f8(qx[(size_t)t * H + k]) * f8(W[(size_t)n * H + k]);
+                acc *= (double)sx[t] * (double)sw13[(size_t)e * 2 * I + n];
+                h[n] = bf(oracle_bf16_round(acc));
+            }
+            for (int i = 0; i < I; ++i) {
+                const double g = h[i];
+                const double silu = g / (1.0 + exp(-g));
+                a[(size_t)p * I + i] = oracle_bf16_round(silu * h[I + i]);
+            }
+        }
+        free(h);
+    }
+}
+
+/* oracle_expert_down_combine on E4M3 operands:
+ *   o_p[n] = s_a[p] * s_w2[e][n] * sum_i q_a[p,i] q_w2[e][n][i]     (not rounded)
+ *   y[t, n] = bf16( sum_j topk_weights[t, j] * o_{t*top_k + j}[n] + residual[t, n] )
+ * q_a [M * top_k, I], s_a [M * top_k]; q_w2 [E, H, I], s_w2 [E, H]. */
+void oracle_expert_down_combine_fp8(const uint8_t *qa, const float *sa, const uint8_t *qw2,
+                                    const float *sw2, const int32_t *topk_ids,
+                                    const float *topk_weights, const bf16_t *residual, int M,
+                                    int top_k, int E, int H, int I, bf16_t *y)
+{
+    (void)E;
+#pragma omp parallel for schedule(static)
+    for (int t = 0; t < M; ++t) {
+        for (int n = 0; n < H; ++n) {
+            double acc = 0.0;
+            for (int j = 0; j < top_k; ++j) {
+                const long p = (long)t * top_k + j;
+                const int e = topk_ids[p];
+                const uint8_t *W = qw2 + (size_t)e * H * I + (size_t)n * I;
+                double o = 0.0;
+                for (int i = 0; i < I; ++i)
+                    o += f8(qa[(size_t)p * I + i]) * f8(W[i]);
+                o *= (double)sa[p] * (double)sw2[(size_t)e * H + n];
+                acc += (double)topk_weights[p] * o;
+            }
+            if (residual)
+                acc += bf(residual[(size_t)t * H + n]);
+            y[(size_t)t * H + n] = oracle_bf16_round(acc);
+        }
+    }
+}
+
+/* The layer with E4M3 expert weights: the router stays bf16 (logits, top-k
+ * as in oracle_moe_forward); x is quantized per token, GEMM 1 runs on codes,
+ * its bf16 output a is quantized per pair, GEMM 2 runs on codes, and the
+ * combine is the bf16 layer's.  qx_out / sx_out / qa_out / sa_out (nullable)
+ * receive the intermediate codes and scales.  Returns 0, or -1 on bad
+ * arguments. */
+int oracle_moe_forward_fp8(const bf16_t *x, const bf16_t *w_router, const bf16_t *router_logits,
+                           const float *router_bias, const uint8_t *qw13, const float *sw13,
+                           const uint8_t *qw2, const float *sw2, const bf16_t *residual, int M,
+                           int E, int top_k, int H, int I, int renormalize, bf16_t *y,
+                           int32_t *topk_ids_out, float *topk_weights_out, bf16_t *logits_out)
+{
+    if ((w_router == NULL) == (router_logits == NULL))
+        return -1;
+    if (M < 0 || E < 1 || top_k < 1 || top_k > E || H < 1 || I < 1)
+        return -1;
+    if (M == 0)
+        return 0;
+    const size_t P = (size_t)M * top_k;
+    bf16_t *logits = (bf16_t *)malloc(sizeof(bf16_t) * (size_t)M * E);
+    int32_t *ids = (int32_t *)malloc(sizeof(int32_t) * P);
+    float *w = (float *)malloc(sizeof(float) * P);
+    bf16_t *a = (bf16_t *)malloc(sizeof(bf16_t) * P * I);
+    uint8_t *qx = (uint8_t *)malloc((size_t)M * H);
+    float *sx = (float *)malloc(sizeof(float) * (size_t)M);
+    uint8_t *qa = (uint8_t *)malloc(P * I);
+    float *sa = (float *)malloc(sizeof(float) * P);
+    if (!logits || !ids || !w || !a || !qx || !sx || !qa || !sa) {
+        free(logits); free(ids); free(w); free(a); free(qx); free(sx); free(qa); free(sa);
+        return -1;
+    }
+    if (w_router)
+        oracle_router_logits(x, w_router, router_bias, M, E, H, logits);
+    else
+        memcpy(logits, router_logits, sizeof(bf16_t) * (size_t)M * E);
+    oracle_topk_softmax(logits, M, E, top_k, renormalize, ids, w);
+    oracle_quant_rows(x, M, H, qx, sx);
+    oracle_expert_act_fp8(qx, sx, qw13, sw13, ids, M, top_k, E, H, I, a);
+    oracle_quant_rows(a, (int)P, I, qa, sa);
+    oracle_expert_down_combine_fp8(qa, sa, qw2, sw2, ids, w, residual, M, top_k, E, H, I, y);
+    if (topk_ids_out)
+        memcpy(topk_ids_out, ids, sizeof(int32_t) * P);
+    if (topk_weights_out)
+        memcpy(topk_weights_out, w, sizeof(float) * P);
+    if (logits_out)
+        memcpy(logits_out, logits, sizeof(bf16_t) * (size_t)M * E);
+    free(logits); free(ids); free(w); free(a); free(qx); free(sx); free(qa); free(sa);
+    return 0;
+}

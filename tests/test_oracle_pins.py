@@ -399,3 +399,142 @@ def test_forward_rejects_bad_router_arguments():
     w2 = np.zeros((2, 16, 16), np.uint16)
     with pytest.raises(ValueError):
         oracle.moe_forward(x, w13, w2, 1)  # neither router weights nor logits
+
+
+# ----------------------------------------------------------------------------- FP8 (E4M3)
+#
+# What pins what:
+#   E4M3 decode        every code against torch.float8_e4m3fn; closed forms (448, 2^-6, 2^-9)
+#   E4M3 rounding      torch fp32 -> float8_e4m3fn casts on 200k values within +-448;
+#                      brute-force nearest search (ties to the even code) over every code;
+#                      saturation to +-448 beyond the range
+#   row quantization   closed forms: the largest element maps to 448, an all-zero row to scale 1
+#                      and codes 0, dequantized values within half an E4M3 step of the input
+#   FP8 expert MLP     reduces to the pinned bf16 expert MLP when codes dequantize to bf16
+#                      values and scales are powers of two (both exact)
+
+def _finite_e4m3():
+    codes = np.arange(256, dtype=np.uint8)
+    vals = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    keep = np.isfinite(vals)
+    return codes[keep], vals[keep]
+
+
+def test_e4m3_decode_matches_torch_and_closed_forms():
+    codes = np.arange(256, dtype=np.uint8)
+    mine = oracle.e4m3_to_f64(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(mine), np.isnan(ref))
+    fin = ~np.isnan(ref)
+    assert np.array_equal(mine[fin], ref[fin])
+    assert mine[0x7E] == 448.0 and mine[0x08] == 2.0 ** -6 and mine[0x01] == 2.0 ** -9
+    assert mine[0xFE] == -448.0 and np.isnan(mine[0x7F]) and np.isnan(mine[0xFF])
+
+
+def test_e4m3_round_matches_torch_cast_on_fp32_values():
+    g = np.random.default_rng(7)
+    v = g.standard_normal(200000) * np.exp(g.uniform(-14, 6.5, 200000))
+    v = v[np.abs(v) <= 448].astype(np.float32)
+    mine = oracle.e4m3_round(v.astype(np.float64))
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(mine, ref)
+
+
+def test_e4m3_round_is_nearest_ties_to_even_and_saturates():
+    codes, vals = _finite_e4m3()
+    pos = codes < 0x80                       # the sign-clear codes: +0 .. 448, ascending
+    pc, pv = codes[pos], vals[pos]
+    order = np.argsort(pv, kind="stable")
+    pc, pv = pc[order], pv[order]
+    g = np.random.default_rng(11)
+    mids = (pv[1:] + pv[:-1]) / 2            # every tie between neighbouring codes
+    v = np.concatenate([g.uniform(0, 448, 50000), mids, pv])
+    i = np.clip(np.searchsorted(pv, v, side="left"), 1, len(pv) - 1)
+    lo, hi = pv[i - 1], pv[i]
+    pick_hi = (hi - v < v - lo) | ((hi - v == v - lo) & ((pc[i] & 1) == 0))
+    want = np.where(pick_hi, pc[i], pc[i - 1])
+    want = np.where(v == pv[i - 1], pc[i - 1], want)
+    assert np.array_equal(oracle.e4m3_round(v), want)
+    assert np.array_equal(oracle.e4m3_round(-v), want | 0x80)
+    assert list(oracle.e4m3_round(np.array([448.0, 460.0, 1e6, -1e30]))) == [0x7E, 0x7E, 0x7E, 0xFE]
+
+
+def test_quant_rows_closed_forms_and_error_bound():
+    g = torch.Generator().manual_seed(3)
+    x = (torch.randn(40, 300, generator=g) * torch.logspace(-3, 3, 40)[:, None]).to(torch.bfloat16)
+    xb = x.view(torch.int16).numpy().view(np.uint16)
+    xb[5] = 0                                  # an all-zero row
+    q, s = oracle.quant_rows(xb)
+    xf = x.float().numpy().astype(np.float64)
+    xf[5] = 0
+    amax = np.abs(xf).max(axis=1)
+    assert s[5] == 1.0 and (q[5] == 0).all()
+    rows = amax > 0
+    assert np.array_equal(s[rows], (amax[rows].astype(np.float32) / np.float32(448)))
+    # the largest element of a row maps to the largest code
+    arg = np.abs(xf).argmax(axis=1)
+    assert ((q[np.arange(40), arg] & 0x7F)[rows] == 0x7E).all()
+    # dequantized values lie within half an E4M3 step (2^-4 relative, or the
+    # subnormal half step) of the inputs
+    deq = oracle.e4m3_to_f64(q) * s[:, None]
+    tol = np.maximum(np.abs(xf) * 2.0 ** -4, (2.0 ** -10) * s[:, None]) * (1 + 1e-6)
+    assert (np.abs(deq - xf) <= tol).all()
+
+
+def _random_codes(shape, seed, spread=64.0):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(*shape, generator=g) * spread).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def _bf16_of(vals):
+    return torch.from_numpy(np.ascontiguousarray(vals, dtype=np.float32)).to(torch.bfloat16) \
+        .view(torch.int16).numpy().view(np.uint16)
+
+
+def test_fp8_expert_mlp_reduces_to_the_bf16_oracle():
+    """E4M3 values are bf16 values, and power-of-two scales are exact: the FP8
+    expert MLP on codes and scales must equal, bit for bit, the pinned bf16
+    expert MLP on the dequantized tensors."""
+    M, E, k, H, I = 5, 6, 3, 64, 48
+    qx = _random_codes((M, H), 1, spread=8.0)
+    qw13 = _random_codes((E, 2 * I, H), 2, spread=8.0)
+    qw2 = _random_codes((E, H, I), 3, spread=8.0)
+    g = np.random.default_rng(5)
+    sx = (2.0 ** g.integers(-4, 2, M)).astype(np.float32)
+    sw13 = (2.0 ** g.integers(-9, -5, (E, 2 * I))).astype(np.float32)
+    sw2 = (2.0 ** g.integers(-9, -5, (E, H))).astype(np.float32)
+    ids = np.stack([g.permutation(E)[:k] for _ in range(M)]).astype(np.int32)
+    wts = g.uniform(0.1, 1.0, (M, k)).astype(np.float32)
+    x_deq = _bf16_of(oracle.e4m3_to_f64(qx) * sx[:, None])
+    w13_deq = _bf16_of(oracle.e4m3_to_f64(qw13) * sw13[:, :, None])
+    w2_deq = _bf16_of(oracle.e4m3_to_f64(qw2) * sw2[:, :, None])
+    a8 = oracle.expert_act_fp8(qx, sx, qw13, sw13, ids)
+    a16 = oracle.expert_act(x_deq, w13_deq, ids)
+    assert np.array_equal(a8, a16)
+    qa = _random_codes((M * k, I), 4, spread=8.0)
+    sa = (2.0 ** g.integers(-3, 3, M * k)).astype(np.float32)
+    a_deq = _bf16_of(oracle.e4m3_to_f64(qa) * sa[:, None])
+    y8 = oracle.expert_down_combine_fp8(qa, sa, qw2, sw2, ids, wts)
+    y16 = oracle.expert_down_combine(a_deq, w2_deq, ids, wts)
+    assert np.array_equal(y8, y16)
+
+
+def test_fp8_forward_quantizes_x_and_a_per_row():
+    """The FP8 layer with every quantization step written out by hand from the
+    pinned pieces above: x's codes and scales from the row quantizer, GEMM 1,
+    a's codes and scales, GEMM 2 and the combine."""
+    M, E, k, H, I = 4, 8, 2, 64, 32
+    g = torch.Generator().manual_seed(9)
+    x = torch.randn(M, H, generator=g).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    lg = torch.randn(M, E, generator=g).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    qw13, qw2 = _random_codes((E, 2 * I, H), 21), _random_codes((E, H, I), 22)
+    sw13 = np.full((E, 2 * I), 0.02 / 64, np.float32)
+    sw2 = np.full((E, H), 0.02 / 64, np.float32)
+    out = oracle.moe_forward_fp8(x, qw13, sw13, qw2, sw2, k, router_logits=lg)
+    ids, wts = oracle.topk_softmax(lg, k)
+    qx, sx = oracle.quant_rows(x)
+    a = oracle.expert_act_fp8(qx, sx, qw13, sw13, ids)
+    qa, sa = oracle.quant_rows(a)
+    y = oracle.expert_down_combine_fp8(qa, sa, qw2, sw2, ids, wts)
+    assert np.array_equal(out["topk_ids"], ids)
+    assert np.array_equal(out["y"], y)

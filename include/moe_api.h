@@ -234,6 +234,81 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *w_router,
                          moe_bf16_t *router_logits_out, void *ws, size_t ws_bytes,
                          cudaStream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * FP8 (E4M3) expert weights, W8A8.  [vLLM] "fused_experts_impl": one kernel
+ * serves bf16 and FP8 weights, and for an FP8 model the GEMM-1 input is the
+ * quantized copy of x.  Format and scale granularity are not given there;
+ * this library takes:
+ *   - E4M3 codes (uint8: 1 sign, 4 exponent bits with bias 7, 3 mantissa
+ *     bits, largest finite 448), each weight matrix with one fp32 scale per
+ *     output row: w13_scales [E, 2I] for W13 codes [E, 2I, H], w2_scales
+ *     [E, H] for W2 codes [E, H, I];
+ *   - activations quantized per row at run time (moe_quantize_rows_fp8):
+ *     x per token before GEMM 1, a per pair before GEMM 2;
+ *   - scales applied after the fp32 sums: h = bf16(s_x s_w sum q_x q_w),
+ *     a = bf16(SiLU(h_gate) * h_up) as in the bf16 layer, and the GEMM-2
+ *     output s_a s_w2 sum q_a q_w2 combined without rounding.
+ * Limits as above; every block size must be one of 16, 32, 64, 128, 256
+ * (the tensor-core tiles; MOE_ERR_UNSUPPORTED_SHAPE otherwise).  Code
+ * pointers are 16-byte aligned.  The router stays bf16.
+ * ------------------------------------------------------------------------- */
+
+/* Per-row dynamic quantization of src [R, K] bf16 (K a multiple of 16):
+ * scales[r] = amax_k |src[r, k]| / 448 (1 for an all-zero row), q[r, k] =
+ * E4M3(src[r, k] / scales[r]) rounded to nearest, ties to even, saturating
+ * at +-448.  amax, the scale and each quotient are fp32 with correctly
+ * rounded division, so the codes depend on the row alone.  q [R, K] uint8
+ * and scales [R] fp32 are outputs.  R == 0 is a no-op. */
+moe_status_t moe_quantize_rows_fp8(const moe_bf16_t *src, int R, int K, uint8_t *q,
+                                   float *scales, cudaStream_t stream);
+
+/* Workspace bytes for moe_forward_fp8: moe_workspace_size's regions plus the quantized x [M, H] / a [M*top_k, I]
+ * codes and their per-row scales.  0 when the arguments are outside the
+ * limits. */
+size_t moe_workspace_size_fp8(int M_max, int E, int top_k, int H, int I, int block_size_m);
+
+/* S3 on E4M3 operands: a [M*top_k, I] bf16 from qx [M, H] codes with
+ * x_scales [M], W13 codes w13 [E, 2I, H] with w13_scales [E, 2I], and the
+ * align lists (as moe_grouped_gemm_w13_act).  block_size_m explicit. */
+moe_status_t moe_grouped_gemm_w13_act_fp8(const uint8_t *qx, const float *x_scales,
+                                          const uint8_t *w13, const float *w13_scales,
+                                          const int32_t *sorted_token_ids,
+                                          const int32_t *expert_ids,
+                                          const int32_t *num_tokens_post_padded, int M,
+                                          int top_k, int E, int H, int I, int block_size_m,
+                                          moe_bf16_t *a, cudaStream_t stream);
+
+/* S4 on E4M3 operands: y [M, H] bf16 = bf16(sum_j w_j s_a s_w2 (q_a . q_w2)
+ * + residual) from qa [M*top_k, I] codes with a_scales [M*top_k], W2 codes
+ * w2 [E, H, I] with w2_scales [E, H], topk_weights [M, top_k] fp32 and the
+ * align lists.  ws_bytes >= moe_workspace_size(M, E, top_k, H, I,
+ * block_size_m) (the fp32 accumulator lives there). */
+moe_status_t moe_grouped_gemm_w2_combine_fp8(const uint8_t *qa, const float *a_scales,
+                                             const uint8_t *w2, const float *w2_scales,
+                                             const int32_t *sorted_token_ids,
+                                             const int32_t *expert_ids,
+                                             const int32_t *num_tokens_post_padded,
+                                             const float *topk_weights,
+                                             const moe_bf16_t *residual, int M, int top_k,
+                                             int E, int H, int I, int block_size_m,
+                                             moe_bf16_t *y, void *ws, size_t ws_bytes,
+                                             cudaStream_t stream);
+
+/* The whole layer with E4M3 expert weights: routing as moe_forward (bf16
+ * router or given logits), x quantized per token, GEMM 1 on codes, a
+ * quantized per pair, GEMM 2 + combine on codes.  Arguments as moe_forward,
+ * with the W13 / W2 codes and their row scales in place of the bf16 weights;
+ * ws_bytes >= moe_workspace_size_fp8(M, E, top_k, H, I, block_size_m).
+ * Runs the kernel chain (MOE_DECODE_LAYER does not apply). */
+moe_status_t moe_forward_fp8(const moe_bf16_t *x, const moe_bf16_t *w_router,
+                             const moe_bf16_t *router_logits, const float *router_bias,
+                             const uint8_t *w13, const float *w13_scales, const uint8_t *w2,
+                             const float *w2_scales, const moe_bf16_t *residual, int M, int E,
+                             int top_k, int H, int I, int renormalize, int block_size_m,
+                             moe_bf16_t *y, int32_t *topk_ids_out, float *topk_weights_out,
+                             moe_bf16_t *router_logits_out, void *ws, size_t ws_bytes,
+                             cudaStream_t stream);
+
 /* Clears the whole workspace (asynchronously on `stream`).  Call it once on a
  * freshly allocated workspace before its first use: the status word at its
  * start must begin at zero.  ws must be 256-byte aligned. */

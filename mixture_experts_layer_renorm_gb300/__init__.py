@@ -27,6 +27,8 @@ __all__ = [
     "moe_align_block_size", "moe_grouped_gemm_w13_act", "moe_grouped_gemm_w2_combine",
     "moe_forward", "moe_get_device_status", "moe_status_string", "Workspace",
     "moe_grouped_gemm_w2_combine_noalloc", "moe_route", "moe_selftest_device_timeout",
+    "moe_quantize_rows_fp8", "moe_workspace_size_fp8", "moe_grouped_gemm_w13_act_fp8",
+    "moe_grouped_gemm_w2_combine_fp8", "moe_forward_fp8",
 ]
 
 STATUS_NAMES = {
@@ -41,7 +43,8 @@ EXPORTED = (
     "moe_topk_softmax", "moe_align_block_size", "moe_grouped_gemm_w13_act",
     "moe_grouped_gemm_w2_combine", "moe_forward", "moe_workspace_init", "moe_get_device_status",
     "moe_status_string", "moe_grouped_gemm_w2_combine_noalloc", "moe_route",
-    "moe_selftest_device_timeout",
+    "moe_selftest_device_timeout", "moe_quantize_rows_fp8", "moe_workspace_size_fp8",
+    "moe_grouped_gemm_w13_act_fp8", "moe_grouped_gemm_w2_combine_fp8", "moe_forward_fp8",
 )
 
 
@@ -87,6 +90,13 @@ def load_library(build_if_missing: bool = False):
         "moe_get_device_status": ([P, P], I),
         "moe_selftest_device_timeout": ([P, Z, I, P], I),
         "moe_status_string": ([I], ctypes.c_char_p),
+        "moe_quantize_rows_fp8": ([P, I, I, P, P, P], I),
+        "moe_workspace_size_fp8": ([I, I, I, I, I, I], Z),
+        "moe_grouped_gemm_w13_act_fp8": ([P, P, P, P, P, P, P, I, I, I, I, I, I, P, P], I),
+        "moe_grouped_gemm_w2_combine_fp8": ([P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, P, P, Z,
+                                             P], I),
+        "moe_forward_fp8": ([P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, P, P, P, Z, P],
+                            I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -149,12 +159,22 @@ def moe_status_string(status: int) -> str:
     return load_library().moe_status_string(int(status)).decode()
 
 
+def moe_workspace_size_fp8(M_max: int, E: int, top_k: int, H: int, I: int,
+                           block_size_m: int = 0) -> int:
+    n = load_library().moe_workspace_size_fp8(M_max, E, top_k, H, I, block_size_m)
+    if n == 0:
+        raise MoeError(2, "moe_workspace_size_fp8")
+    return int(n)
+
+
 class Workspace:
-    """One caller-owned workspace buffer, sized once and reused by every call."""
+    """One caller-owned workspace buffer, sized once and reused by every call
+    (fp8=True sizes it for moe_forward_fp8)."""
 
     def __init__(self, M_max: int, E: int, top_k: int, H: int, I: int, block_size_m: int = 0,
-                 device=None, stream=None):
-        self.nbytes = moe_workspace_size(M_max, E, top_k, H, I, block_size_m)
+                 device=None, stream=None, fp8: bool = False):
+        size = moe_workspace_size_fp8 if fp8 else moe_workspace_size
+        self.nbytes = size(M_max, E, top_k, H, I, block_size_m)
         self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device or "cuda")
         moe_workspace_init(self.buf, stream=stream)
 
@@ -320,3 +340,74 @@ def moe_forward(x, w13, w2, top_k: int, y, ws, *, w_router=None, router_logits=N
                                    int(bool(renormalize)), block_size_m, _p(y), _p(topk_ids_out),
                                    _p(topk_weights_out), _p(router_logits_out), ptr, n,
                                    _stream(stream)), "moe_forward")
+
+
+# ----------------------------------------------------------------------------- FP8 (E4M3) weights
+# Codes are torch.uint8 tensors (E4M3 bit patterns, e.g. a float8_e4m3fn tensor
+# viewed as uint8); scales are fp32, one per row.
+
+def moe_quantize_rows_fp8(src, q, scales, stream=None) -> None:
+    """Per-row dynamic E4M3 quantization: scales[r] = amax|src[r]| / 448, q = e4m3(src / s)."""
+    _check_dtype(src, torch.bfloat16, "src")
+    _check_dtype(q, torch.uint8, "q")
+    _check_dtype(scales, torch.float32, "scales")
+    R, K = src.shape
+    _ok(load_library().moe_quantize_rows_fp8(_p(src), R, K, _p(q), _p(scales), _stream(stream)),
+        "moe_quantize_rows_fp8")
+
+
+def moe_grouped_gemm_w13_act_fp8(qx, x_scales, w13, w13_scales, sorted_token_ids, expert_ids,
+                                 num_tokens_post_padded, top_k: int, block_size_m: int, a,
+                                 stream=None) -> None:
+    for t, n in ((qx, "qx"), (w13, "w13")):
+        _check_dtype(t, torch.uint8, n)
+    for t, n in ((x_scales, "x_scales"), (w13_scales, "w13_scales")):
+        _check_dtype(t, torch.float32, n)
+    _check_dtype(a, torch.bfloat16, "a")
+    M, H = qx.shape
+    E, twoI, _ = w13.shape
+    _ok(load_library().moe_grouped_gemm_w13_act_fp8(
+        _p(qx), _p(x_scales), _p(w13), _p(w13_scales), _p(sorted_token_ids), _p(expert_ids),
+        _p(num_tokens_post_padded), M, top_k, E, H, twoI // 2, block_size_m, _p(a),
+        _stream(stream)), "moe_grouped_gemm_w13_act_fp8")
+
+
+def moe_grouped_gemm_w2_combine_fp8(qa, a_scales, w2, w2_scales, sorted_token_ids, expert_ids,
+                                    num_tokens_post_padded, topk_weights, top_k: int,
+                                    block_size_m: int, y, ws, residual=None, stream=None) -> None:
+    for t, n in ((qa, "qa"), (w2, "w2")):
+        _check_dtype(t, torch.uint8, n)
+    for t, n in ((a_scales, "a_scales"), (w2_scales, "w2_scales"), (topk_weights, "topk_weights")):
+        _check_dtype(t, torch.float32, n)
+    _check_dtype(y, torch.bfloat16, "y")
+    _check_dtype(residual, torch.bfloat16, "residual")
+    M, H = y.shape
+    E, _, I = w2.shape
+    ptr, n = _ws(ws)
+    _ok(load_library().moe_grouped_gemm_w2_combine_fp8(
+        _p(qa), _p(a_scales), _p(w2), _p(w2_scales), _p(sorted_token_ids), _p(expert_ids),
+        _p(num_tokens_post_padded), _p(topk_weights), _p(residual), M, top_k, E, H, I,
+        block_size_m, _p(y), ptr, n, _stream(stream)), "moe_grouped_gemm_w2_combine_fp8")
+
+
+def moe_forward_fp8(x, w13, w13_scales, w2, w2_scales, top_k: int, y, ws, *, w_router=None,
+                    router_logits=None, router_bias=None, residual=None,
+                    renormalize: bool = True, block_size_m: int = 0, topk_ids_out=None,
+                    topk_weights_out=None, router_logits_out=None, stream=None) -> None:
+    for t, n in ((x, "x"), (y, "y"), (w_router, "w_router"), (router_logits, "router_logits"),
+                 (residual, "residual"), (router_logits_out, "router_logits_out")):
+        _check_dtype(t, torch.bfloat16, n)
+    for t, n in ((w13, "w13"), (w2, "w2")):
+        _check_dtype(t, torch.uint8, n)
+    for t, n in ((w13_scales, "w13_scales"), (w2_scales, "w2_scales"),
+                 (router_bias, "router_bias"), (topk_weights_out, "topk_weights_out")):
+        _check_dtype(t, torch.float32, n)
+    _check_dtype(topk_ids_out, torch.int32, "topk_ids_out")
+    M, H = x.shape
+    E, twoI, _ = w13.shape
+    ptr, n = _ws(ws)
+    _ok(load_library().moe_forward_fp8(
+        _p(x), _p(w_router), _p(router_logits), _p(router_bias), _p(w13), _p(w13_scales), _p(w2),
+        _p(w2_scales), _p(residual), M, E, top_k, H, twoI // 2, int(bool(renormalize)),
+        block_size_m, _p(y), _p(topk_ids_out), _p(topk_weights_out), _p(router_logits_out), ptr, n,
+        _stream(stream)), "moe_forward_fp8")

@@ -250,6 +250,17 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint6
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// D[tmem] (+)= A[smem] . B[smem]^T, E4M3 inputs, fp32 accumulate (K = 32 per
+// instruction: the same 32 bytes of each row as a bf16 MMA's K = 16).
+__device__ __forceinline__ void umma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // Arrives once on the barrier when every MMA this thread issued has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile(
@@ -267,6 +278,15 @@ __device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, 
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_e4m3_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
@@ -369,6 +389,12 @@ __host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N) {
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Instruction descriptor of kind::f8f6f4: E4M3 A and B (K-major), fp32 D, M x N
+// (A and B format fields 0 = E4M3).
+__host__ __device__ constexpr uint32_t umma_idesc_e4m3(int M, int N) {
+  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 template <int N, int MODE, bool P2 = false>
 struct TcConfig {
   // Wide tiles (N = 256 token columns, GEMMs 1 and 2): ONE 128-row weight tile
@@ -415,7 +441,7 @@ struct TcConfig {
 };
 
 // Tile t of the persistent schedule: block b, weight tile c, and the K-stage
-// range [kb0, kb1) of split sp (ksplit splits; the splits of one tile are
+// range [kb0, kb1) of split sp (ksplit <= nk splits; the splits of one tile are
 // neighbours in the schedule and run side by side).  With n_pass > 1 (GEMM 2
 // with a large combine accumulator) the weight tiles are cut into n_pass
 // ranges of ctp tiles, run one range after the other over every block: while
@@ -452,9 +478,10 @@ __device__ __forceinline__ TileCoord tile_coord(int t, const TileSched &s) {
   const int cl = r / s.ksplit;
   tc.c = p * s.ctp + cl;
   const int sp = r - cl * s.ksplit;
-  const int span = (s.nk + s.ksplit - 1) / s.ksplit;
-  tc.kb0 = min(s.nk, sp * span);
-  tc.kb1 = min(s.nk, tc.kb0 + span);
+  // balanced ranges: none is empty while ksplit <= nk (an empty range would
+  // hand the epilogue an accumulator that no MMA of this tile wrote)
+  tc.kb0 = sp * s.nk / s.ksplit;
+  tc.kb1 = (sp + 1) * s.nk / s.ksplit;
   return tc;
 }
 
@@ -503,7 +530,13 @@ __device__ __forceinline__ void pair_bar_sync(int pair) {
 //                                 y_acc[p / top_k, n] += topk_w[p] * o
 // MODE 2: router logits           rows = x[t] (blocks of N consecutive tokens),
 //                                 A = W_r rows e0..e0+255, logits[t, e] = bf16(D + bias[e])
-template <int N, int MODE, bool P2>
+//
+// F8 (GEMM 1 and 2): E4M3 weights and E4M3 rows (src holds codes, one byte
+// each), one fp32 scale per weight row (row_scale [E, a_rows]) and per source
+// row (col_scale: per token for GEMM 1, per pair for GEMM 2); the sums are
+// scaled by both before the epilogue's rounding or combine.  A stage then
+// covers 128 K elements (the same 128 bytes per row).
+template <int N, int MODE, bool P2, bool F8>
 __global__ void __launch_bounds__(kTcThreads, 1)
 k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict__ src,
           int src_rows, const int32_t *__restrict__ sorted_ids, const int32_t *__restrict__ expert_ids,
@@ -512,9 +545,12 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
           float *__restrict__ h_acc, int *__restrict__ tile_cnt, uint16_t *__restrict__ out16,
           float *__restrict__ y_acc, int H_out, int *status, int early_weights, int n_pass,
           const uint8_t *__restrict__ w_pf, long pf_bytes, float4 *__restrict__ zero_dst,
-          long zero_n4) {
+          long zero_n4, const float *__restrict__ row_scale, const float *__restrict__ col_scale) {
   using Cfg = TcConfig<N, MODE, P2>;
   constexpr int S = Cfg::kStages;
+  static_assert(!F8 || MODE != 2, "the router runs in bf16");
+  constexpr int kElt = F8 ? 1 : 2;              // bytes per element
+  constexpr int kBKe = kBK * 2 / kElt;          // K elements per stage (128 bytes per row)
   // With early_weights (GEMM 2 right after GEMM 1 in one layer) only the row
   // gathers wait for the previous kernel: the weight tiles and the routing
   // lists it reads were final before GEMM 1 started, so the weights stream
@@ -615,7 +651,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
   tc_fence_after();
   if constexpr (P2) cluster_sync();  // the other CTA's barriers exist before any arrival
   const uint32_t tmem = *tmem_slot;
-  const int nk = (K + kBK - 1) / kBK;
+  const int nk = (K + kBKe - 1) / kBKe;
   const TileSched sched = make_sched(n_cunits, ksplit, nk, n_blocks, MODE == 1 ? n_pass : 1);
   auto coord = [&](int t) {
     TileCoord tc = tile_coord(t, sched);
@@ -664,8 +700,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
           const uint32_t fb = smem_u32(&full[s]);
           const uint32_t a_s = smem_u32(a_tiles + s * Cfg::kATiles * kATileBytes);
           mbar_arrive_expect_tx(fb, tx);
-          tma_load_3d(a_s, &tmap_w, kb * kBK, row0, e, fb);
-          if (two) tma_load_3d(a_s + second, &tmap_w, kb * kBK, row1, e, fb);
+          tma_load_3d(a_s, &tmap_w, kb * kBKe, row0, e, fb);
+          if (two) tma_load_3d(a_s + second, &tmap_w, kb * kBKe, row1, e, fb);
         }
       }
       if constexpr (P2) {
@@ -759,12 +795,13 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
           break;
         }
         const uint32_t b_s = smem_u32(b_tiles + s * Cfg::kBStageBytes);
-        const int kel = kb * kBK + ch * 8;
+        const int kel = kb * kBKe + ch * (16 / kElt);  // first element of this thread's chunk
+        const uint8_t *srcb = reinterpret_cast<const uint8_t *>(src);
 #pragma unroll
         for (int u = 0; u < Cfg::kChunksPerThread; ++u) {
           const int r = (gt >> 3) + 16 * u;
           const bool ok = rowv[u] >= 0 && kel < K;
-          const uint16_t *gp = ok ? src + (size_t)rowv[u] * K + kel : src;
+          const uint8_t *gp = ok ? srcb + ((size_t)rowv[u] * K + kel) * kElt : srcb;
           const uint32_t dst = b_s + (r >> 3) * 1024 + (r & 7) * 128 + ((ch ^ (r & 7)) << 4);
           cp_async_16(dst, gp, ok ? 16u : 0u);
         }
@@ -775,7 +812,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA
     if (lane == 0 && (!P2 || rank == 0)) {
-      constexpr uint32_t idesc = umma_idesc_bf16(P2 ? 2 * kTileM : kTileM, N);
+      constexpr uint32_t idesc = F8 ? umma_idesc_e4m3(P2 ? 2 * kTileM : kTileM, N)
+                                    : umma_idesc_bf16(P2 ? 2 * kTileM : kTileM, N);
       int g = 0, i = 0;
       bool stop = false;
       for (int t = t0; t < n_tiles && !stop; t += tstride) {
@@ -802,8 +840,13 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint32_t accumulate = (kb > tc.kb0 || kk > 0) ? 1u : 0u;
             const uint64_t bd = sw128_kmajor_desc(bt + kk * 32);
-            if constexpr (P2) {
+            if constexpr (P2 && F8) {
+              umma_e4m3_pair(d0, sw128_kmajor_desc(a0 + kk * 32), bd, idesc, accumulate);
+            } else if constexpr (P2) {
               umma_bf16_pair(d0, sw128_kmajor_desc(a0 + kk * 32), bd, idesc, accumulate);
+            } else if constexpr (F8) {
+              umma_e4m3(d0, sw128_kmajor_desc(a0 + kk * 32), bd, idesc, accumulate);
+              if (two) umma_e4m3(d0 + N, sw128_kmajor_desc(a1 + kk * 32), bd, idesc, accumulate);
             } else {
               umma_bf16(d0, sw128_kmajor_desc(a0 + kk * 32), bd, idesc, accumulate);
               if (two) umma_bf16(d0 + N, sw128_kmajor_desc(a1 + kk * 32), bd, idesc, accumulate);
@@ -825,13 +868,19 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
     const int et = threadIdx.x - 64;   // 0..255 over the epilogue warps
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     if (MODE == 0 && zero_n4 > 0) zero_slice(et, kEpiThreads);
+    // F8 GEMM 2: the per-pair scales staged below are the previous kernel's
+    // output (the quantization of a), unlike the routing lists
+    if (F8 && early) griddep_wait();
     int i = 0;
     for (int t = t0; t < n_tiles; t += tstride) {
       const TileCoord tc = coord(t);
       const int b = tc.b, c = tc.c;
       // a block whose expert id lies outside [0, E) is computed (on zero
       // weights) but writes nothing
-      const bool e_ok = MODE == 2 || (static_cast<unsigned>(expert_ids[b]) < static_cast<unsigned>(E));
+      const int e_cur = MODE == 2 ? 0 : expert_ids[b];
+      const bool e_ok = MODE == 2 || (static_cast<unsigned>(e_cur) < static_cast<unsigned>(E));
+      // F8: scale of weight row r of this tile's expert
+      auto wscale = [&](int r) { return F8 && e_ok ? row_scale[(size_t)e_cur * a_rows + r] : 1.f; };
       const bool two = !Cfg::kWide && (MODE == 0 || c * 2 * kTileM + kTileM < a_rows);
       const int acc = i % Cfg::kAccBufs;
       const uint32_t use = i / Cfg::kAccBufs;
@@ -848,6 +897,9 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
           if (p >= 0 && p < P) {
             d = MODE == 0 ? p : p / top_k;
             if (MODE == 1) wgt = vec[p];
+            // F8: the source row's scale (GEMM 1: the token's; GEMM 2: the
+            // pair's, folded into the router weight)
+            if (F8) wgt = MODE == 0 ? col_scale[p / top_k] : wgt * col_scale[p];
           }
         }
         dst_row[j] = d;
@@ -873,12 +925,20 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
         const bool valid = chn < R_out;
         // [pair][buffer][direction][column half][lane] of 16 bytes (8 bf16 columns)
         uint4 *slot = reinterpret_cast<uint4 *>(xchg) + pair * (2 * 2 * 32 * 2);
+        const float srow = valid ? wscale(is_gate ? chn : R_out + chn) : 1.f;
 #pragma unroll 1
         for (int j0 = 32 * half, it = 0; j0 < N; j0 += 64, ++it) {
           uint32_t lo[16], hi[16];
           tmem_ld_32x32b_x16(d0 + j0, lo);
           tmem_ld_32x32b_x16(d0 + j0 + 16, hi);
           tmem_ld_wait();
+          if constexpr (F8) {
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+              lo[jj] = __float_as_uint(__uint_as_float(lo[jj]) * srow * dst_w[j0 + jj]);
+              hi[jj] = __float_as_uint(__uint_as_float(hi[jj]) * srow * dst_w[j0 + 16 + jj]);
+            }
+          }
           uint4 *buf = slot + (it & 1) * (2 * 32 * 2);
           // the gate warp gives away columns 16..31, the up warp columns 0..15
           {
@@ -911,12 +971,20 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
       } else if (MODE == 0) {
         const int chn = c * kTileM + q * 32 + lane;
         const bool valid = chn < R_out;
+        const float sg = valid ? wscale(chn) : 1.f, su = valid ? wscale(R_out + chn) : 1.f;
 #pragma unroll 1
         for (int j0 = 16 * half; j0 < N; j0 += 32) {
           uint32_t gt[16], up[16];
           tmem_ld_32x32b_x16(d0 + j0, gt);
           tmem_ld_32x32b_x16(d0 + N + j0, up);
           tmem_ld_wait();
+          if constexpr (F8) {
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+              gt[jj] = __float_as_uint(__uint_as_float(gt[jj]) * sg * dst_w[j0 + jj]);
+              up[jj] = __float_as_uint(__uint_as_float(up[jj]) * su * dst_w[j0 + jj]);
+            }
+          }
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) {
             const int p = dst_row[j0 + jj];
@@ -946,9 +1014,10 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
         auto process = [&](int item, const uint32_t (&o)[16]) {
           const int h = item / n_chunks, j0 = (item - h * n_chunks) * 16;
           const int n = c * Cfg::kRowsPerCTile + h * kTileM + q * 32 + lane;
+          const float srow = (F8 && MODE == 1 && n < H_out) ? wscale(n) : 1.f;
           if (MODE == 1 && Cfg::kWide) {
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) scr[jj * 32 + lane] = __uint_as_float(o[jj]);
+            for (int jj = 0; jj < 16; ++jj) scr[jj * 32 + lane] = __uint_as_float(o[jj]) * srow;
             __syncwarp();
             const int n4 = n - lane + 4 * q4;  // first of this thread's 4 channels
             if (n4 < H_out) {                  // H_out is a multiple of 16: all 4 or none
@@ -973,7 +1042,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
               const int d = dst_row[j0 + jj];
               if (valid && d >= 0) {
                 if (MODE == 1)
-                  atomicAdd(y_acc + (size_t)d * H_out + n, dst_w[j0 + jj] * __uint_as_float(o[jj]));
+                  atomicAdd(y_acc + (size_t)d * H_out + n, dst_w[j0 + jj] * (__uint_as_float(o[jj]) * srow));
                 else
                   out16[(size_t)d * a_rows + n] = float_to_bf16_bits(__uint_as_float(o[jj]) + bias);
               }
@@ -1056,19 +1125,22 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
   return fn;
 }
 
-// 3-D map over weights [E][rows][K] (bf16, K contiguous), box 64 x box_rows x 1,
-// 128-byte swizzle; out-of-range rows and columns read as zero.
-cudaError_t encode_weight_map(CUtensorMap *map, const uint16_t *w, int K, int rows, int E,
-                              int box_rows) {
+// 3-D map over weights [E][rows][K] (bf16, or E4M3 codes with elt_bytes = 1;
+// K contiguous), box of 128 bytes of K x box_rows x 1, 128-byte swizzle;
+// out-of-range rows and columns read as zero.
+cudaError_t encode_weight_map(CUtensorMap *map, const void *w, int K, int rows, int E,
+                              int box_rows, int elt_bytes) {
   PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode_fn();
   if (encode == nullptr) return cudaErrorNotSupported;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows),
                               static_cast<cuuint64_t>(E)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2,
-                                 static_cast<cuuint64_t>(K) * 2 * rows};
-  const cuuint32_t box[3] = {kBK, static_cast<cuuint32_t>(box_rows), 1};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * elt_bytes,
+                                 static_cast<cuuint64_t>(K) * elt_bytes * rows};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kBK * 2 / elt_bytes),
+                             static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t *>(w),
+  const CUresult r = encode(map, elt_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                            3, const_cast<void *>(w),
                             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -1080,15 +1152,15 @@ cudaError_t encode_weight_map(CUtensorMap *map, const uint16_t *w, int K, int ro
 struct MapEntry {
   int dev;
   const void *ptr;
-  int K, rows, E, box_rows;
+  int K, rows, E, box_rows, elt;
   CUtensorMap map;
 };
 std::mutex g_map_mutex;
 MapEntry g_maps[128];
 int g_map_next = 0, g_map_count = 0;
 
-cudaError_t make_weight_map(CUtensorMap *map, const uint16_t *w, int K, int rows, int E,
-                            int box_rows = kTileM) {
+cudaError_t make_weight_map(CUtensorMap *map, const void *w, int K, int rows, int E,
+                            int box_rows = kTileM, int elt_bytes = 2) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
@@ -1096,15 +1168,15 @@ cudaError_t make_weight_map(CUtensorMap *map, const uint16_t *w, int K, int rows
   for (int i = 0; i < g_map_count; ++i) {
     const MapEntry &m = g_maps[i];
     if (m.dev == dev && m.ptr == w && m.K == K && m.rows == rows && m.E == E &&
-        m.box_rows == box_rows) {
+        m.box_rows == box_rows && m.elt == elt_bytes) {
       *map = m.map;
       return cudaSuccess;
     }
   }
-  err = encode_weight_map(map, w, K, rows, E, box_rows);
+  err = encode_weight_map(map, w, K, rows, E, box_rows, elt_bytes);
   if (err != cudaSuccess) return err;
   MapEntry &m = g_maps[g_map_next];
-  m = MapEntry{dev, w, K, rows, E, box_rows, *map};
+  m = MapEntry{dev, w, K, rows, E, box_rows, elt_bytes, *map};
   g_map_next = (g_map_next + 1) % 128;
   if (g_map_count < 128) ++g_map_count;
   return cudaSuccess;
@@ -1130,10 +1202,12 @@ struct TcArgs {
   long pf_bytes = 0;
   float *zero_dst = nullptr;  // GEMM 1: fp32 buffer to clear (zero_n floats, a multiple of 4)
   long zero_n = 0;
+  const float *row_scale = nullptr;  // E4M3 weights: per weight row
+  const float *col_scale = nullptr;  // E4M3 rows: per token (GEMM 1) or pair (GEMM 2)
 };
 
 // Clusters of two CTAs of the 2-SM kernel that can be resident at once (0: none).
-template <int N, int MODE>
+template <int N, int MODE, bool F8>
 int max_pair_clusters() {
   static int cached[64];
   static bool known[64];
@@ -1154,7 +1228,7 @@ int max_pair_clusters() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, k_gemm_tc<N, MODE, true>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, k_gemm_tc<N, MODE, true, F8>, &cfg) != cudaSuccess) {
       (void)cudaGetLastError();
       n = 0;
     }
@@ -1164,7 +1238,7 @@ int max_pair_clusters() {
   return cached[dev];
 }
 
-template <int N, int MODE>
+template <int N, int MODE, bool F8>
 cudaError_t launch_tc_n(const CUtensorMap &map_w, const TcArgs &a, cudaStream_t s) {
   using Cfg = TcConfig<N, MODE>;
   cudaError_t err;
@@ -1175,10 +1249,10 @@ cudaError_t launch_tc_n(const CUtensorMap &map_w, const TcArgs &a, cudaStream_t 
     const char *force = std::getenv("MOE_FORCE_PATH");
     const bool no_pairs = force != nullptr && std::strcmp(force, "tc1") == 0;
     if (kPairTiles && !no_pairs && a.ksplit == 1 && a.n_ctiles % 2 == 0) {
-      auto kern2 = k_gemm_tc<N, MODE, true>;
+      auto kern2 = k_gemm_tc<N, MODE, true, F8>;
       err = ensure_smem_limit(reinterpret_cast<const void *>(kern2), TcConfig<N, MODE, true>::kSmemBytes);
       if (err != cudaSuccess) return err;
-      const int units_max = max_pair_clusters<N, MODE>();
+      const int units_max = max_pair_clusters<N, MODE, F8>();
       if (units_max > 0) {
         const int units =
             static_cast<int>(std::min<long>(a.max_blocks * (a.n_ctiles / 2), units_max));
@@ -1189,11 +1263,12 @@ cudaError_t launch_tc_n(const CUtensorMap &map_w, const TcArgs &a, cudaStream_t 
                                   a.top_k, a.E, a.K, a.R_out, a.a_rows, a.B, a.cap, a.n_ctiles,
                                   a.ksplit, a.h_acc, a.tile_cnt, a.out16, a.y_acc, a.H_out,
                                   a.status, a.early_weights, a.n_pass, a.w_pf, a.pf_bytes,
-                                  reinterpret_cast<float4 *>(a.zero_dst), a.zero_n / 4);
+                                  reinterpret_cast<float4 *>(a.zero_dst), a.zero_n / 4,
+                                  a.row_scale, a.col_scale);
       }
     }
   }
-  auto kern = k_gemm_tc<N, MODE, false>;
+  auto kern = k_gemm_tc<N, MODE, false, F8>;
   err = ensure_smem_limit(reinterpret_cast<const void *>(kern), Cfg::kSmemBytes);
   if (err != cudaSuccess) return err;
   // persistent: one CTA per SM at most, each walking the tile list with stride gridDim.x
@@ -1204,17 +1279,18 @@ cudaError_t launch_tc_n(const CUtensorMap &map_w, const TcArgs &a, cudaStream_t 
                     a.src_rows, a.sorted_ids, a.expert_ids, a.n_post, a.vec, a.P, a.top_k, a.E,
                     a.K, a.R_out, a.a_rows, a.B, a.cap, a.n_ctiles, a.ksplit, a.h_acc, a.tile_cnt,
                     a.out16, a.y_acc, a.H_out, a.status, a.early_weights, a.n_pass, a.w_pf,
-                    a.pf_bytes, reinterpret_cast<float4 *>(a.zero_dst), a.zero_n / 4);
+                    a.pf_bytes, reinterpret_cast<float4 *>(a.zero_dst), a.zero_n / 4, a.row_scale,
+                    a.col_scale);
 }
 
-template <int MODE>
+template <int MODE, bool F8 = false>
 cudaError_t launch_tc(int N, const CUtensorMap &map_w, const TcArgs &a, cudaStream_t s) {
   switch (N) {
-    case 16: return launch_tc_n<16, MODE>(map_w, a, s);
-    case 32: return launch_tc_n<32, MODE>(map_w, a, s);
-    case 64: return launch_tc_n<64, MODE>(map_w, a, s);
-    case 128: return launch_tc_n<128, MODE>(map_w, a, s);
-    case 256: return launch_tc_n<256, MODE>(map_w, a, s);
+    case 16: return launch_tc_n<16, MODE, F8>(map_w, a, s);
+    case 32: return launch_tc_n<32, MODE, F8>(map_w, a, s);
+    case 64: return launch_tc_n<64, MODE, F8>(map_w, a, s);
+    case 128: return launch_tc_n<128, MODE, F8>(map_w, a, s);
+    case 256: return launch_tc_n<256, MODE, F8>(map_w, a, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -1223,20 +1299,27 @@ cudaError_t launch_tc(int N, const CUtensorMap &map_w, const TcArgs &a, cudaStre
 
 bool tc_supports_block(int B) { return B == 16 || B == 32 || B == 64 || B == 128 || B == 256; }
 
-cudaError_t launch_tc_w13_act(const uint16_t *x, const uint16_t *w13, const int32_t *sorted_ids,
-                              const int32_t *expert_ids, const int32_t *n_post, int P, int top_k,
-                              int E, int H, int I, int B, int cap, uint16_t *a, int ksplit,
-                              float *h_acc, int *tile_cnt, int *status, int pf_experts,
-                              float *zero_dst, long zero_n, cudaStream_t s) {
+namespace {
+
+// GEMM 1 on bf16 operands, or (F8) on E4M3 codes with per-row scales.
+template <bool F8>
+cudaError_t tc_w13_impl(const void *x, const void *w13, const float *w13_scale,
+                        const float *x_scale, const int32_t *sorted_ids, const int32_t *expert_ids,
+                        const int32_t *n_post, int P, int top_k, int E, int H, int I, int B,
+                        int cap, uint16_t *a, int ksplit, float *h_acc, int *tile_cnt,
+                        int *status, int pf_experts, float *zero_dst, long zero_n,
+                        cudaStream_t s) {
+  constexpr int elt = F8 ? 1 : 2;
+  constexpr int bke = kBK * 2 / elt;  // K elements per stage
   // wide tiles (B = 256): 64 gate rows over 64 up rows per weight tile, no K split
   const bool wide = B == 256;
   CUtensorMap map_w;
-  cudaError_t err = make_weight_map(&map_w, w13, H, 2 * I, E, wide ? kTileM / 2 : kTileM);
+  cudaError_t err = make_weight_map(&map_w, w13, H, 2 * I, E, wide ? kTileM / 2 : kTileM, elt);
   if (err != cudaSuccess) return err;
-  const int nk = (H + kBK - 1) / kBK;
+  const int nk = (H + bke - 1) / bke;
   if (wide || ksplit < 1 || ksplit > nk || h_acc == nullptr || tile_cnt == nullptr) ksplit = 1;
   TcArgs args{};
-  args.src = x;
+  args.src = static_cast<const uint16_t *>(x);
   args.src_rows = (P + top_k - 1) / top_k;
   args.sorted_ids = sorted_ids;
   args.expert_ids = expert_ids;
@@ -1259,16 +1342,41 @@ cudaError_t launch_tc_w13_act(const uint16_t *x, const uint16_t *w13, const int3
   args.max_blocks = cap / B;
   args.zero_dst = zero_dst;
   args.zero_n = zero_dst != nullptr ? zero_n : 0;
+  args.row_scale = w13_scale;
+  args.col_scale = x_scale;
   if (pf_experts > 0) {
     // the first wave's experts: ceil(SMs / tiles per block) blocks, one expert
     // each at decode sizes, plus one for an expert without pairs among them
-    const long per_e = 2l * I * H * 2;
+    const long per_e = 2l * I * H * elt;
     const int wave = (num_sms() + args.n_ctiles * ksplit - 1) / (args.n_ctiles * ksplit) + 1;
     const int n_e = std::min(std::min(pf_experts, wave), E);
-    args.w_pf = reinterpret_cast<const uint8_t *>(w13);
+    args.w_pf = static_cast<const uint8_t *>(w13);
     args.pf_bytes = std::min<long>(n_e * per_e, 96l << 20);
   }
-  return launch_tc<0>(B, map_w, args, s);
+  return launch_tc<0, F8>(B, map_w, args, s);
+}
+
+}  // namespace
+
+cudaError_t launch_tc_w13_act(const uint16_t *x, const uint16_t *w13, const int32_t *sorted_ids,
+                              const int32_t *expert_ids, const int32_t *n_post, int P, int top_k,
+                              int E, int H, int I, int B, int cap, uint16_t *a, int ksplit,
+                              float *h_acc, int *tile_cnt, int *status, int pf_experts,
+                              float *zero_dst, long zero_n, cudaStream_t s) {
+  return tc_w13_impl<false>(x, w13, nullptr, nullptr, sorted_ids, expert_ids, n_post, P, top_k, E,
+                            H, I, B, cap, a, ksplit, h_acc, tile_cnt, status, pf_experts, zero_dst,
+                            zero_n, s);
+}
+
+cudaError_t launch_tc_w13_act_f8(const uint8_t *qx, const float *sx, const uint8_t *w13q,
+                                 const float *w13s, const int32_t *sorted_ids,
+                                 const int32_t *expert_ids, const int32_t *n_post, int P, int top_k,
+                                 int E, int H, int I, int B, int cap, uint16_t *a, int ksplit,
+                                 float *h_acc, int *tile_cnt, int *status, int pf_experts,
+                                 float *zero_dst, long zero_n, cudaStream_t s) {
+  return tc_w13_impl<true>(qx, w13q, w13s, sx, sorted_ids, expert_ids, n_post, P, top_k, E, H, I,
+                           B, cap, a, ksplit, h_acc, tile_cnt, status, pf_experts, zero_dst,
+                           zero_n, s);
 }
 
 // Ranges of GEMM 2's weight tiles run one after the other so that the live
@@ -1282,17 +1390,22 @@ static int gemm2_passes(long y_bytes, int n_ctiles) {
   return (n_ctiles + ctp - 1) / ctp;
 }
 
-cudaError_t launch_tc_w2_combine(const uint16_t *a, const uint16_t *w2, const int32_t *sorted_ids,
-                                 const int32_t *expert_ids, const int32_t *n_post,
-                                 const float *topk_weights, int P, int top_k, int E, int H, int I,
-                                 int B, int cap, float *y_acc, int ksplit, int *status,
-                                 bool early_weights, cudaStream_t s) {
+namespace {
+
+template <bool F8>
+cudaError_t tc_w2_impl(const void *a, const void *w2, const float *w2_scale, const float *a_scale,
+                       const int32_t *sorted_ids, const int32_t *expert_ids, const int32_t *n_post,
+                       const float *topk_weights, int P, int top_k, int E, int H, int I, int B,
+                       int cap, float *y_acc, int ksplit, int *status, bool early_weights,
+                       cudaStream_t s) {
+  constexpr int elt = F8 ? 1 : 2;
+  constexpr int bke = kBK * 2 / elt;
   CUtensorMap map_w;
-  cudaError_t err = make_weight_map(&map_w, w2, I, H, E);
+  cudaError_t err = make_weight_map(&map_w, w2, I, H, E, kTileM, elt);
   if (err != cudaSuccess) return err;
-  const int nk = (I + kBK - 1) / kBK;
+  const int nk = (I + bke - 1) / bke;
   TcArgs args{};
-  args.src = a;
+  args.src = static_cast<const uint16_t *>(a);
   args.src_rows = P;
   args.sorted_ids = sorted_ids;
   args.expert_ids = expert_ids;
@@ -1315,7 +1428,30 @@ cudaError_t launch_tc_w2_combine(const uint16_t *a, const uint16_t *w2, const in
   args.max_blocks = cap / B;
   args.early_weights = early_weights ? 1 : 0;
   args.n_pass = gemm2_passes(static_cast<long>(P / top_k) * H * 4, args.n_ctiles);
-  return launch_tc<1>(B, map_w, args, s);
+  args.row_scale = w2_scale;
+  args.col_scale = a_scale;
+  return launch_tc<1, F8>(B, map_w, args, s);
+}
+
+}  // namespace
+
+cudaError_t launch_tc_w2_combine(const uint16_t *a, const uint16_t *w2, const int32_t *sorted_ids,
+                                 const int32_t *expert_ids, const int32_t *n_post,
+                                 const float *topk_weights, int P, int top_k, int E, int H, int I,
+                                 int B, int cap, float *y_acc, int ksplit, int *status,
+                                 bool early_weights, cudaStream_t s) {
+  return tc_w2_impl<false>(a, w2, nullptr, nullptr, sorted_ids, expert_ids, n_post, topk_weights,
+                           P, top_k, E, H, I, B, cap, y_acc, ksplit, status, early_weights, s);
+}
+
+cudaError_t launch_tc_w2_combine_f8(const uint8_t *qa, const float *sa, const uint8_t *w2q,
+                                    const float *w2s, const int32_t *sorted_ids,
+                                    const int32_t *expert_ids, const int32_t *n_post,
+                                    const float *topk_weights, int P, int top_k, int E, int H,
+                                    int I, int B, int cap, float *y_acc, int ksplit, int *status,
+                                    bool early_weights, cudaStream_t s) {
+  return tc_w2_impl<true>(qa, w2q, w2s, sa, sorted_ids, expert_ids, n_post, topk_weights, P, top_k,
+                          E, H, I, B, cap, y_acc, ksplit, status, early_weights, s);
 }
 
 cudaError_t launch_selftest_timeout(int *status, int limit_ms, cudaStream_t s) {

@@ -48,14 +48,17 @@ long capacity(long P, int E, int B) {
 // Workspace regions, each 256-byte aligned.  The status word is always at
 // offset 0 so that moe_get_device_status can find it from the pointer alone.
 struct WsLayout {
-  size_t status, logits, ids, wts, sorted, eids, offsets, npost, hist, a, yacc, hacc, tcnt, total;
+  size_t status, logits, ids, wts, sorted, eids, offsets, npost, hist, a, qx, sx, qa, sa, yacc,
+      hacc, tcnt, total;
 };
 
 // Decode-sized batches (those the fused routing kernel serves) may split
 // GEMM 1's K range; they reserve its fp32 partial sums and tile counters.
 constexpr int kSplitMaxTokens = 256;
 
-WsLayout ws_layout(int M, int E, int top_k, int H, int I, int B) {
+// fp8: the E4M3 codes and row scales of x and a (before y_acc, so that the
+// span the routing kernel clears from y_acc on is the same in both layouts).
+WsLayout ws_layout(int M, int E, int top_k, int H, int I, int B, bool fp8 = false) {
   const long P = static_cast<long>(M) * top_k;
   const long cap = capacity(P, E, B);
   WsLayout w{};
@@ -75,6 +78,10 @@ WsLayout ws_layout(int M, int E, int top_k, int H, int I, int B) {
   w.npost = take(sizeof(int32_t));
   w.hist = take(sizeof(int32_t) * static_cast<size_t>(moe::align_hist_entries(P, E)));
   w.a = take(sizeof(uint16_t) * static_cast<size_t>(P) * I);
+  w.qx = take(fp8 ? static_cast<size_t>(M) * H : 0);
+  w.sx = take(fp8 ? sizeof(float) * static_cast<size_t>(M) : 0);
+  w.qa = take(fp8 ? static_cast<size_t>(P) * I : 0);
+  w.sa = take(fp8 ? sizeof(float) * static_cast<size_t>(P) : 0);
   w.yacc = take(sizeof(float) * static_cast<size_t>(M) * H);
   // h_acc and the tile counters directly follow y_acc: one span to clear
   const bool split = M <= kSplitMaxTokens;
@@ -261,6 +268,51 @@ moe_status_t run_gemm2(const uint16_t *a, const uint16_t *w2, const int32_t *sor
   }
 }
 
+// The FP8 grouped GEMMs run on the tensor cores only (E4M3 tiles of the
+// tcgen05 kernels); the K split follows the bf16 rule with 128-element stages.
+moe_status_t run_gemm1_f8(const uint8_t *qx, const float *sx, const uint8_t *w13,
+                          const float *w13s, const int32_t *sorted, const int32_t *eids,
+                          const int32_t *npost, int M, int top_k, int E, int H, int I, int B,
+                          uint16_t *a, float *h_acc, int *tile_cnt, int *status, bool prefetch,
+                          float *zero_dst, long zero_n, cudaStream_t s) {
+  const long P = static_cast<long>(M) * top_k;
+  const int cap = static_cast<int>(capacity(P, E, B));
+  const int ks = h_acc != nullptr ? pick_ksplit(M, E, top_k, (I + 127) / 128, (H + 127) / 128) : 1;
+  const double D = E * (1.0 - std::pow(1.0 - static_cast<double>(top_k) / E, M));
+  const int pf_experts = (prefetch && D >= 0.9 * E) ? E : 0;
+  return cuda_status(moe::launch_tc_w13_act_f8(qx, sx, w13, w13s, sorted, eids, npost,
+                                               static_cast<int>(P), top_k, E, H, I, B, cap, a, ks,
+                                               h_acc, tile_cnt, status, pf_experts, zero_dst,
+                                               zero_n, s));
+}
+
+moe_status_t run_gemm2_f8(const uint8_t *qa, const float *sa, const uint8_t *w2, const float *w2s,
+                          const int32_t *sorted, const int32_t *eids, const int32_t *npost,
+                          const float *wts, int M, int top_k, int E, int H, int I, int B,
+                          float *yacc, int *status, bool early_weights, cudaStream_t s) {
+  const long P = static_cast<long>(M) * top_k;
+  const int cap = static_cast<int>(capacity(P, E, B));
+  const int ks = pick_ksplit(M, E, top_k, (H + 255) / 256, (I + 127) / 128);
+  return cuda_status(moe::launch_tc_w2_combine_f8(qa, sa, w2, w2s, sorted, eids, npost, wts,
+                                                  static_cast<int>(P), top_k, E, H, I, B, cap,
+                                                  yacc, ks, status, early_weights, s));
+}
+
+size_t workspace_bytes(int M_max, int E, int top_k, int H, int I, int block_size_m, bool fp8) {
+  if (check_shapes(M_max, E, top_k, H, I) != MOE_OK) return 0;
+  if (block_size_m != 0 && !valid_block_size(block_size_m)) return 0;
+  // a smaller batch may reserve split-K scratch that M_max does not
+  const int M_split = std::min(M_max, kSplitMaxTokens);
+  auto need = [&](int B) {
+    return std::max(ws_layout(M_max, E, top_k, H, I, B, fp8).total,
+                    ws_layout(M_split, E, top_k, H, I, B, fp8).total);
+  };
+  if (block_size_m != 0) return need(block_size_m);
+  size_t best = 0;
+  for (int B : {16, 32, 64, 128, 256}) best = std::max(best, need(B));
+  return best;
+}
+
 }  // namespace
 
 extern "C" {
@@ -301,18 +353,12 @@ long moe_align_capacity(int M, int top_k, int E, int block_size_m) {
 }
 
 size_t moe_workspace_size(int M_max, int E, int top_k, int H, int I, int block_size_m) {
-  if (check_shapes(M_max, E, top_k, H, I) != MOE_OK) return 0;
-  if (block_size_m != 0 && !valid_block_size(block_size_m)) return 0;
-  // a smaller batch may reserve split-K scratch that M_max does not
-  const int M_split = std::min(M_max, kSplitMaxTokens);
-  auto need = [&](int B) {
-    return std::max(ws_layout(M_max, E, top_k, H, I, B).total,
-                    ws_layout(M_split, E, top_k, H, I, B).total);
-  };
-  if (block_size_m != 0) return need(block_size_m);
-  size_t best = 0;
-  for (int B : {16, 32, 64, 128, 256}) best = std::max(best, need(B));
-  return best;
+  return workspace_bytes(M_max, E, top_k, H, I, block_size_m, false);
+}
+
+size_t moe_workspace_size_fp8(int M_max, int E, int top_k, int H, int I, int block_size_m) {
+  if (block_size_m != 0 && !moe::tc_supports_block(block_size_m)) return 0;
+  return workspace_bytes(M_max, E, top_k, H, I, block_size_m, true);
 }
 
 moe_status_t moe_router_logits(const moe_bf16_t *x, const moe_bf16_t *w_router,
@@ -506,6 +552,130 @@ moe_status_t moe_route(const moe_bf16_t *x, const moe_bf16_t *w_router,
                    sorted_token_ids, expert_ids, expert_offsets, num_tokens_post_padded,
                    at<int32_t>(ws, L.hist), at<int>(ws, 0), nullptr, 0, &zeroed,
                    /*skip_sort=*/false, stream);
+}
+
+moe_status_t moe_quantize_rows_fp8(const moe_bf16_t *src, int R, int K, uint8_t *q,
+                                   float *scales, cudaStream_t stream) {
+  if (R < 0) return MOE_ERR_INVALID_ARG;
+  if (K < 16 || K > kMaxDim || K % 16 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (R == 0) return MOE_OK;
+  if (!src || !q || !scales || !aligned16(src) || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(moe::launch_quant_rows(src, R, K, q, scales, stream));
+}
+
+moe_status_t moe_grouped_gemm_w13_act_fp8(const uint8_t *qx, const float *x_scales,
+                                          const uint8_t *w13, const float *w13_scales,
+                                          const int32_t *sorted_token_ids,
+                                          const int32_t *expert_ids,
+                                          const int32_t *num_tokens_post_padded, int M,
+                                          int top_k, int E, int H, int I, int block_size_m,
+                                          moe_bf16_t *a, cudaStream_t stream) {
+  moe_status_t st = check_shapes(M, E, top_k, H, I);
+  if (st != MOE_OK) return st;
+  if (!moe::tc_supports_block(block_size_m)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0) return MOE_OK;
+  if (!qx || !x_scales || !w13 || !w13_scales || !sorted_token_ids || !expert_ids ||
+      !num_tokens_post_padded || !a)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(qx) || !aligned16(w13)) return MOE_ERR_INVALID_ARG;
+  return run_gemm1_f8(qx, x_scales, w13, w13_scales, sorted_token_ids, expert_ids,
+                      num_tokens_post_padded, M, top_k, E, H, I, block_size_m, a, nullptr,
+                      nullptr, lib_status(), /*prefetch=*/false, /*zero_dst=*/nullptr, 0, stream);
+}
+
+moe_status_t moe_grouped_gemm_w2_combine_fp8(const uint8_t *qa, const float *a_scales,
+                                             const uint8_t *w2, const float *w2_scales,
+                                             const int32_t *sorted_token_ids,
+                                             const int32_t *expert_ids,
+                                             const int32_t *num_tokens_post_padded,
+                                             const float *topk_weights,
+                                             const moe_bf16_t *residual, int M, int top_k,
+                                             int E, int H, int I, int block_size_m,
+                                             moe_bf16_t *y, void *ws, size_t ws_bytes,
+                                             cudaStream_t stream) {
+  moe_status_t st = check_shapes(M, E, top_k, H, I);
+  if (st != MOE_OK) return st;
+  if (!moe::tc_supports_block(block_size_m)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0) return MOE_OK;
+  if (!qa || !a_scales || !w2 || !w2_scales || !sorted_token_ids || !expert_ids ||
+      !num_tokens_post_padded || !topk_weights || !y || !ws)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(qa) || !aligned16(w2) || !aligned16(y) || (residual && !aligned16(residual)))
+    return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(M, E, top_k, H, I, block_size_m);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  float *yacc = at<float>(ws, L.yacc);
+  cudaError_t e = cudaMemsetAsync(yacc, 0, sizeof(float) * static_cast<size_t>(M) * H, stream);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  st = run_gemm2_f8(qa, a_scales, w2, w2_scales, sorted_token_ids, expert_ids,
+                    num_tokens_post_padded, topk_weights, M, top_k, E, H, I, block_size_m, yacc,
+                    at<int>(ws, 0), /*early_weights=*/false, stream);
+  if (st != MOE_OK) return st;
+  return cuda_status(moe::launch_finalize(yacc, residual, M, H, y, stream));
+}
+
+moe_status_t moe_forward_fp8(const moe_bf16_t *x, const moe_bf16_t *w_router,
+                             const moe_bf16_t *router_logits, const float *router_bias,
+                             const uint8_t *w13, const float *w13_scales, const uint8_t *w2,
+                             const float *w2_scales, const moe_bf16_t *residual, int M, int E,
+                             int top_k, int H, int I, int renormalize, int block_size_m,
+                             moe_bf16_t *y, int32_t *topk_ids_out, float *topk_weights_out,
+                             moe_bf16_t *router_logits_out, void *ws, size_t ws_bytes,
+                             cudaStream_t stream) {
+  moe_status_t st = check_shapes(M, E, top_k, H, I);
+  if (st != MOE_OK) return st;
+  if (block_size_m != 0 && !moe::tc_supports_block(block_size_m)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if ((w_router == nullptr) == (router_logits == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (router_bias && !w_router) return MOE_ERR_INVALID_ARG;
+  if (M == 0) return MOE_OK;
+  if (!x || !w13 || !w13_scales || !w2 || !w2_scales || !y || !ws) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w13) || !aligned16(w2) || !aligned16(y) ||
+      (residual && !aligned16(residual)) || (w_router && !aligned16(w_router)))
+    return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return MOE_ERR_INVALID_ARG;
+  const int B = block_size_m != 0 ? block_size_m : moe_pick_block_size(M, E, top_k, H, I);
+  const WsLayout L = ws_layout(M, E, top_k, H, I, B, /*fp8=*/true);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+
+  const long P = static_cast<long>(M) * top_k;
+  int *status = at<int>(ws, L.status);
+  int32_t *ids = topk_ids_out ? topk_ids_out : at<int32_t>(ws, L.ids);
+  float *wts = topk_weights_out ? topk_weights_out : at<float>(ws, L.wts);
+  uint16_t *logits_ws = router_logits_out ? router_logits_out : at<uint16_t>(ws, L.logits);
+  int32_t *sorted = at<int32_t>(ws, L.sorted);
+  int32_t *eids = at<int32_t>(ws, L.eids);
+  int32_t *offs = at<int32_t>(ws, L.offsets);
+  int32_t *npost = at<int32_t>(ws, L.npost);
+  float *yacc = at<float>(ws, L.yacc);
+  uint8_t *qx = at<uint8_t>(ws, L.qx);
+  float *sx = at<float>(ws, L.sx);
+  uint8_t *qa = at<uint8_t>(ws, L.qa);
+  float *sa = at<float>(ws, L.sa);
+  const long yn = static_cast<long>(M) * H;
+  const bool want_split =
+      L.hacc != L.tcnt && pick_ksplit(M, E, top_k, (I + 127) / 128, (H + 127) / 128) > 1;
+  const long zn = want_split ? static_cast<long>((L.total - L.yacc) / sizeof(float)) : yn;
+  bool zeroed = false;
+  st = run_route(x, w_router, router_logits, router_bias, M, E, top_k, H, renormalize, B,
+                 logits_ws, ids, wts, sorted, eids, offs, npost, at<int32_t>(ws, L.hist), status,
+                 yacc, zn, &zeroed, /*skip_sort=*/P * 4 <= E, stream);
+  if (st != MOE_OK) return st;
+  st = cuda_status(moe::launch_quant_rows(x, M, H, qx, sx, stream));
+  if (st != MOE_OK) return st;
+  uint16_t *a = at<uint16_t>(ws, L.a);
+  const bool split_ok = zeroed && want_split;
+  st = run_gemm1_f8(qx, sx, w13, w13_scales, sorted, eids, npost, M, top_k, E, H, I, B, a,
+                    split_ok ? at<float>(ws, L.hacc) : nullptr,
+                    split_ok ? at<int>(ws, L.tcnt) : nullptr, status, /*prefetch=*/true,
+                    zeroed ? nullptr : yacc, yn, stream);
+  if (st != MOE_OK) return st;
+  st = cuda_status(moe::launch_quant_rows(a, static_cast<int>(P), I, qa, sa, stream));
+  if (st != MOE_OK) return st;
+  st = run_gemm2_f8(qa, sa, w2, w2_scales, sorted, eids, npost, wts, M, top_k, E, H, I, B, yacc,
+                    status, /*early_weights=*/true, stream);
+  if (st != MOE_OK) return st;
+  return cuda_status(moe::launch_finalize(yacc, residual, M, H, y, stream));
 }
 
 moe_status_t moe_selftest_device_timeout(void *ws, size_t ws_bytes, int limit_ms,

@@ -156,6 +156,26 @@ cudaError_t launch_tc_w2_combine(const uint16_t *a, const uint16_t *w2, const in
                                  int B, int cap, float *y_acc, int ksplit, int *status,
                                  bool early_weights, cudaStream_t s);
 
+// FP8 (E4M3) versions of S3 / S4: codes [rows, K] with one fp32 scale per row
+// on both sides (w13s [E, 2I], sx [M]; w2s [E, H], sa [P]).  GEMM 1 writes a in
+// bf16 as the bf16 path does; the caller quantizes it for GEMM 2.
+cudaError_t launch_tc_w13_act_f8(const uint8_t *qx, const float *sx, const uint8_t *w13q,
+                                 const float *w13s, const int32_t *sorted_ids,
+                                 const int32_t *expert_ids, const int32_t *n_post, int P, int top_k,
+                                 int E, int H, int I, int B, int cap, uint16_t *a, int ksplit,
+                                 float *h_acc, int *tile_cnt, int *status, int pf_experts,
+                                 float *zero_dst, long zero_n, cudaStream_t s);
+cudaError_t launch_tc_w2_combine_f8(const uint8_t *qa, const float *sa, const uint8_t *w2q,
+                                    const float *w2s, const int32_t *sorted_ids,
+                                    const int32_t *expert_ids, const int32_t *n_post,
+                                    const float *topk_weights, int P, int top_k, int E, int H,
+                                    int I, int B, int cap, float *y_acc, int ksplit, int *status,
+                                    bool early_weights, cudaStream_t s);
+// Per-row dynamic E4M3 quantization of a bf16 [R, K] matrix (K a multiple of
+// 16): s[r] = amax / 448 (1 for a zero row), q[r, :] = e4m3(src[r, :] / s[r]).
+cudaError_t launch_quant_rows(const uint16_t *src, int R, int K, uint8_t *q, float *s,
+                              cudaStream_t st);
+
 // S0 on the tensor cores: logits [M,E] = bf16(x . w_router^T + bias), blocks of 128 tokens.
 // One CTA whose bounded wait on an mbarrier nothing completes gives up after
 // about limit_ms ms and records the timeout status (self-test of that path).

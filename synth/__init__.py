@@ -16,9 +16,13 @@ SGLang issue page):
   tail      M in {1,64,8192},        E=60,  k=4, H=2048, I=1408, logits ~ N(0,1) given
 
 Distributions: weights W_r, W13, W2 ~ N(0, 0.02), x ~ N(0, 1), given logits
-~ N(0, 1); each drawn in fp32 and rounded to bf16.  Seeds:
-s = 1_000_003 * cfg + 1_009 * layer + tensor_idx (W_r:0, W13:1, W2:2, x:3,
-logits:4; the toy config uses s = tensor_idx).  Timing repetitions draw x with
+~ N(0, 1); each drawn in fp32 and rounded to bf16.  FP8 expert weights
+(layer_weights_fp8) are drawn as codes directly: E4M3 codes of N(0, 64^2)
+values (torch's float8_e4m3fn cast of a clamped fp32 draw) with one fp32 row
+scale 0.02/64 * U(0.8, 1.2), so the weights they stand for have about the
+bf16 weights' spread.  Seeds: s = 1_000_003 * cfg + 1_009 * layer +
+tensor_idx (W_r:0, W13:1, W2:2, x:3, logits:4, W13 scales:5, W2 scales:6;
+the toy config uses s = tensor_idx).  Timing repetitions draw x with
 seed s + 100 * rep so that the routed expert set changes between reps.
 """
 from __future__ import annotations
@@ -27,7 +31,8 @@ import dataclasses
 
 import torch
 
-TENSOR_IDX = {"w_router": 0, "w13": 1, "w2": 2, "x": 3, "logits": 4}
+TENSOR_IDX = {"w_router": 0, "w13": 1, "w2": 2, "x": 3, "logits": 4, "w13_scale": 5,
+              "w2_scale": 6}
 
 
 @dataclasses.dataclass(frozen=True)
@@ -91,18 +96,48 @@ def zipf_router_bias(E: int, s: float, seed: int = 1) -> torch.Tensor:
     return (-s * torch.log(rank)).to(torch.float32)
 
 
+def router_weights(w: Workload, layer: int = 0, device="cpu") -> dict:
+    """W_r [E,H] bf16 (None when logits are given) and the router bias [E] (or None)."""
+    out = {"w_router": None, "router_bias": None}
+    if not w.logits_given:
+        out["w_router"] = normal_bf16((w.E, w.H), 0.02, seed_of(w.cfg, layer, "w_router"), device)
+    if w.zipf_s > 0:
+        out["router_bias"] = zipf_router_bias(w.E, w.zipf_s).to(device)
+    return out
+
+
 def layer_weights(w: Workload, layer: int = 0, device="cpu") -> dict:
     """W_r [E,H] (unless logits are given), W13 [E,2I,H], W2 [E,H,I] (bf16), bias [E] or None."""
     out = {
         "w13": normal_bf16((w.E, 2 * w.I, w.H), 0.02, seed_of(w.cfg, layer, "w13"), device),
         "w2": normal_bf16((w.E, w.H, w.I), 0.02, seed_of(w.cfg, layer, "w2"), device),
-        "w_router": None,
-        "router_bias": None,
     }
-    if not w.logits_given:
-        out["w_router"] = normal_bf16((w.E, w.H), 0.02, seed_of(w.cfg, layer, "w_router"), device)
-    if w.zipf_s > 0:
-        out["router_bias"] = zipf_router_bias(w.E, w.zipf_s).to(device)
+    out.update(router_weights(w, layer, device))
+    return out
+
+
+def fp8_codes(shape, seed: int, device="cpu") -> torch.Tensor:
+    """uint8 E4M3 bit patterns of N(0, 64^2) draws (clamped to +-448 before the cast)."""
+    g = _gen(seed, device)
+    t = torch.randn(*shape, generator=g, device=device, dtype=torch.float32).mul_(64.0)
+    return t.clamp_(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+
+
+def row_scales(shape, seed: int, device="cpu") -> torch.Tensor:
+    """fp32 per-row scales 0.02/64 * U(0.8, 1.2)."""
+    g = _gen(seed, device)
+    u = torch.rand(*shape, generator=g, device=device, dtype=torch.float32)
+    return u.mul_(0.4).add_(0.8).mul_(0.02 / 64.0)
+
+
+def layer_weights_fp8(w: Workload, layer: int = 0, device="cpu") -> dict:
+    """E4M3 expert weights: W13 codes [E,2I,H] + scales [E,2I], W2 codes [E,H,I] + scales [E,H]
+    (uint8 / fp32); W_r and the bias as layer_weights draws them."""
+    out = router_weights(w, layer, device)
+    out["w13"] = fp8_codes((w.E, 2 * w.I, w.H), seed_of(w.cfg, layer, "w13"), device)
+    out["w13_scale"] = row_scales((w.E, 2 * w.I), seed_of(w.cfg, layer, "w13_scale"), device)
+    out["w2"] = fp8_codes((w.E, w.H, w.I), seed_of(w.cfg, layer, "w2"), device)
+    out["w2_scale"] = row_scales((w.E, w.H), seed_of(w.cfg, layer, "w2_scale"), device)
     return out
 
 

@@ -147,6 +147,62 @@ def test_step_argument_checks(lib):
     assert lib.moe_selftest_device_timeout(FAKE, 16, 10, S) == INVALID   # smaller than the status block
 
 
+def test_fp8_sizes(lib):
+    n = moe.moe_workspace_size(64, 128, 8, 2048, 768, 16)
+    n8 = moe.moe_workspace_size_fp8(64, 128, 8, 2048, 768, 16)
+    # plus x codes [64, 2048], a codes [512, 768] and their row scales
+    assert n8 >= n + 64 * 2048 + 512 * 768 + (64 + 512) * 4
+    assert lib.moe_workspace_size_fp8(64, 128, 8, 2048, 768, 24) == 0   # not a tensor-core tile
+    assert lib.moe_workspace_size_fp8(64, 128, 8, 2040, 768, 16) == 0
+    assert moe.moe_workspace_size_fp8(64, 128, 8, 2048, 768, 0) >= n8
+
+
+@needs_no_gpu
+def test_fp8_argument_checks(lib):
+    q = lib.moe_quantize_rows_fp8
+    assert q(FAKE, 0, 64, FAKE, FAKE, S) == OK
+    assert q(FAKE, -1, 64, FAKE, FAKE, S) == INVALID
+    assert q(FAKE, 4, 60, FAKE, FAKE, S) == SHAPE            # K not a multiple of 16
+    assert q(NULL, 4, 64, FAKE, FAKE, S) == INVALID
+    assert q(FAKE, 4, 64, FAKE_MIS, FAKE, S) == INVALID      # misaligned codes
+    assert q(FAKE, 4, 64, FAKE, NULL, S) == INVALID
+    g1 = lib.moe_grouped_gemm_w13_act_fp8
+    assert g1(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2, 8, 64, 32, 24, FAKE, S) == SHAPE
+    assert g1(FAKE, NULL, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2, 8, 64, 32, 16, FAKE, S) == INVALID
+    assert g1(FAKE, FAKE, FAKE, NULL, FAKE, FAKE, FAKE, 4, 2, 8, 64, 32, 16, FAKE, S) == INVALID
+    assert g1(FAKE_MIS, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2, 8, 64, 32, 16, FAKE, S) == INVALID
+    g2 = lib.moe_grouped_gemm_w2_combine_fp8
+    assert g2(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, NULL, 4, 2, 8, 64, 32, 16, FAKE, FAKE,
+              64, S) == WS_SMALL
+    assert g2(FAKE, FAKE, FAKE, NULL, FAKE, FAKE, FAKE, FAKE, NULL, 4, 2, 8, 64, 32, 16, FAKE, FAKE,
+              1 << 30, S) == INVALID
+    assert g2(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, NULL, 4, 2, 8, 64, 32, 1, FAKE, FAKE,
+              1 << 30, S) == SHAPE
+    f = lib.moe_forward_fp8
+    args = dict(x=FAKE, wr=FAKE, lg=NULL, bias=NULL, w13=FAKE, s13=FAKE, w2=FAKE, s2=FAKE, res=NULL,
+                M=4, E=8, k=2, H=64, I=32, renorm=1, B=16, y=FAKE, ids=NULL, wts=NULL, lgo=NULL,
+                ws=FAKE, wsb=1 << 40)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return f(a["x"], a["wr"], a["lg"], a["bias"], a["w13"], a["s13"], a["w2"], a["s2"],
+                 a["res"], a["M"], a["E"], a["k"], a["H"], a["I"], a["renorm"], a["B"], a["y"],
+                 a["ids"], a["wts"], a["lgo"], a["ws"], a["wsb"], S)
+
+    assert call(M=0) == OK
+    assert call(M=-1) == INVALID
+    assert call(B=48) == SHAPE                  # the FP8 GEMMs tile 16..256 powers of two only
+    assert call(H=56) == SHAPE
+    assert call(lg=FAKE) == INVALID
+    assert call(s13=NULL) == INVALID
+    assert call(s2=NULL) == INVALID
+    assert call(w2=FAKE_MIS) == INVALID
+    assert call(ws=FAKE_MIS) == INVALID
+    need = moe.moe_workspace_size_fp8(4, 8, 2, 64, 32, 16)
+    assert call(wsb=need - 1) == WS_SMALL
+    assert need > moe.moe_workspace_size(4, 8, 2, 64, 32, 16)
+
+
 def test_product_path_fails_loudly_without_the_library(monkeypatch, tmp_path):
     from mixture_experts_layer_renorm_gb300 import _build
     monkeypatch.setattr(_build, "LIB_PATH", str(tmp_path / "missing.so"))

@@ -274,7 +274,9 @@ def run_forward(x, w13, w2, k, *, lg=None, wr=None, bias=None, res=None, B=0, re
 
 @pytest.mark.parametrize("M,E,k,H,I,B", [(3, 4, 2, 128, 64, 16), (1, 60, 4, 2048, 1408, 0),
                                          (64, 60, 4, 2048, 1408, 0), (21, 9, 9, 64, 48, 0),
-                                         (50, 24, 5, 96, 32, 8), (300, 64, 6, 256, 128, 0)])
+                                         (50, 24, 5, 96, 32, 8), (300, 64, 6, 256, 128, 0),
+                                         # both GEMMs split K = 4 stages three ways
+                                         (6, 128, 8, 208, 208, 0)])
 @pytest.mark.parametrize("renorm", [True, False])
 def test_forward_given_logits(M, E, k, H, I, B, renorm):
     x, w13, w2, lg = layer_case(M, E, k, H, I, seed=3 * M + E)

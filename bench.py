@@ -71,6 +71,18 @@ def gemm1_bytes(w, M, D):
     return D * 2 * w.I * w.H * 2 + M * w.H * 2 + M * w.top_k * w.I * 2
 
 
+def layer_bytes_fp8(w, M, D):
+    """layer_bytes with E4M3 expert weights: one byte per weight plus one fp32
+    scale per weight row (2I rows of W13, H rows of W2 per expert)."""
+    return layer_bytes(w, M, D) - D * 3 * w.H * w.I * 2 + D * (3 * w.H * w.I + (2 * w.I + w.H) * 4)
+
+
+def gemm1_bytes_fp8(w, M, D):
+    """Grouped GEMM 1 on E4M3 codes: W13 codes and row scales of the touched
+    experts, the M quantized rows of x and their scales, a written in bf16."""
+    return D * 2 * w.I * (w.H + 4) + M * (w.H + 4) + M * w.top_k * w.I * 2
+
+
 def layer_flops(w, M):
     return M * w.top_k * 6 * w.H * w.I + (0 if w.logits_given else 2 * M * w.H * w.E)
 
@@ -238,10 +250,11 @@ def barrier(world: int):
 class Layer:
     """Device-resident weights, inputs and buffers of one workload point."""
 
-    def __init__(self, moe, w, M, n_inputs, device, layer=0):
-        self.w, self.M = w, M
-        wt = synth.layer_weights(w, layer=layer, device=device)
+    def __init__(self, moe, w, M, n_inputs, device, layer=0, fp8=False):
+        self.w, self.M, self.fp8 = w, M, fp8
+        wt = (synth.layer_weights_fp8 if fp8 else synth.layer_weights)(w, layer=layer, device=device)
         self.wr, self.bias, self.w13, self.w2 = wt["w_router"], wt["router_bias"], wt["w13"], wt["w2"]
+        self.s13, self.s2 = wt.get("w13_scale"), wt.get("w2_scale")
         self.inputs = [synth.layer_input(w, M, rep=r, device=device) for r in range(n_inputs)]
         self.B = w.block_size_m or moe.moe_pick_block_size(M, w.E, w.top_k, w.H, w.I)
         P = M * w.top_k
@@ -256,7 +269,14 @@ class Layer:
         self.npost = torch.empty((1,), **i32)
         self.a = torch.empty((P, w.I), dtype=torch.bfloat16, device=device)
         self.y = torch.empty((M, w.H), dtype=torch.bfloat16, device=device)
-        self.ws = moe.Workspace(M, w.E, w.top_k, w.H, w.I, 0, device=device)
+        self.ws = moe.Workspace(M, w.E, w.top_k, w.H, w.I, 0, device=device, fp8=fp8)
+        if fp8:
+            self.qx = torch.empty((M, w.H), dtype=torch.uint8, device=device)
+            self.sx = torch.empty((M,), dtype=torch.float32, device=device)
+            self.qa = torch.empty((P, w.I), dtype=torch.uint8, device=device)
+            self.sa = torch.empty((P,), dtype=torch.float32, device=device)
+        self.phases = (["route", "quant_x", "gemm1_act", "quant_a", "gemm2_combine"] if fp8
+                       else ["route", "gemm1_act", "gemm2_combine"])
 
     def kernels_per_step(self):
         """Our kernels per step: routing (one fused launch up to 256 tokens, else
@@ -265,32 +285,57 @@ class Layer:
             route = 1
         else:
             route = (0 if self.w.logits_given else 1) + 1 + (1 if self.M * self.w.top_k <= 16384 else 2)
-        return route + 1 + 2
+        # E4M3 weights: two more launches, the per-row quantizations of x and a
+        return route + 1 + 2 + (2 if self.fp8 else 0)
 
     def step(self, moe, i, stream, ev):
-        """One pass of the layer through the step entry points; ev[0..3] bracket
-        routing (S0-S2), GEMM 1 + activation and GEMM 2 + combine."""
+        """One pass of the layer through the step entry points; ev[0..len(phases)]
+        bracket the phases (routing S0-S2, GEMM 1 + activation, GEMM 2 +
+        combine, and with E4M3 weights the quantizations of x and a)."""
         w, inp = self.w, self.inputs[i]
         x = inp["x"]
+        res = x if w.residual else None
         ev[0].record(stream)
         moe.moe_route(w.top_k, self.B, self.ids, self.wts, self.sorted, self.eids, self.offs,
                       self.npost, self.ws, x=None if w.logits_given else x,
                       w_router=self.wr, router_logits=inp["router_logits"], router_bias=self.bias,
                       renormalize=w.renormalize, stream=stream)
         ev[1].record(stream)
+        if self.fp8:
+            moe.moe_quantize_rows_fp8(x, self.qx, self.sx, stream=stream)
+            ev[2].record(stream)
+            moe.moe_grouped_gemm_w13_act_fp8(self.qx, self.sx, self.w13, self.s13, self.sorted,
+                                             self.eids, self.npost, w.top_k, self.B, self.a,
+                                             stream=stream)
+            ev[3].record(stream)
+            moe.moe_quantize_rows_fp8(self.a, self.qa, self.sa, stream=stream)
+            ev[4].record(stream)
+            moe.moe_grouped_gemm_w2_combine_fp8(self.qa, self.sa, self.w2, self.s2, self.sorted,
+                                                self.eids, self.npost, self.wts, w.top_k, self.B,
+                                                self.y, self.ws, residual=res, stream=stream)
+            ev[5].record(stream)
+            return
         moe.moe_grouped_gemm_w13_act(x, self.w13, self.sorted, self.eids, self.npost, w.top_k,
                                      self.B, self.a, stream=stream)
         ev[2].record(stream)
         moe.moe_grouped_gemm_w2_combine(self.a, self.w2, self.sorted, self.eids, self.npost,
                                         self.wts, w.top_k, self.B, self.y, self.ws,
-                                        residual=x if w.residual else None, stream=stream)
+                                        residual=res, stream=stream)
         ev[3].record(stream)
 
     def forward(self, moe, i, stream):
         """One pass of the layer through the whole-layer entry point moe_forward
-        (what the timed steps run: its kernels may overlap each other's launch)."""
+        (moe_forward_fp8 for E4M3 weights; what the timed steps run: its
+        kernels may overlap each other's launch)."""
         w, inp = self.w, self.inputs[i]
         x = inp["x"]
+        if self.fp8:
+            moe.moe_forward_fp8(x, self.w13, self.s13, self.w2, self.s2, w.top_k, self.y, self.ws,
+                                w_router=None if w.logits_given else self.wr,
+                                router_logits=inp["router_logits"], router_bias=self.bias,
+                                residual=x if w.residual else None, renormalize=w.renormalize,
+                                block_size_m=self.B, stream=stream)
+            return
         moe.moe_forward(x, self.w13, self.w2, w.top_k, self.y, self.ws,
                         w_router=None if w.logits_given else self.wr,
                         router_logits=inp["router_logits"], router_bias=self.bias,
@@ -316,13 +361,13 @@ class Layer:
                 "experts_without_pairs": int((n == 0).sum())}
 
 
-def run_point(moe, w, M, steps, warmup, device, stream, flush, L=None):
+def run_point(moe, w, M, steps, warmup, device, stream, flush, L=None, fp8=False):
     """Timed steps: moe_forward with CUDA events around each step only.  Then a
     breakdown pass through the step entry points with events between routing,
     GEMM 1 and GEMM 2 (events between kernels keep them from overlapping, so
     the breakdown is not the timed number)."""
     if L is None:
-        L = Layer(moe, w, M, warmup + steps, device)
+        L = Layer(moe, w, M, warmup + steps, device, fp8=fp8)
     # inputs are drawn on the default stream; the steps run on `stream`
     torch.cuda.synchronize()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -344,7 +389,8 @@ def run_point(moe, w, M, steps, warmup, device, stream, flush, L=None):
         torch.cuda.nvtx.range_pop()
     step_ms = [evs[i][0].elapsed_time(evs[i][1]) for i in range(warmup, warmup + steps)]
     nb = min(steps, 10)
-    bev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(nb)]
+    ne = len(L.phases) + 1
+    bev = [[torch.cuda.Event(enable_timing=True) for _ in range(ne)] for _ in range(nb)]
     with torch.cuda.stream(stream):
         torch.cuda.nvtx.range_push(f"breakdown M={M}")
         for i in range(nb):
@@ -352,7 +398,7 @@ def run_point(moe, w, M, steps, warmup, device, stream, flush, L=None):
             L.step(moe, warmup + i, stream, bev[i])
         stream.synchronize()
         torch.cuda.nvtx.range_pop()
-    per = [[bev[i][j].elapsed_time(bev[i][j + 1]) for j in range(3)] for i in range(nb)]
+    per = [[bev[i][j].elapsed_time(bev[i][j + 1]) for j in range(ne - 1)] for i in range(nb)]
     D = [L.distinct_experts(moe, i, stream) for i in range(warmup, warmup + steps)]
     return L, per, step_ms, D
 
@@ -655,6 +701,53 @@ def prefill_point(moe, args, device, stream, flush, peaks, world):
     return out
 
 
+def fp8_point(moe, args, device, stream, flush, peaks, world, cfg_name, M):
+    """The layer with E4M3 expert weights (moe_forward_fp8) on one workload
+    point: tokens/s and the roofline of grouped GEMM 1 against HBM (decode) or
+    the FP8 tensor peak (prefill), taken as the measured bf16 peak times the
+    nominal FP8/bf16 ratio 2 (4.5 / 2.25 PFLOP/s dense)."""
+    w = synth.WORKLOADS[WORKLOAD_CFG[cfg_name]]
+    steps = max(5, args.steps // 2)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(device) as clk:
+        L, per, step_ms, D = run_point(moe, w, M, steps, args.warmup, device, stream, flush, fp8=True)
+    total = max_over_ranks(sum(step_ms), world, device)
+    ms = total / steps
+    g1 = L.phases.index("gemm1_act")
+    gemm1_ms = statistics.mean(p[g1] for p in per)
+    f8_tflops = 2.0 * peaks["bf16_tflops"]
+    g1_flops = gemm1_flops(w, M)
+    g1_bytes = statistics.mean(gemm1_bytes_fp8(w, M, d) for d in D)
+    ridge = f8_tflops * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if g1_flops / g1_bytes > ridge:
+        roof = {"bound": "tensor", "achieved": round(g1_flops / (gemm1_ms / 1e3) / 1e12, 1),
+                "peak": f8_tflops, "unit": "TFLOP/s", "algorithmic_flops": int(g1_flops),
+                "peak_source": f"{peaks['source']} bf16 x 2 (nominal FP8/bf16 ratio)"}
+    else:
+        roof = {"bound": "hbm", "achieved": round(g1_bytes / (gemm1_ms / 1e3) / 1e9, 1),
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "algorithmic_bytes": int(g1_bytes),
+                "peak_source": peaks["source"]}
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    lay_bytes = statistics.mean(layer_bytes_fp8(w, M, d) for d in D)
+    out = {
+        "workload": f"{w.name}_fp8_m{M}", "M": M, "block_size_m": L.B, "dtype": "e4m3 x e4m3 -> f32",
+        "value": round(world * M / (ms / 1e3), 1), "unit": UNIT, "ms_per_layer": round(ms, 5),
+        "layer_hbm_frac": round(lay_bytes / (ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+        "layer_tc_frac_fp8": round(layer_flops(w, M) / (ms / 1e3) / 1e12 / f8_tflops, 4),
+        "roofline": dict({"kernel": "grouped GEMM 1 (E4M3) + SiLU-and-mul"}, **roof,
+                         ms=round(gemm1_ms, 5)),
+        "step_breakdown_ms": {k: round(statistics.mean(p[j] for p in per), 5)
+                              for j, k in enumerate(L.phases)},
+        "distinct_experts": round(statistics.mean(D), 2),
+        "steps": steps, "warmup": args.warmup,
+        "gpu_launches": L.kernels_per_step() * steps,
+        "clocks": clk.summary(),
+    }
+    del L
+    return out
+
+
 def ours(args):
     import mixture_experts_layer_renorm_gb300 as moe
     world, rank, local = dist_env()
@@ -757,6 +850,14 @@ def ours(args):
     if args.workload == "decode" and not args.no_prefill:
         prefill = prefill_point(moe, args, device, stream, flush, peaks, world)
 
+    # the same two points with E4M3 expert weights (moe_forward_fp8)
+    fp8 = None
+    if args.workload == "decode" and not args.no_fp8:
+        fp8 = {"decode": fp8_point(moe, args, device, stream, flush, peaks, world, "decode", M)}
+        if not args.no_prefill:
+            fp8["prefill"] = fp8_point(moe, args, device, stream, flush, peaks, world, "prefill",
+                                       max(synth.WORKLOADS[WORKLOAD_CFG["prefill"]].Ms))
+
     if rank != 0:
         return
     cpu = None if (world > 1 or args.no_cpu_baseline) else cpu_baseline(w, L)
@@ -797,6 +898,7 @@ def ours(args):
         "points": points,
         "one_kernel_layer": one_kernel,
         "prefill": prefill,
+        "fp8": fp8,
     }
     print(json.dumps(line), flush=True)
 
@@ -864,6 +966,8 @@ def main(argv=None):
     ap.add_argument("--flush-mb", type=int, default=512)
     ap.add_argument("--no-points", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-fp8", action="store_true",
+                    help="skip the E4M3-weight points of the decode run")
     ap.add_argument("--no-prefill", action="store_true",
                     help="decode workload: skip the prefill point (M = 16384) in the same run")
     ap.add_argument("--ref-tokens", type=int, default=64)

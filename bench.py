@@ -392,6 +392,9 @@ def run_point(moe, w, M, steps, warmup, device, stream, flush, L=None, fp8=False
     ne = len(L.phases) + 1
     bev = [[torch.cuda.Event(enable_timing=True) for _ in range(ne)] for _ in range(nb)]
     with torch.cuda.stream(stream):
+        # one untimed pass first: the first call of a step entry point pays
+        # one-time host work (symbol lookups) inside its events
+        L.step(moe, warmup, stream, [torch.cuda.Event(enable_timing=True) for _ in range(ne)])
         torch.cuda.nvtx.range_push(f"breakdown M={M}")
         for i in range(nb):
             flush.zero_()
@@ -767,6 +770,13 @@ def ours(args):
     if w.layers > 1:
         ours_stack(args, moe, w, M, device, stream, flush, world, rank, peaks)
         return
+    if args.fp8:
+        # one point with E4M3 expert weights (the fp8 entry of the default
+        # decode line, for any single-layer workload and M)
+        out = fp8_point(moe, args, device, stream, flush, peaks, world, args.workload, M)
+        if rank == 0:
+            print(json.dumps(out), flush=True)
+        return
 
     L = Layer(moe, w, M, args.warmup + args.steps, device)
     # the timed region: K steps, barrier + synchronize on both sides
@@ -966,6 +976,8 @@ def main(argv=None):
     ap.add_argument("--flush-mb", type=int, default=512)
     ap.add_argument("--no-points", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fp8", action="store_true",
+                    help="time only the workload's layer with E4M3 expert weights (moe_forward_fp8)")
     ap.add_argument("--no-fp8", action="store_true",
                     help="skip the E4M3-weight points of the decode run")
     ap.add_argument("--no-prefill", action="store_true",

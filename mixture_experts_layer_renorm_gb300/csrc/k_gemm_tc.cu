@@ -959,13 +959,20 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
           const uint32_t other[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
           const uint32_t *mine = is_gate ? lo : hi;
           const int cbase = j0 + (is_gate ? 0 : 16);
+          // all 16 values first, then the stores: sixteen independent chains
+          // (exp, reciprocal) that the scheduler interleaves, where a value
+          // computed under its store's condition costs a full chain each
+          uint16_t res[16];
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) {
             const float o = __uint_as_float((jj & 1) ? (other[jj >> 1] & 0xFFFF0000u) : (other[jj >> 1] << 16));
             const float m = __uint_as_float(mine[jj]);
+            res[jj] = silu_mul_bf16(is_gate ? m : o, is_gate ? o : m);
+          }
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
             const int p = dst_row[cbase + jj];
-            if (valid && p >= 0)
-              out16[(size_t)p * R_out + chn] = is_gate ? silu_mul_bf16(m, o) : silu_mul_bf16(o, m);
+            if (valid && p >= 0) out16[(size_t)p * R_out + chn] = res[jj];
           }
         }
       } else if (MODE == 0) {
@@ -985,18 +992,25 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
               up[jj] = __float_as_uint(__uint_as_float(up[jj]) * su * dst_w[j0 + jj]);
             }
           }
+          if (ksplit > 1) {
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) {
-            const int p = dst_row[j0 + jj];
-            if (valid && p >= 0) {
-              if (ksplit > 1) {
+            for (int jj = 0; jj < 16; ++jj) {
+              const int p = dst_row[j0 + jj];
+              if (valid && p >= 0) {
                 // a partial sum over this split's K range: add it up in fp32
                 atomicAdd(h_acc + (size_t)p * 2 * R_out + chn, __uint_as_float(gt[jj]));
                 atomicAdd(h_acc + (size_t)p * 2 * R_out + R_out + chn, __uint_as_float(up[jj]));
-              } else {
-                out16[(size_t)p * R_out + chn] =
-                    silu_mul_bf16(__uint_as_float(gt[jj]), __uint_as_float(up[jj]));
               }
+            }
+          } else {
+            uint16_t res[16];  // the values first, then the stores (as above)
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj)
+              res[jj] = silu_mul_bf16(__uint_as_float(gt[jj]), __uint_as_float(up[jj]));
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+              const int p = dst_row[j0 + jj];
+              if (valid && p >= 0) out16[(size_t)p * R_out + chn] = res[jj];
             }
           }
         }

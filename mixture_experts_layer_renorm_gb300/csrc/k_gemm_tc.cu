@@ -871,17 +871,50 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
     // F8 GEMM 2: the per-pair scales staged below are the previous kernel's
     // output (the quantization of a), unlike the routing lists
     if (F8 && early) griddep_wait();
+    static_assert(N <= kEpiThreads, "one staged column per epilogue thread");
     int i = 0;
+    // The next tile's block entries -- its expert id and this thread's entry
+    // of sorted_token_ids (column et) -- are loaded while this tile is
+    // processed, so that staging a tile waits for one load (the weight or
+    // scale behind the entry) instead of two in a row.
+    int pf_e = 0, pf_p = -1;
+    auto prefetch = [&](int t) {
+      if (MODE == 2 || t >= n_tiles) return;
+      const int bb = coord(t).b;
+      pf_e = expert_ids[bb];
+      pf_p = et < N && et < B ? sorted_ids[(size_t)bb * B + et] : -1;
+    };
+    prefetch(t0);
     for (int t = t0; t < n_tiles; t += tstride) {
       const TileCoord tc = coord(t);
       const int b = tc.b, c = tc.c;
       // a block whose expert id lies outside [0, E) is computed (on zero
       // weights) but writes nothing
-      const int e_cur = MODE == 2 ? 0 : expert_ids[b];
+      const int e_cur = MODE == 2 ? 0 : pf_e;
+      const int p_cur = pf_p;
+      prefetch(t + tstride);
       const bool e_ok = MODE == 2 || (static_cast<unsigned>(e_cur) < static_cast<unsigned>(E));
-      // F8: scale of weight row r of this tile's expert
-      auto wscale = [&](int r) { return F8 && e_ok ? row_scale[(size_t)e_cur * a_rows + r] : 1.f; };
       const bool two = !Cfg::kWide && (MODE == 0 || c * 2 * kTileM + kTileM < a_rows);
+      // F8: the scales of the weight rows this thread's TMEM lane holds (1 for
+      // a row past the end), loaded together with the staging below
+      float s_lo = 1.f, s_hi = 1.f;
+      if (F8 && e_ok) {
+        const float *rs = row_scale + (size_t)e_cur * a_rows;
+        if (MODE == 0 && Cfg::kWide) {
+          const int chn = c * Cfg::kRowsPerCTile + (q & 1) * 32 + lane;  // gate rows in quarters 0-1
+          if (chn < R_out) s_lo = rs[q < 2 ? chn : R_out + chn];
+        } else if (MODE == 0) {
+          const int chn = c * kTileM + q * 32 + lane;
+          if (chn < R_out) {
+            s_lo = rs[chn];
+            s_hi = rs[R_out + chn];
+          }
+        } else if (MODE == 1) {
+          const int n = c * Cfg::kRowsPerCTile + q * 32 + lane;  // h = 0 and h = 1 (two tiles)
+          if (n < H_out) s_lo = rs[n];
+          if (two && n + kTileM < H_out) s_hi = rs[n + kTileM];
+        }
+      }
       const int acc = i % Cfg::kAccBufs;
       const uint32_t use = i / Cfg::kAccBufs;
       ++i;
@@ -893,7 +926,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
         if (MODE == 2) {
           if (b * N + j < src_rows) d = b * N + j;
         } else if (j < B && e_ok) {
-          const int p = sorted_ids[(size_t)b * B + j];
+          const int p = p_cur;  // (j == et)
           if (p >= 0 && p < P) {
             d = MODE == 0 ? p : p / top_k;
             if (MODE == 1) wgt = vec[p];
@@ -925,7 +958,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
         const bool valid = chn < R_out;
         // [pair][buffer][direction][column half][lane] of 16 bytes (8 bf16 columns)
         uint4 *slot = reinterpret_cast<uint4 *>(xchg) + pair * (2 * 2 * 32 * 2);
-        const float srow = valid ? wscale(is_gate ? chn : R_out + chn) : 1.f;
+        const float srow = s_lo;
 #pragma unroll 1
         for (int j0 = 32 * half, it = 0; j0 < N; j0 += 64, ++it) {
           uint32_t lo[16], hi[16];
@@ -959,26 +992,41 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
           const uint32_t other[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
           const uint32_t *mine = is_gate ? lo : hi;
           const int cbase = j0 + (is_gate ? 0 : 16);
-          // all 16 values first, then the stores: sixteen independent chains
-          // (exp, reciprocal) that the scheduler interleaves, where a value
-          // computed under its store's condition costs a full chain each
-          uint16_t res[16];
+          if constexpr (F8) {
+            // E4M3 operands halve the mainloop and leave the epilogue the
+            // longer path: all 16 values first, then the stores -- sixteen
+            // independent chains (exp, reciprocal) that the scheduler
+            // interleaves, where a value computed under its store's
+            // condition costs a full chain each (measured: 0.50 -> 0.37 ms
+            // at the 16384-token prefill).  With bf16 operands the mainloop
+            // is the longer path and this form measured 3 % slower there.
+            uint16_t res[16];
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) {
-            const float o = __uint_as_float((jj & 1) ? (other[jj >> 1] & 0xFFFF0000u) : (other[jj >> 1] << 16));
-            const float m = __uint_as_float(mine[jj]);
-            res[jj] = silu_mul_bf16(is_gate ? m : o, is_gate ? o : m);
-          }
+            for (int jj = 0; jj < 16; ++jj) {
+              const float o = __uint_as_float((jj & 1) ? (other[jj >> 1] & 0xFFFF0000u) : (other[jj >> 1] << 16));
+              const float m = __uint_as_float(mine[jj]);
+              res[jj] = silu_mul_bf16(is_gate ? m : o, is_gate ? o : m);
+            }
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) {
-            const int p = dst_row[cbase + jj];
-            if (valid && p >= 0) out16[(size_t)p * R_out + chn] = res[jj];
+            for (int jj = 0; jj < 16; ++jj) {
+              const int p = dst_row[cbase + jj];
+              if (valid && p >= 0) out16[(size_t)p * R_out + chn] = res[jj];
+            }
+          } else {
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+              const float o = __uint_as_float((jj & 1) ? (other[jj >> 1] & 0xFFFF0000u) : (other[jj >> 1] << 16));
+              const float m = __uint_as_float(mine[jj]);
+              const int p = dst_row[cbase + jj];
+              if (valid && p >= 0)
+                out16[(size_t)p * R_out + chn] = silu_mul_bf16(is_gate ? m : o, is_gate ? o : m);
+            }
           }
         }
       } else if (MODE == 0) {
         const int chn = c * kTileM + q * 32 + lane;
         const bool valid = chn < R_out;
-        const float sg = valid ? wscale(chn) : 1.f, su = valid ? wscale(R_out + chn) : 1.f;
+        const float sg = s_lo, su = s_hi;
 #pragma unroll 1
         for (int j0 = 16 * half; j0 < N; j0 += 32) {
           uint32_t gt[16], up[16];
@@ -1002,7 +1050,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
                 atomicAdd(h_acc + (size_t)p * 2 * R_out + R_out + chn, __uint_as_float(up[jj]));
               }
             }
-          } else {
+          } else if constexpr (F8) {
             uint16_t res[16];  // the values first, then the stores (as above)
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj)
@@ -1011,6 +1059,14 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
             for (int jj = 0; jj < 16; ++jj) {
               const int p = dst_row[j0 + jj];
               if (valid && p >= 0) out16[(size_t)p * R_out + chn] = res[jj];
+            }
+          } else {
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+              const int p = dst_row[j0 + jj];
+              if (valid && p >= 0)
+                out16[(size_t)p * R_out + chn] =
+                    silu_mul_bf16(__uint_as_float(gt[jj]), __uint_as_float(up[jj]));
             }
           }
         }
@@ -1028,7 +1084,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
         auto process = [&](int item, const uint32_t (&o)[16]) {
           const int h = item / n_chunks, j0 = (item - h * n_chunks) * 16;
           const int n = c * Cfg::kRowsPerCTile + h * kTileM + q * 32 + lane;
-          const float srow = (F8 && MODE == 1 && n < H_out) ? wscale(n) : 1.f;
+          const float srow = h == 0 ? s_lo : s_hi;
           if (MODE == 1 && Cfg::kWide) {
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) scr[jj * 32 + lane] = __uint_as_float(o[jj]) * srow;

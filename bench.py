@@ -739,7 +739,8 @@ def fp8_point(moe, args, device, stream, flush, peaks, world, cfg_name, M):
         "layer_hbm_frac": round(lay_bytes / (ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
         "layer_tc_frac_fp8": round(layer_flops(w, M) / (ms / 1e3) / 1e12 / f8_tflops, 4),
         "roofline": dict({"kernel": "grouped GEMM 1 (E4M3) + SiLU-and-mul"}, **roof,
-                         ms=round(gemm1_ms, 5)),
+                         ms=round(gemm1_ms, 5),
+                         traffic=profiled_traffic(f"k_gemm_tc_gemm1_{w.name}_fp8_m{M}.md", L.B)),
         "step_breakdown_ms": {k: round(statistics.mean(p[j] for p in per), 5)
                               for j, k in enumerate(L.phases)},
         "distinct_experts": round(statistics.mean(D), 2),

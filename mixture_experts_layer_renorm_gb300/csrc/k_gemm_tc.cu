@@ -566,15 +566,6 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
     const long end = min(pf_bytes, begin + slice);
     for (long o = begin; o < end; o += 65536) prefetch_l2_bulk(w_pf + o, (uint32_t)min(65536l, end - o));
   }
-  if (!early) griddep_wait();
-  griddep_launch_dependents();
-  int n_blocks;
-  if (MODE == 2) {
-    n_blocks = (src_rows + N - 1) / N;
-  } else {
-    const int n_post = min(max(*n_post_ptr, 0), cap);
-    n_blocks = n_post / B;
-  }
   // 2-SM tiles (P2, clusters of two): the pair's tile t covers weight tiles
   // c = 2 c2 (even CTA) and 2 c2 + 1 (odd CTA) of one block; the even CTA
   // issues M = 256 MMAs over both CTAs' shared memory, each CTA gathers half of
@@ -584,25 +575,10 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
   const int t0 = P2 ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
   const int tstride = P2 ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
   const int n_cunits = P2 ? n_ctiles / 2 : n_ctiles;
-  const int n_tiles = n_blocks * n_cunits * ksplit;
-  // GEMM 1 inside a layer clears the combine accumulator that GEMM 2 adds
-  // into (zero_n4 float4s at zero_dst): each CTA its slice, the epilogue warps
-  // while the first tile's mainloop runs (GEMM 2 reads it only after this
-  // kernel has completed).
-  auto zero_slice = [&](int tid, int nthreads) {
-    const long slice = (zero_n4 + gridDim.x - 1) / gridDim.x;
-    const long begin = static_cast<long>(blockIdx.x) * slice;
-    const long end = min(zero_n4, begin + slice);
-    for (long i = begin + tid; i < end; i += nthreads) zero_dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  };
-  if (t0 >= n_tiles) {  // (both CTAs of a pair leave here together)
-    // this kernel must not finish before the one it follows has: the next
-    // kernels count on that when they reuse what it read
-    if (early) griddep_wait();
-    if (MODE == 0 && zero_n4 > 0) zero_slice(threadIdx.x, blockDim.x);
-    return;
-  }
 
+  // Set-up that reads nothing an earlier kernel writes -- barriers, tensor
+  // memory, the weight map's descriptor -- runs before the dependency wait,
+  // while the previous kernel finishes.
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t *a_tiles = smem;                                   // [S][kATiles][16 KB]
@@ -651,6 +627,46 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
   tc_fence_after();
   if constexpr (P2) cluster_sync();  // the other CTA's barriers exist before any arrival
   const uint32_t tmem = *tmem_slot;
+  if (threadIdx.x == 0)
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_w)) : "memory");
+
+  if (!early) griddep_wait();
+  griddep_launch_dependents();
+  int n_blocks;
+  if (MODE == 2) {
+    n_blocks = (src_rows + N - 1) / N;
+  } else {
+    const int n_post = min(max(*n_post_ptr, 0), cap);
+    n_blocks = n_post / B;
+  }
+  const int n_tiles = n_blocks * n_cunits * ksplit;
+  // GEMM 1 inside a layer clears the combine accumulator that GEMM 2 adds
+  // into (zero_n4 float4s at zero_dst): each CTA its slice, the epilogue warps
+  // while the first tile's mainloop runs (GEMM 2 reads it only after this
+  // kernel has completed).
+  auto zero_slice = [&](int tid, int nthreads) {
+    const long slice = (zero_n4 + gridDim.x - 1) / gridDim.x;
+    const long begin = static_cast<long>(blockIdx.x) * slice;
+    const long end = min(zero_n4, begin + slice);
+    for (long i = begin + tid; i < end; i += nthreads) zero_dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  };
+  if (t0 >= n_tiles) {  // (both CTAs of a pair leave here together)
+    // this kernel must not finish before the one it follows has: the next
+    // kernels count on that when they reuse what it read
+    if (early) griddep_wait();
+    if (MODE == 0 && zero_n4 > 0) zero_slice(threadIdx.x, blockDim.x);
+    // give back the tensor memory allocated above (a pair: both CTAs)
+    tc_fence_before();
+    __syncthreads();
+    if constexpr (P2) {
+      cluster_sync();
+      if (warp == 1) tmem_dealloc_pair(tmem, Cfg::kTmemCols);
+    } else {
+      if (warp == 1) tmem_dealloc(tmem, Cfg::kTmemCols);
+    }
+    return;
+  }
+
   const int nk = (K + kBKe - 1) / kBKe;
   const TileSched sched = make_sched(n_cunits, ksplit, nk, n_blocks, MODE == 1 ? n_pass : 1);
   auto coord = [&](int t) {
@@ -754,7 +770,6 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
     // straight on to the next stage.
     const int gt = threadIdx.x - kGatherWarp0 * 32;
     const int ch = gt & 7;
-    if (early) griddep_wait();  // the gathered rows are the previous kernel's output
     // Entries of sorted_token_ids (MODE 2: token ids) of this thread's rows in
     // tile t; the next tile's are loaded while this tile's rows are copied.
     // (2-SM tiles: this CTA's rows are the block's rows rank * N/2 + r)
@@ -770,6 +785,9 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
     };
     int ids_next[Cfg::kChunksPerThread];
     fetch_ids(t0, ids_next);
+    // the gathered rows are the previous kernel's output; the row ids (the
+    // routing lists, final before GEMM 1 started) were loaded before the wait
+    if (early) griddep_wait();
     int g = 0;
     bool stop = false;
     for (int t = t0; t < n_tiles && !stop; t += tstride) {

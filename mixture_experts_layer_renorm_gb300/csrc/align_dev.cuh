@@ -186,6 +186,76 @@ __device__ void align_one_cta(int *smem, const int32_t *__restrict__ topk_ids, i
   }
 }
 
+// The same layout from ONE warp, for small inputs (P <= 32 * kWarpAlignRounds
+// pairs, E <= 1024): no block-wide barrier, ids read from `ids` (shared
+// memory of this CTA).  Pairs are ranked within their expert in pair order
+// (__match_any_sync per round of 32, counts carried across rounds), padded
+// group starts come from a warp scan over the experts (E / 32 contiguous
+// experts per lane), pads are written over the whole used range before the
+// pairs (ordered by __syncwarp).  smem: 2 * E + 1 ints.
+constexpr int kWarpAlignRounds = 8;
+
+__device__ void align_one_warp(int *smem, const int32_t *ids, int P, int E, int B,
+                               int32_t *__restrict__ sorted_ids, int32_t *__restrict__ expert_ids,
+                               int32_t *__restrict__ expert_offsets, int32_t *__restrict__ n_post,
+                               int *status) {
+  const int lane = threadIdx.x & 31;
+  int *cnt = smem, *off = smem + E;  // off: E + 1 entries
+  for (int e = lane; e < E; e += 32) cnt[e] = 0;
+  __syncwarp();
+  int my_e[kWarpAlignRounds], my_r[kWarpAlignRounds];
+  bool bad = false;
+#pragma unroll
+  for (int r = 0; r < kWarpAlignRounds; ++r) {
+    const int p = lane + 32 * r;
+    int e = p < P ? ids[p] : -1;
+    if (p < P && (e < 0 || e >= E)) {
+      bad = true;
+      e = -1;
+    }
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    const uint32_t before = peers & lanemask_lt();
+    my_e[r] = e;
+    my_r[r] = (e >= 0 ? cnt[e] : 0) + __popc(before);
+    __syncwarp();  // every lane has read cnt before the group leaders add to it
+    if (e >= 0 && before == 0) cnt[e] += __popc(peers);
+    __syncwarp();
+    if (32 * (r + 1) >= P) break;
+  }
+  if (bad) report_status(status, kStatusBadExpertId);
+  // padded group starts: lane l scans experts [l * per, (l + 1) * per)
+  const int per = (E + 31) / 32;
+  const int e_lo = min(E, lane * per), e_hi = min(E, e_lo + per);
+  int sum = 0;
+  for (int e = e_lo; e < e_hi; ++e) sum += (cnt[e] + B - 1) / B * B;
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  const int total = __shfl_sync(0xffffffffu, incl, 31);
+  int run = incl - sum;
+  for (int e = e_lo; e < e_hi; ++e) {
+    off[e] = run;
+    expert_offsets[e] = run;
+    const int padded = (cnt[e] + B - 1) / B * B;
+    for (int b = run / B; b < (run + padded) / B; ++b) expert_ids[b] = e;
+    run += padded;
+  }
+  if (lane == 0) {
+    expert_offsets[E] = total;
+    *n_post = total;
+  }
+  for (int i = lane; i < total; i += 32) sorted_ids[i] = P;  // pads; the pairs overwrite theirs
+  __syncwarp();
+#pragma unroll
+  for (int r = 0; r < kWarpAlignRounds; ++r) {
+    if (my_e[r] >= 0) sorted_ids[off[my_e[r]] + my_r[r]] = lane + 32 * r;
+    if (32 * (r + 1) >= P) break;
+  }
+}
+
 inline size_t align_smem_bytes(int E) {
   return sizeof(int) * (3 * (size_t)E + kAlignWarps * E + kAlignWarps + 1);
 }

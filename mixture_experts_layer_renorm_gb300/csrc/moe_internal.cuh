@@ -79,6 +79,25 @@ __device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
+// acc + the 8 products of two rows of 8 bf16 (16 bytes each), taken in order
+// with the mixed-precision multiply-add (bf16 operands, fp32 sum: the product
+// of two bf16 values is exact in fp32, so each step rounds once, as an fp32
+// fma of the widened values would).
+__device__ __forceinline__ float dot8_bf16(const uint4 &w, const uint4 &x, float acc) {
+  asm("{\n\t.reg .b16 w0, w1, w2, w3, w4, w5, w6, w7, x0, x1, x2, x3, x4, x5, x6, x7;\n\t"
+      "mov.b32 {w0, w1}, %1;\n\tmov.b32 {w2, w3}, %2;\n\t"
+      "mov.b32 {w4, w5}, %3;\n\tmov.b32 {w6, w7}, %4;\n\t"
+      "mov.b32 {x0, x1}, %5;\n\tmov.b32 {x2, x3}, %6;\n\t"
+      "mov.b32 {x4, x5}, %7;\n\tmov.b32 {x6, x7}, %8;\n\t"
+      "fma.rn.f32.bf16 %0, w0, x0, %0;\n\tfma.rn.f32.bf16 %0, w1, x1, %0;\n\t"
+      "fma.rn.f32.bf16 %0, w2, x2, %0;\n\tfma.rn.f32.bf16 %0, w3, x3, %0;\n\t"
+      "fma.rn.f32.bf16 %0, w4, x4, %0;\n\tfma.rn.f32.bf16 %0, w5, x5, %0;\n\t"
+      "fma.rn.f32.bf16 %0, w6, x6, %0;\n\tfma.rn.f32.bf16 %0, w7, x7, %0;\n\t}"
+      : "+f"(acc)
+      : "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w), "r"(x.x), "r"(x.y), "r"(x.z), "r"(x.w));
+  return acc;
+}
+
 // Record the first problem a kernel meets; later ones keep the first code.
 __device__ __forceinline__ void report_status(int *status, int code) {
   if (status != nullptr) atomicCAS(status, 0, code);

@@ -24,11 +24,13 @@ __device__ __forceinline__ uint16_t bf16_from_order_key(uint32_t k) {
 // and, among equal logits, the lowest expert id.  top_k rounds of a warp
 // max-reduction pick the slots in order; the winner's key is cleared.
 // Logits written earlier in the same kernel by other CTAs are read around L1.
+// ids_copy (nullable, e.g. shared memory): a second copy of the chosen ids.
 template <int VPL, bool kFromOtherCtas>
 __device__ __forceinline__ void topk_softmax_warp(const uint16_t *__restrict__ row, int E,
                                                   int top_k, int renormalize,
                                                   int32_t *__restrict__ ids_out,
-                                                  float *__restrict__ w_out, int lane) {
+                                                  float *__restrict__ w_out, int lane,
+                                                  int32_t *ids_copy = nullptr) {
   uint32_t key[VPL];
   float val[VPL];
   float mx = -INFINITY;
@@ -46,15 +48,18 @@ __device__ __forceinline__ void topk_softmax_warp(const uint16_t *__restrict__ r
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  // the full softmax denominator only when the weights are not renormalized
   float den = 0.f;
+  if (!renormalize) {
 #pragma unroll
-  for (int i = 0; i < VPL; ++i)
-    if (lane + 32 * i < E) den += expf(val[i] - mx);
+    for (int i = 0; i < VPL; ++i)
+      if (lane + 32 * i < E) den += expf(val[i] - mx);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-
-  int my_id = 0;
-  float my_p = 0.f, kept = 0.f;
+    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+  }
+  // top_k rounds pick the keys (lane j keeps the j-th); the exponentials of
+  // the chosen logits are then taken by their lanes side by side
+  uint32_t my_key = 0;
   for (int j = 0; j < top_k; ++j) {
     uint32_t best = 0;
 #pragma unroll
@@ -63,17 +68,16 @@ __device__ __forceinline__ void topk_softmax_warp(const uint16_t *__restrict__ r
 #pragma unroll
     for (int i = 0; i < VPL; ++i)
       if (key[i] == best) key[i] = 0;
-    const int e = static_cast<int>(0xFFFFu - (best & 0xFFFFu));
-    const float v = bf16_bits_to_float(bf16_from_order_key(best >> 16));
-    const float pj = expf(v - mx);
-    kept += pj;
-    if (lane == j) {
-      my_id = e;
-      my_p = pj;
-    }
+    if (lane == j) my_key = best;
   }
+  const int my_id = static_cast<int>(0xFFFFu - (my_key & 0xFFFFu));
+  const float my_p = lane < top_k ? expf(bf16_bits_to_float(bf16_from_order_key(my_key >> 16)) - mx) : 0.f;
+  float kept = my_p;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) kept += __shfl_xor_sync(0xffffffffu, kept, o);
   if (lane < top_k) {
     ids_out[lane] = my_id;
+    if (ids_copy != nullptr) ids_copy[lane] = my_id;
     w_out[lane] = renormalize ? my_p / kept : my_p / den;
   }
 }

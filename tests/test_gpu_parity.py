@@ -527,6 +527,37 @@ def test_route_with_router_weights(cfg, M):
     assert np.array_equal(out["o"], ro)
 
 
+@pytest.mark.parametrize("M,E,k,H,B", [(1, 128, 8, 2048, 16), (8, 128, 8, 2048, 16),
+                                       (5, 60, 4, 2048, 16), (2, 20, 3, 256, 16),
+                                       (8, 256, 8, 2048, 16), (3, 200, 6, 2112, 32),
+                                       (7, 16, 2, 64, 16), (4, 129, 32, 4160, 16)])
+def test_route_small_batches_with_router_weights(M, E, k, H, B):
+    """Decode batches (M <= 8) with router weights run one thread-block cluster
+    (up to 8 CTAs, E/n experts each, logits handed over in shared memory): the
+    logits within the fp32 bound, ids and weights the oracle's top-k of those
+    logits and the lists the oracle's align of those ids, bit for bit; cluster
+    sizes 1 to 8, two experts per warp (E > 128), K over several staged chunks
+    (H > 2048) and a ragged last chunk."""
+    x = rand_bf16((M, H), 1.0, 600 + M + E)
+    wr = rand_bf16((E, H), 0.02, 700 + E)
+    bias = synth.zipf_router_bias(E, 1.1).to(DEV) if E % 2 == 0 else None
+    g_lg = torch.empty((M, E), dtype=torch.bfloat16, device=DEV)
+    ws = moe.Workspace(M, E, k, H, 16, B)
+    for rep in range(2):  # a second call on the same workspace
+        out, _ = run_route(M, E, k, B, x=x, wr=wr, bias=bias, lg_out=g_lg, ws=ws)
+        lg_b = bits(g_lg)
+        check_logits(lg_b, x, wr, bias)
+        rid, rw = oracle.topk_softmax(lg_b, k)
+        assert np.array_equal(out["ids"], rid)
+        assert np.abs(out["w"].astype(np.float64) - rw).max() <= W_ABS
+        rs, re_, ro, rn = oracle.align_block_size(rid, E, B)
+        nn = int(out["n"][0])
+        assert nn == rn
+        assert np.array_equal(out["s"][:nn], rs[:nn])
+        assert np.array_equal(out["e"][: nn // B], re_[: nn // B])
+        assert np.array_equal(out["o"], ro)
+
+
 # ----------------------------------------------------------------------------- small-batch sort skip
 
 @pytest.mark.parametrize("cfg,M", [(2, 1), (2, 4), (5, 1), (4, 1), (4, 8)])

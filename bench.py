@@ -284,7 +284,7 @@ class Layer:
         if self.M <= 256 and self.M * self.w.top_k <= 16384:
             route = 1
         else:
-            route = (0 if self.w.logits_given else 1) + 1 + (1 if self.M * self.w.top_k <= 16384 else 2)
+            route = (0 if self.w.logits_given else 1) + 1 + (1 if self.M * self.w.top_k <= 2048 else 2)
         # E4M3 weights: two more launches, the per-row quantizations of x and a
         return route + 1 + 2 + (2 if self.fp8 else 0)
 
@@ -554,7 +554,7 @@ class Stack:
         if M <= 256 and M * w.top_k <= 16384:
             route = 1
         else:
-            route = 2 + (1 if M * w.top_k <= 16384 else 2)
+            route = 2 + (1 if M * w.top_k <= 2048 else 2)
         return w.layers * (route + 3)
 
     def step(self, moe, x, stream, keep_ids=False):

@@ -67,18 +67,22 @@ __device__ AlignSmem carve(int *smem, int E) {
 }
 
 // Writes expert_offsets, n_post, expert_ids of every real block and the pad
-// entries of every group.  cnt/off hold whole-input counts and offsets.
+// entries of every group.  cnt/off hold whole-input counts and offsets.  With
+// several CTAs holding the same counts, CTA `part` of `parts` writes the
+// expert ids of every parts-th block and the pads of every parts-th expert.
 __device__ void write_layout(const AlignSmem &s, int E, int B, int P, int total,
                              int32_t *sorted_ids, int32_t *expert_ids, int32_t *expert_offsets,
-                             int32_t *n_post) {
+                             int32_t *n_post, int part = 0, int parts = 1) {
   const int tid = threadIdx.x;
-  for (int e = tid; e < E; e += blockDim.x) expert_offsets[e] = s.off[e];
-  if (tid == 0) {
-    expert_offsets[E] = total;
-    *n_post = total;
+  if (part == 0) {
+    for (int e = tid; e < E; e += blockDim.x) expert_offsets[e] = s.off[e];
+    if (tid == 0) {
+      expert_offsets[E] = total;
+      *n_post = total;
+    }
   }
   // expert of block blk: the last expert whose group starts at or before blk*B
-  for (int blk = tid; blk < total / B; blk += blockDim.x) {
+  for (int blk = part + parts * tid; blk < total / B; blk += parts * blockDim.x) {
     const int pos = blk * B;
     int lo = 0, hi = E;  // first e with off[e] > pos, minus one
     while (lo < hi) {
@@ -89,7 +93,7 @@ __device__ void write_layout(const AlignSmem &s, int E, int B, int P, int total,
     expert_ids[blk] = lo - 1;
   }
   const int warp = tid >> 5, lane = tid & 31;
-  for (int e = warp; e < E; e += blockDim.x / 32) {
+  for (int e = part + parts * warp; e < E; e += parts * (blockDim.x / 32)) {
     const int c = s.cnt[e];
     const int padded = (c + B - 1) / B * B;
     for (int r = c + lane; r < padded; r += 32) sorted_ids[s.off[e] + r] = P;
@@ -103,17 +107,18 @@ __device__ __forceinline__ int load_id(const int32_t *p) {
 }
 
 // Stable scatter of pairs [begin, end) using s.run as each expert's next slot.
+// The id of a thread's pair in the next round is loaded before this round's
+// barriers, so no round waits on a global load.
 template <bool kFromOtherCtas = false>
 __device__ void scatter_chunk(const AlignSmem &s, const int32_t *__restrict__ topk_ids, int begin,
                               int end, int E, int32_t *__restrict__ sorted_ids) {
   const int tid = threadIdx.x, warp = tid >> 5;
+  int e_next = begin + tid < end ? load_id<kFromOtherCtas>(topk_ids + begin + tid) : -1;
   for (int base = begin; base < end; base += kAlignThreads) {
     const int p = base + tid;
-    int e = -1;
-    if (p < end) {
-      e = load_id<kFromOtherCtas>(topk_ids + p);
-      if (e < 0 || e >= E) e = -1;
-    }
+    int e = e_next;
+    if (p + kAlignThreads < end) e_next = load_id<kFromOtherCtas>(topk_ids + p + kAlignThreads);
+    if (p >= end || e < 0 || e >= E) e = -1;
     const uint32_t peers = __match_any_sync(0xffffffffu, e);
     const int rank = __popc(peers & lanemask_lt());
     const bool leader = rank == 0;
@@ -154,6 +159,7 @@ __device__ void align_one_cta(int *smem, const int32_t *__restrict__ topk_ids, i
       else bad = true;
     }
   } else {
+#pragma unroll 4
     for (int p = tid; p < P; p += blockDim.x) {
       const int e = load_id<kFromOtherCtas>(topk_ids + p);
       if (e >= 0 && e < E) atomicAdd(&s.cnt[e], 1);

@@ -23,7 +23,7 @@ namespace moe {
 namespace {
 
 constexpr int kAlignChunk = 2048;          // pairs per CTA in the multi-CTA path
-constexpr int kAlignSingleMax = 16384;     // up to this many pairs: one CTA
+constexpr int kAlignSingleMax = 2048;      // up to this many pairs: one CTA
 
 // One CTA does the whole align.
 __global__ void __launch_bounds__(kAlignThreads)
@@ -51,6 +51,7 @@ k_align_count(const int32_t *__restrict__ topk_ids, int P, int E, int32_t *__res
   const int begin = blockIdx.x * kAlignChunk;
   const int end = min(P, begin + kAlignChunk);
   bool bad = false;
+#pragma unroll 4
   for (int p = begin + tid; p < end; p += blockDim.x) {
     const int e = topk_ids[p];
     if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
@@ -62,7 +63,8 @@ k_align_count(const int32_t *__restrict__ topk_ids, int P, int E, int32_t *__res
 }
 
 // Multi-CTA, pass 2: every CTA sums the histogram table (whole-input counts
-// and the counts of the chunks before its own), scans the padded counts, and
+// and the counts of the chunks before its own; all threads over the whole
+// table, added up with shared-memory atomics), scans the padded counts, and
 // scatters its chunk.  CTA 0 also writes offsets, expert_ids and pads.
 __global__ void __launch_bounds__(kAlignThreads)
 k_align_scatter(const int32_t *__restrict__ topk_ids, int P, int E, int B,
@@ -77,20 +79,34 @@ k_align_scatter(const int32_t *__restrict__ topk_ids, int P, int E, int B,
   const int c = blockIdx.x, C = gridDim.x;
   for (int i = tid; i < kAlignWarps * E; i += blockDim.x) s.wc[i] = 0;
   for (int e = tid; e < E; e += blockDim.x) {
-    int tot = 0, before = 0;
-    for (int cc = 0; cc < C; ++cc) {
-      const int v = hist[(size_t)cc * E + e];
-      tot += v;
-      if (cc < c) before += v;
-    }
-    s.cnt[e] = tot;
-    s.run[e] = before;
-    s.off[e] = (tot + B - 1) / B * B;
+    s.cnt[e] = 0;
+    s.run[e] = 0;
   }
+  __syncthreads();
+  // sixteen table entries per thread in flight at once, then their sums
+  const int n_hist = C * E;
+  for (int i0 = tid; i0 < n_hist; i0 += 16 * kAlignThreads) {
+    int v[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const int i = i0 + u * kAlignThreads;
+      v[u] = i < n_hist ? hist[i] : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const int i = i0 + u * kAlignThreads;
+      if (v[u] != 0) {
+        atomicAdd(&s.cnt[i % E], v[u]);
+        if (i < c * E) atomicAdd(&s.run[i % E], v[u]);  // a chunk before this CTA's
+      }
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += blockDim.x) s.off[e] = (s.cnt[e] + B - 1) / B * B;
   __syncthreads();
   const int total = block_exclusive_scan(s.off, E, s.misc);
   for (int e = tid; e < E; e += blockDim.x) s.run[e] += s.off[e];
-  if (c == 0) write_layout(s, E, B, P, total, sorted_ids, expert_ids, expert_offsets, n_post);
+  write_layout(s, E, B, P, total, sorted_ids, expert_ids, expert_offsets, n_post, c, C);
   __syncthreads();
   const int begin = c * kAlignChunk;
   scatter_chunk(s, topk_ids, begin, min(P, begin + kAlignChunk), E, sorted_ids);

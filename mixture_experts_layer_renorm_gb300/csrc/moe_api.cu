@@ -195,27 +195,6 @@ moe_status_t run_route(const uint16_t *x, const uint16_t *w_router, const uint16
                                        npost, hist, control, s));
 }
 
-// Decode-sized batches (M <= kSplitMaxTokens) with at least a wave of tiles
-// use the stage-balanced schedule: whole waves of tiles, then the remaining
-// tiles' K stages shared equally, so that the block count (which changes
-// with every batch) leaves no CTA a tile more than the others.  With fewer
-// tiles than SMs the tile schedule and its K split (pick_ksplit) measured
-// as fast or faster.  GEMM 1's cut tiles need the split-K scratch cleared
-// (P x 2I floats, by the routing kernel): where the expected last wave is
-// nearly full (>= 80 %) that costs more than it saves, measured at the
-// Qwen3 decode M = 64 (bf16 and E4M3).  MOE_GEMM_SCHEDULE=tiles keeps the
-// tile schedule everywhere (for comparisons).  n_ctiles: weight tiles per
-// block.
-bool stage_balanced(int M, int E, int top_k, int n_ctiles, bool gemm1) {
-  if (M > kSplitMaxTokens) return false;
-  const char *v = std::getenv("MOE_GEMM_SCHEDULE");
-  if (v != nullptr && std::strcmp(v, "tiles") == 0) return false;
-  const double D = E * (1.0 - std::pow(1.0 - static_cast<double>(top_k) / E, M));
-  const double waves = D * n_ctiles / moe::num_sms();
-  if (waves < 1.0) return false;
-  return !gemm1 || waves - std::floor(waves) < 0.8;
-}
-
 // Splits of each tile's K range for a grouped GEMM with n_ctiles weight tiles
 // per block: decode batches can have fewer tiles than SMs, or a last wave
 // that leaves most SMs idle.  The block count is estimated on the host as the
@@ -249,10 +228,7 @@ moe_status_t run_gemm1(const uint16_t *x, const uint16_t *w13, const int32_t *so
   const int cap = static_cast<int>(capacity(P, E, B));
   switch (pick_path(M, E, top_k, B)) {
     case GemmPath::kTensorCore: {
-      const int ks = h_acc == nullptr ? 1
-                     : stage_balanced(M, E, top_k, (I + 127) / 128, true)
-                         ? 0
-                         : pick_ksplit(M, E, top_k, (I + 127) / 128, (H + 63) / 64);
+      const int ks = h_acc != nullptr ? pick_ksplit(M, E, top_k, (I + 127) / 128, (H + 63) / 64) : 1;
       const double D = E * (1.0 - std::pow(1.0 - static_cast<double>(top_k) / E, M));
       const int pf_experts = (prefetch && D >= 0.9 * E) ? E : 0;
       return cuda_status(moe::launch_tc_w13_act(x, w13, sorted, eids, npost, static_cast<int>(P),
@@ -279,9 +255,7 @@ moe_status_t run_gemm2(const uint16_t *a, const uint16_t *w2, const int32_t *sor
   const int cap = static_cast<int>(capacity(P, E, B));
   switch (pick_path(M, E, top_k, B)) {
     case GemmPath::kTensorCore: {
-      const int ks = stage_balanced(M, E, top_k, (H + 255) / 256, false)
-                         ? 0
-                         : pick_ksplit(M, E, top_k, (H + 255) / 256, (I + 63) / 64);
+      const int ks = pick_ksplit(M, E, top_k, (H + 255) / 256, (I + 63) / 64);
       return cuda_status(moe::launch_tc_w2_combine(a, w2, sorted, eids, npost, wts,
                                                    static_cast<int>(P), top_k, E, H, I, B, cap,
                                                    yacc, ks, status, early_weights, s));
@@ -303,10 +277,7 @@ moe_status_t run_gemm1_f8(const uint8_t *qx, const float *sx, const uint8_t *w13
                           float *zero_dst, long zero_n, cudaStream_t s) {
   const long P = static_cast<long>(M) * top_k;
   const int cap = static_cast<int>(capacity(P, E, B));
-  const int ks = h_acc == nullptr ? 1
-                 : stage_balanced(M, E, top_k, (I + 127) / 128, true)
-                     ? 0
-                     : pick_ksplit(M, E, top_k, (I + 127) / 128, (H + 127) / 128);
+  const int ks = h_acc != nullptr ? pick_ksplit(M, E, top_k, (I + 127) / 128, (H + 127) / 128) : 1;
   const double D = E * (1.0 - std::pow(1.0 - static_cast<double>(top_k) / E, M));
   const int pf_experts = (prefetch && D >= 0.9 * E) ? E : 0;
   return cuda_status(moe::launch_tc_w13_act_f8(qx, sx, w13, w13s, sorted, eids, npost,
@@ -321,9 +292,7 @@ moe_status_t run_gemm2_f8(const uint8_t *qa, const float *sa, const uint8_t *w2,
                           float *yacc, int *status, bool early_weights, cudaStream_t s) {
   const long P = static_cast<long>(M) * top_k;
   const int cap = static_cast<int>(capacity(P, E, B));
-  const int ks = stage_balanced(M, E, top_k, (H + 255) / 256, false)
-                     ? 0
-                     : pick_ksplit(M, E, top_k, (H + 255) / 256, (I + 127) / 128);
+  const int ks = pick_ksplit(M, E, top_k, (H + 255) / 256, (I + 127) / 128);
   return cuda_status(moe::launch_tc_w2_combine_f8(qa, sa, w2, w2s, sorted, eids, npost, wts,
                                                   static_cast<int>(P), top_k, E, H, I, B, cap,
                                                   yacc, ks, status, early_weights, s));
@@ -530,8 +499,7 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *w_router,
   // the fused routing kernel clears y_acc, and h_acc and the tile counters
   // behind it when GEMM 1 will split its K range (one span)
   const bool want_split = L.hacc != L.tcnt && pick_path(M, E, top_k, B) == GemmPath::kTensorCore &&
-                          (stage_balanced(M, E, top_k, (I + 127) / 128, true) ||
-                           pick_ksplit(M, E, top_k, (I + 127) / 128, (H + 63) / 64) > 1);
+                          pick_ksplit(M, E, top_k, (I + 127) / 128, (H + 63) / 64) > 1;
   const long zn = want_split ? static_cast<long>((L.total - L.yacc) / sizeof(float)) : yn;
   bool zeroed = false;
   st = run_route(x, w_router, router_logits, router_bias, M, E, top_k, H, renormalize, B,
@@ -686,9 +654,7 @@ moe_status_t moe_forward_fp8(const moe_bf16_t *x, const moe_bf16_t *w_router,
   float *sa = at<float>(ws, L.sa);
   const long yn = static_cast<long>(M) * H;
   const bool want_split =
-      L.hacc != L.tcnt &&
-      (stage_balanced(M, E, top_k, (I + 127) / 128, true) ||
-       pick_ksplit(M, E, top_k, (I + 127) / 128, (H + 127) / 128) > 1);
+      L.hacc != L.tcnt && pick_ksplit(M, E, top_k, (I + 127) / 128, (H + 127) / 128) > 1;
   const long zn = want_split ? static_cast<long>((L.total - L.yacc) / sizeof(float)) : yn;
   bool zeroed = false;
   st = run_route(x, w_router, router_logits, router_bias, M, E, top_k, H, renormalize, B,

@@ -651,28 +651,30 @@ def test_forward_back_to_back_on_one_workspace_with_changing_batches():
 
 
 @pytest.mark.parametrize("cfg,M", [(2, 8), (2, 32), (2, 20), (5, 64), (4, 128), (2, 200)])
-@pytest.mark.parametrize("schedule", ["stage", "tiles"])
-def test_forward_decode_schedules_match_the_oracle(cfg, M, schedule, monkeypatch):
-    """Decode batches with at least a wave of tiles run whole waves and then
-    cut the remaining tiles' K stages across all CTAs (GEMM 1's cut tiles
-    finished through the split-K scratch by whichever part completes the K
-    stages); the tile schedule with its K split is the comparison.  Both
-    match the oracle on every token (given logits, so routing is exact)."""
-    if schedule == "tiles":
-        monkeypatch.setenv("MOE_GEMM_SCHEDULE", "tiles")
-    else:
-        monkeypatch.delenv("MOE_GEMM_SCHEDULE", raising=False)
+def test_forward_decode_batches_twice_per_workspace(cfg, M):
+    """Decode batches whose GEMM tiles are split along K (the partial sums
+    added up in the split-K scratch, the last part of each tile forming its
+    output) match the oracle on every token (given logits, so routing is
+    exact), on two calls in a row on one workspace: the tile counters must be
+    back at zero after each call."""
     w = synth.WORKLOADS[cfg]
     wt = synth.layer_weights(w, device=DEV)
     x = rand_bf16((M, w.H), 1.0, 1300 + M)
     lg = rand_bf16((M, w.E), 1.0, 1400 + M, "cpu")
     res = x if w.residual else None
-    for rep in range(2):  # the cut tiles' counters must be back at zero
-        yb, ids, wts = run_forward(x, wt["w13"], wt["w2"], w.top_k, lg=lg.to(DEV), res=res)
-        ref = oracle.moe_forward(bits(x), bits(wt["w13"]), bits(wt["w2"]), w.top_k,
-                                 router_logits=bits(lg), residual=None if res is None else bits(res))
-        assert np.array_equal(ids, ref["topk_ids"])
-        assert_close_bf16(yb, ref["y"], f"y (call {rep})")
+    ref = oracle.moe_forward(bits(x), bits(wt["w13"]), bits(wt["w2"]), w.top_k,
+                             router_logits=bits(lg), residual=None if res is None else bits(res))
+    ws = moe.Workspace(M, w.E, w.top_k, w.H, w.I)
+    lgd = lg.to(DEV)
+    for rep in range(2):  # the split tiles' counters must be back at zero
+        y = torch.empty((M, w.H), dtype=torch.bfloat16, device=DEV)
+        ids = torch.empty((M, w.top_k), dtype=torch.int32, device=DEV)
+        moe.moe_forward(x, wt["w13"], wt["w2"], w.top_k, y, ws, router_logits=lgd, residual=res,
+                        topk_ids_out=ids)
+        torch.cuda.synchronize()
+        assert moe.moe_get_device_status(ws) == 0
+        assert np.array_equal(ids.cpu().numpy(), ref["topk_ids"])
+        assert_close_bf16(bits(y), ref["y"], f"y (call {rep})")
 
 
 # ----------------------------------------------------------------------------- one-kernel decode layer

@@ -639,7 +639,19 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
     const int n_post = min(max(*n_post_ptr, 0), cap);
     n_blocks = n_post / B;
   }
-  const int n_tiles = n_blocks * n_cunits * ksplit;
+  // This CTA's work: n_work tiles (block, weight tile, K-stage range), tiles
+  // t0, t0 + tstride, ... of the persistent schedule, each split ksplit ways
+  // along K.
+  const int kspl = ksplit < 1 ? 1 : ksplit;
+  const int nk = (K + kBKe - 1) / kBKe;
+  const int n_tiles = n_blocks * n_cunits * kspl;
+  const TileSched sched = make_sched(n_cunits, kspl, nk, n_blocks, MODE == 1 ? n_pass : 1);
+  const int n_work = t0 < n_tiles ? (n_tiles - 1 - t0) / tstride + 1 : 0;
+  auto work = [&](int j) {
+    TileCoord tc = tile_coord(t0 + j * tstride, sched);
+    if (P2) tc.c = 2 * tc.c + rank;
+    return tc;
+  };
   // GEMM 1 inside a layer clears the combine accumulator that GEMM 2 adds
   // into (zero_n4 float4s at zero_dst): each CTA its slice, the epilogue warps
   // while the first tile's mainloop runs (GEMM 2 reads it only after this
@@ -650,7 +662,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
     const long end = min(zero_n4, begin + slice);
     for (long i = begin + tid; i < end; i += nthreads) zero_dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   };
-  if (t0 >= n_tiles) {  // (both CTAs of a pair leave here together)
+  if (n_work == 0) {  // (both CTAs of a pair leave here together)
     // this kernel must not finish before the one it follows has: the next
     // kernels count on that when they reuse what it read
     if (early) griddep_wait();
@@ -667,14 +679,6 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
     return;
   }
 
-  const int nk = (K + kBKe - 1) / kBKe;
-  const TileSched sched = make_sched(n_cunits, ksplit, nk, n_blocks, MODE == 1 ? n_pass : 1);
-  auto coord = [&](int t) {
-    TileCoord tc = tile_coord(t, sched);
-    if (P2) tc.c = 2 * tc.c + rank;
-    return tc;
-  };
-
   if (warp == 0) {
     // ------------------------------------------------------------ weight tiles (TMA)
     // The next tile's expert id is loaded while this tile's copies go out.  An
@@ -683,14 +687,12 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
     if (lane == 0) {
       int g = 0;
       bool stop = false;
-      int t = t0;
-      int e_next = MODE == 2 ? 0 : expert_ids[coord(t).b];
-      for (; t < n_tiles && !stop; t += tstride) {
-        const TileCoord tc = coord(t);
+      int e_next = MODE == 2 ? 0 : expert_ids[work(0).b];
+      for (int j = 0; j < n_work && !stop; ++j) {
+        const TileCoord tc = work(j);
         const int c = tc.c;
         const int e = e_next;
-        const int tn = t + tstride;
-        if (MODE != 2 && tn < n_tiles) e_next = expert_ids[coord(tn).b];
+        if (MODE != 2 && j + 1 < n_work) e_next = expert_ids[work(j + 1).b];
         // weight rows of the stage's tile(s); wide GEMM 1 loads 64 gate rows
         // and the matching 64 up rows as the two halves of one 128-row tile
         // (the map's box is then 64 rows high)
@@ -747,8 +749,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
     if (P2 && rank == 1 && lane == 0) {
       int g = 0;
       bool stop = false;
-      for (int t = t0; t < n_tiles && !stop; t += tstride) {
-        const TileCoord tc = coord(t);
+      for (int j = 0; j < n_work && !stop; ++j) {
+        const TileCoord tc = work(j);
         for (int kb = tc.kb0; kb < tc.kb1; ++kb, ++g) {
           if (g % kRelayWarps != rw) continue;
           const int sf = g % S;
@@ -774,8 +776,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
     // tile t; the next tile's are loaded while this tile's rows are copied.
     // (2-SM tiles: this CTA's rows are the block's rows rank * N/2 + r)
     const int rbase = P2 ? rank * Cfg::kBRows : 0;
-    auto fetch_ids = [&](int t, int (&ids)[Cfg::kChunksPerThread]) {
-      const int b = coord(t).b;
+    auto fetch_ids = [&](int j, int (&ids)[Cfg::kChunksPerThread]) {
+      const int b = work(j).b;
 #pragma unroll
       for (int u = 0; u < Cfg::kChunksPerThread; ++u) {
         const int r = rbase + (gt >> 3) + 16 * u;
@@ -784,14 +786,14 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
       }
     };
     int ids_next[Cfg::kChunksPerThread];
-    fetch_ids(t0, ids_next);
+    fetch_ids(0, ids_next);
     // the gathered rows are the previous kernel's output; the row ids (the
     // routing lists, final before GEMM 1 started) were loaded before the wait
     if (early) griddep_wait();
     int g = 0;
     bool stop = false;
-    for (int t = t0; t < n_tiles && !stop; t += tstride) {
-      const TileCoord tc = coord(t);
+    for (int j = 0; j < n_work && !stop; ++j) {
+      const TileCoord tc = work(j);
       int rowv[Cfg::kChunksPerThread];
 #pragma unroll
       for (int u = 0; u < Cfg::kChunksPerThread; ++u) {
@@ -804,8 +806,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
         }
         rowv[u] = row;
       }
-      const int tn = t + tstride;
-      if (tn < n_tiles) fetch_ids(tn, ids_next);
+      if (j + 1 < n_work) fetch_ids(j + 1, ids_next);
       for (int kb = tc.kb0; kb < tc.kb1; ++kb, ++g) {
         const int s = g % S;
         if (!wait_bounded(smem_u32(&empty[s]), ((g / S) & 1) ^ 1, abort, status)) {
@@ -834,8 +835,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
                                     : umma_idesc_bf16(P2 ? 2 * kTileM : kTileM, N);
       int g = 0, i = 0;
       bool stop = false;
-      for (int t = t0; t < n_tiles && !stop; t += tstride) {
-        const TileCoord tc = coord(t);
+      for (int j = 0; j < n_work && !stop; ++j) {
+        const TileCoord tc = work(j);
         const bool two = !Cfg::kWide && (MODE == 0 || tc.c * 2 * kTileM + kTileM < a_rows);
         const int acc = i % Cfg::kAccBufs;
         const uint32_t use = i / Cfg::kAccBufs;
@@ -896,21 +897,23 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
     // processed, so that staging a tile waits for one load (the weight or
     // scale behind the entry) instead of two in a row.
     int pf_e = 0, pf_p = -1;
-    auto prefetch = [&](int t) {
-      if (MODE == 2 || t >= n_tiles) return;
-      const int bb = coord(t).b;
+    auto prefetch = [&](int j) {
+      if (MODE == 2 || j >= n_work) return;
+      const int bb = work(j).b;
       pf_e = expert_ids[bb];
       pf_p = et < N && et < B ? sorted_ids[(size_t)bb * B + et] : -1;
     };
-    prefetch(t0);
-    for (int t = t0; t < n_tiles; t += tstride) {
-      const TileCoord tc = coord(t);
+    prefetch(0);
+    for (int jw = 0; jw < n_work; ++jw) {
+      const TileCoord tc = work(jw);
       const int b = tc.b, c = tc.c;
+      // a K range short of the whole tile: partial sums (GEMM 1 through h_acc)
+      const bool partial = tc.kb0 > 0 || tc.kb1 < nk;
       // a block whose expert id lies outside [0, E) is computed (on zero
       // weights) but writes nothing
       const int e_cur = MODE == 2 ? 0 : pf_e;
       const int p_cur = pf_p;
-      prefetch(t + tstride);
+      prefetch(jw + 1);
       const bool e_ok = MODE == 2 || (static_cast<unsigned>(e_cur) < static_cast<unsigned>(E));
       const bool two = !Cfg::kWide && (MODE == 0 || c * 2 * kTileM + kTileM < a_rows);
       // F8: the scales of the weight rows this thread's TMEM lane holds (1 for
@@ -1058,7 +1061,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
               up[jj] = __float_as_uint(__uint_as_float(up[jj]) * su * dst_w[j0 + jj]);
             }
           }
-          if (ksplit > 1) {
+          if (partial) {
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
               const int p = dst_row[j0 + jj];
@@ -1163,12 +1166,15 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
         if (P2 && rank == 1) mbar_arrive_cluster(map_to_cta(smem_u32(&acc_empty[acc]), 0));
         else mbar_arrive(smem_u32(&acc_empty[acc]));
       }
-      if (MODE == 0 && ksplit > 1) {
-        // The last split of this tile to finish (an atomic count after a fence;
-        // nobody waits) reads the summed h back and writes a.
+      if (MODE == 0 && partial) {
+        // The last part of this tile to finish (an atomic count of K stages
+        // after a fence; nobody waits) reads the summed h back and writes a.
         __threadfence();
         epilogue_bar_sync();
-        if (et == 0) *split_last = atomicAdd(&tile_cnt[b * n_ctiles + c], 1) == ksplit - 1;
+        if (et == 0) {
+          const int mine = tc.kb1 - tc.kb0;
+          *split_last = atomicAdd(&tile_cnt[b * n_ctiles + c], mine) + mine == nk;
+        }
         epilogue_bar_sync();
         if (*split_last) {
           __threadfence();
@@ -1360,8 +1366,8 @@ cudaError_t launch_tc_n(const CUtensorMap &map_w, const TcArgs &a, cudaStream_t 
   err = ensure_smem_limit(reinterpret_cast<const void *>(kern), Cfg::kSmemBytes);
   if (err != cudaSuccess) return err;
   // persistent: one CTA per SM at most, each walking the tile list with stride gridDim.x
-  const int grid = static_cast<int>(
-      std::min<long>(a.max_blocks * a.n_ctiles * a.ksplit, num_sms()));
+  const long units = a.max_blocks * a.n_ctiles * a.ksplit;
+  const int grid = static_cast<int>(std::min<long>(units, num_sms()));
   if (grid <= 0) return cudaSuccess;
   return launch_pdl(kern, dim3(grid), dim3(kTcThreads), Cfg::kSmemBytes, s, map_w, a.src,
                     a.src_rows, a.sorted_ids, a.expert_ids, a.n_post, a.vec, a.P, a.top_k, a.E,
@@ -1405,6 +1411,7 @@ cudaError_t tc_w13_impl(const void *x, const void *w13, const float *w13_scale,
   cudaError_t err = make_weight_map(&map_w, w13, H, 2 * I, E, wide ? kTileM / 2 : kTileM, elt);
   if (err != cudaSuccess) return err;
   const int nk = (H + bke - 1) / bke;
+  // splits need the split-K scratch; 256-token tiles are not split
   if (wide || ksplit < 1 || ksplit > nk || h_acc == nullptr || tile_cnt == nullptr) ksplit = 1;
   TcArgs args{};
   args.src = static_cast<const uint16_t *>(x);
@@ -1436,7 +1443,8 @@ cudaError_t tc_w13_impl(const void *x, const void *w13, const float *w13_scale,
     // the first wave's experts: ceil(SMs / tiles per block) blocks, one expert
     // each at decode sizes, plus one for an expert without pairs among them
     const long per_e = 2l * I * H * elt;
-    const int wave = (num_sms() + args.n_ctiles * ksplit - 1) / (args.n_ctiles * ksplit) + 1;
+    const int per_block = args.n_ctiles * std::max(ksplit, 1);
+    const int wave = (num_sms() + per_block - 1) / per_block + 1;
     const int n_e = std::min(std::min(pf_experts, wave), E);
     args.w_pf = static_cast<const uint8_t *>(w13);
     args.pf_bytes = std::min<long>(n_e * per_e, 96l << 20);

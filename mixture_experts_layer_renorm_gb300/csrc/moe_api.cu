@@ -198,8 +198,18 @@ moe_status_t run_route(const uint16_t *x, const uint16_t *w_router, const uint16
 // Splits of each tile's K range for a grouped GEMM with n_ctiles weight tiles
 // per block: decode batches can have fewer tiles than SMs, or a last wave
 // that leaves most SMs idle.  The block count is estimated on the host as the
-// expected number of distinct experts, E (1 - (1 - top_k/E)^M).
-int pick_ksplit(int M, int E, int top_k, int n_ctiles, int nk) {
+// expected number of distinct experts, E (1 - (1 - top_k/E)^M).  Each split
+// beyond the first is charged split_cost of a tile's time (the fp32 partial
+// sums it adds, the finishing pass, the split scratch the routing kernel
+// clears): 0.15 with bf16 operands, 0.30 with E4M3 ones, whose mainloop is
+// half as long.  Measured against 0.03 on one box: Qwen3 decode M = 8
+// 115.3 -> 110.4 us (E4M3 102.6 -> 85.3), M = 32 204.0 -> 200.0 (E4M3
+// 143.4 -> 134.0), E60 tail M = 64 199.7 -> 189.8 (E4M3 144.0 -> 126.5),
+// 64-layer stack M = 16 7.97 -> 7.48 ms; M = 1 and M = 64 unchanged.
+constexpr double kSplitCostBf16 = 0.15;
+constexpr double kSplitCostE4M3 = 0.30;
+
+int pick_ksplit(int M, int E, int top_k, int n_ctiles, int nk, double split_cost) {
   if (M > kSplitMaxTokens) return 1;
   const double D = E * (1.0 - std::pow(1.0 - static_cast<double>(top_k) / E, M));
   const double tiles = std::max(1.0, std::ceil(D)) * n_ctiles;
@@ -209,7 +219,7 @@ int pick_ksplit(int M, int E, int top_k, int n_ctiles, int nk) {
   for (int ks = 1; ks <= 4 && ks <= nk; ++ks) {
     const double units = tiles * ks;
     const double eff = units / (std::ceil(units / sms) * sms);  // busy fraction of the waves
-    const double score = eff / (1.0 + 0.03 * (ks - 1));          // a split costs a little
+    const double score = eff / (1.0 + split_cost * (ks - 1));
     if (score > best_score + 1e-9) {
       best_score = score;
       best = ks;
@@ -228,7 +238,9 @@ moe_status_t run_gemm1(const uint16_t *x, const uint16_t *w13, const int32_t *so
   const int cap = static_cast<int>(capacity(P, E, B));
   switch (pick_path(M, E, top_k, B)) {
     case GemmPath::kTensorCore: {
-      const int ks = h_acc != nullptr ? pick_ksplit(M, E, top_k, (I + 127) / 128, (H + 63) / 64) : 1;
+      const int ks = h_acc != nullptr
+                         ? pick_ksplit(M, E, top_k, (I + 127) / 128, (H + 63) / 64, kSplitCostBf16)
+                         : 1;
       const double D = E * (1.0 - std::pow(1.0 - static_cast<double>(top_k) / E, M));
       const int pf_experts = (prefetch && D >= 0.9 * E) ? E : 0;
       return cuda_status(moe::launch_tc_w13_act(x, w13, sorted, eids, npost, static_cast<int>(P),
@@ -255,7 +267,7 @@ moe_status_t run_gemm2(const uint16_t *a, const uint16_t *w2, const int32_t *sor
   const int cap = static_cast<int>(capacity(P, E, B));
   switch (pick_path(M, E, top_k, B)) {
     case GemmPath::kTensorCore: {
-      const int ks = pick_ksplit(M, E, top_k, (H + 255) / 256, (I + 63) / 64);
+      const int ks = pick_ksplit(M, E, top_k, (H + 255) / 256, (I + 63) / 64, kSplitCostBf16);
       return cuda_status(moe::launch_tc_w2_combine(a, w2, sorted, eids, npost, wts,
                                                    static_cast<int>(P), top_k, E, H, I, B, cap,
                                                    yacc, ks, status, early_weights, s));
@@ -277,7 +289,9 @@ moe_status_t run_gemm1_f8(const uint8_t *qx, const float *sx, const uint8_t *w13
                           float *zero_dst, long zero_n, cudaStream_t s) {
   const long P = static_cast<long>(M) * top_k;
   const int cap = static_cast<int>(capacity(P, E, B));
-  const int ks = h_acc != nullptr ? pick_ksplit(M, E, top_k, (I + 127) / 128, (H + 127) / 128) : 1;
+  const int ks = h_acc != nullptr
+                     ? pick_ksplit(M, E, top_k, (I + 127) / 128, (H + 127) / 128, kSplitCostE4M3)
+                     : 1;
   const double D = E * (1.0 - std::pow(1.0 - static_cast<double>(top_k) / E, M));
   const int pf_experts = (prefetch && D >= 0.9 * E) ? E : 0;
   return cuda_status(moe::launch_tc_w13_act_f8(qx, sx, w13, w13s, sorted, eids, npost,
@@ -292,7 +306,7 @@ moe_status_t run_gemm2_f8(const uint8_t *qa, const float *sa, const uint8_t *w2,
                           float *yacc, int *status, bool early_weights, cudaStream_t s) {
   const long P = static_cast<long>(M) * top_k;
   const int cap = static_cast<int>(capacity(P, E, B));
-  const int ks = pick_ksplit(M, E, top_k, (H + 255) / 256, (I + 127) / 128);
+  const int ks = pick_ksplit(M, E, top_k, (H + 255) / 256, (I + 127) / 128, kSplitCostE4M3);
   return cuda_status(moe::launch_tc_w2_combine_f8(qa, sa, w2, w2s, sorted, eids, npost, wts,
                                                   static_cast<int>(P), top_k, E, H, I, B, cap,
                                                   yacc, ks, status, early_weights, s));
@@ -499,7 +513,7 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *w_router,
   // the fused routing kernel clears y_acc, and h_acc and the tile counters
   // behind it when GEMM 1 will split its K range (one span)
   const bool want_split = L.hacc != L.tcnt && pick_path(M, E, top_k, B) == GemmPath::kTensorCore &&
-                          pick_ksplit(M, E, top_k, (I + 127) / 128, (H + 63) / 64) > 1;
+                          pick_ksplit(M, E, top_k, (I + 127) / 128, (H + 63) / 64, kSplitCostBf16) > 1;
   const long zn = want_split ? static_cast<long>((L.total - L.yacc) / sizeof(float)) : yn;
   bool zeroed = false;
   st = run_route(x, w_router, router_logits, router_bias, M, E, top_k, H, renormalize, B,
@@ -654,7 +668,8 @@ moe_status_t moe_forward_fp8(const moe_bf16_t *x, const moe_bf16_t *w_router,
   float *sa = at<float>(ws, L.sa);
   const long yn = static_cast<long>(M) * H;
   const bool want_split =
-      L.hacc != L.tcnt && pick_ksplit(M, E, top_k, (I + 127) / 128, (H + 127) / 128) > 1;
+      L.hacc != L.tcnt &&
+      pick_ksplit(M, E, top_k, (I + 127) / 128, (H + 127) / 128, kSplitCostE4M3) > 1;
   const long zn = want_split ? static_cast<long>((L.total - L.yacc) / sizeof(float)) : yn;
   bool zeroed = false;
   st = run_route(x, w_router, router_logits, router_bias, M, E, top_k, H, renormalize, B,

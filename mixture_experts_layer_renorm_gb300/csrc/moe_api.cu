@@ -347,15 +347,24 @@ const char *moe_status_string(moe_status_t st) {
 int moe_pick_block_size(int M, int E, int top_k, int H, int I) {
   if (M <= 0 || E <= 0 || top_k <= 0) return 16;
   const double mean = static_cast<double>(M) * top_k / E;  // mean pairs per expert
-  if (mean <= 24) return 16;
-  if (mean <= 48) return 32;
-  if (mean <= 96) return 64;
+  // Blocks a few times the mean group: where the layer streams weights, one
+  // block per expert reads each expert's tiles once, and skewed routing
+  // (a few experts with many pairs) gains most (Zipf prefill: 256 tokens
+  // 193.8 -> 156.2 us with 64-token blocks, 512 tokens 218.4 -> 183.2 with
+  // 128, 1024 tokens 243.9 -> 217.6 with 128); decode batches of a few pairs
+  // per expert run the same with 16 or 32.
+  if (mean <= 6) return 16;
+  if (mean <= 12) return 32;
+  if (mean <= 24) return 64;
+  if (mean <= 64) return 128;
   // 256-token tiles (one N = 256 MMA per K step) pay off once their padding is
-  // small next to the groups: from about 256 pairs per expert when both GEMMs
+  // small next to the groups: from about 64 pairs per expert when both GEMMs
   // run them as 2-SM tiles (an even number of weight tiles: ceil(I/64) for
-  // GEMM 1, ceil(H/128) for GEMM 2), else from about 1024
+  // GEMM 1, ceil(H/128) for GEMM 2; E60 tail 1024 tokens 226.1 -> 214.7 us,
+  // 2048 tokens 250.0 -> 229.7, Zipf prefill 2048 tokens 288.5 -> 280.6),
+  // else from about 1024
   const bool pairs = ((I + 63) / 64) % 2 == 0 && ((H + 127) / 128) % 2 == 0;
-  if (mean >= (pairs ? 256 : 1024)) return 256;
+  if (pairs || mean >= 1024) return 256;
   return 128;
 }
 

@@ -66,10 +66,17 @@ def test_sizes_and_capacity(lib):
     assert moe.moe_workspace_size(300, 128, 8, 2048, 768, 16) >= moe.moe_workspace_size(256, 128, 8, 2048, 768, 16)
     for M in (1, 8, 64, 512, 4096, 16384):
         assert moe.moe_pick_block_size(M, 128, 8, 2048, 768) in (16, 32, 64, 128, 256)
-    # 256-token tiles from 256 pairs per expert where both GEMMs run 2-SM tiles
-    # (even weight-tile counts: ceil(I/64) and ceil(H/128)), else from 1024
-    assert moe.moe_pick_block_size(4096, 128, 8, 2048, 768) == 256      # 256 per expert, 12 and 16 tiles
-    assert moe.moe_pick_block_size(2048, 128, 8, 2048, 768) == 128      # 128 per expert
+    # blocks a few times the mean group: 16 up to 6 pairs per expert, 32 up to
+    # 12, 64 up to 24, 128 up to 64
+    assert moe.moe_pick_block_size(64, 128, 8, 2048, 768) == 16         # 4 per expert
+    assert moe.moe_pick_block_size(128, 128, 8, 2048, 768) == 32        # 8 per expert
+    assert moe.moe_pick_block_size(256, 128, 8, 2048, 768) == 64        # 16 per expert
+    assert moe.moe_pick_block_size(512, 128, 8, 2048, 768) == 128       # 32 per expert
+    assert moe.moe_pick_block_size(1024, 128, 8, 2048, 768) == 128      # 64 per expert
+    # then 256-token tiles where both GEMMs run 2-SM tiles (even weight-tile
+    # counts: ceil(I/64) and ceil(H/128)), else from 1024 per expert
+    assert moe.moe_pick_block_size(2048, 128, 8, 2048, 768) == 256      # 128 per expert, 12 and 16 tiles
+    assert moe.moe_pick_block_size(4096, 128, 8, 2048, 768) == 256      # 256 per expert
     assert moe.moe_pick_block_size(8192, 60, 4, 2048, 1408) == 256      # 546 per expert, 22 and 16 tiles
     assert moe.moe_pick_block_size(4096, 128, 8, 2048, 704) == 128      # 11 GEMM-1 weight tiles
     assert moe.moe_pick_block_size(16384, 128, 8, 2048, 704) == 256     # 1024 per expert

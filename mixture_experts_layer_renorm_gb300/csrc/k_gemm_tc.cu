@@ -558,8 +558,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
   const bool early = MODE == 1 && early_weights != 0;
   // Decode GEMM 1 inside a layer: while routing still runs, the CTAs bring the
   // weights their first tiles will most likely read (the lowest experts' W13,
-  // pf_bytes from w_pf) into L2; the host asks only when nearly every expert
-  // is routed to.  Weights never change, so this needs no wait.
+  // pf_bytes from w_pf) into L2; the host asks only when most of the experts
+  // are routed to.  Weights never change, so this needs no wait.
   if (MODE == 0 && pf_bytes > 0 && threadIdx.x == 0) {
     const long slice = ((pf_bytes + gridDim.x - 1) / gridDim.x + 15) / 16 * 16;
     const long begin = (long)blockIdx.x * slice;

@@ -89,3 +89,56 @@ def test_forward_replayed_from_a_cuda_graph(cfg, M, one_kernel, monkeypatch):
             compare_routed_layer(bits(y), g_ids, bits(lg_out), x_in, wt["w_router"],
                                  wt["router_bias"], wt["w13"], wt["w2"], w.top_k,
                                  x_in if w.residual else None, w.renormalize)
+
+
+# E4M3 expert weights: the two row quantizations join the captured chain and
+# the GEMMs' K splits run on 128-element stages.  Given logits keep routing
+# exact, so every replay is compared with the oracle's E4M3 layer directly;
+# with router weights (last case) the replay's logits are checked against
+# their fp32 bound and the oracle's layer is run on them.
+@pytest.mark.parametrize("cfg,M,given", [(2, 1, True), (2, 8, True), (2, 64, True), (5, 64, True),
+                                         (2, 8, False)])
+def test_forward_fp8_replayed_from_a_cuda_graph(cfg, M, given):
+    from test_gpu_fp8 import oracle_fp8
+    from test_gpu_parity import check_logits
+    w = synth.WORKLOADS[cfg]
+    wt = synth.layer_weights_fp8(w, device=DEV)
+    wr = None if given else wt["w_router"]
+    x_in = torch.empty((M, w.H), dtype=torch.bfloat16, device=DEV)
+    lg_in = torch.empty((M, w.E), dtype=torch.bfloat16, device=DEV) if given else None
+    lg_out = None if given else torch.empty((M, w.E), dtype=torch.bfloat16, device=DEV)
+    y = torch.empty((M, w.H), dtype=torch.bfloat16, device=DEV)
+    ids = torch.empty((M, w.top_k), dtype=torch.int32, device=DEV)
+    ws = moe.Workspace(M, w.E, w.top_k, w.H, w.I, 0, fp8=True)
+
+    def load(rep):
+        x_in.copy_(synth.normal_bf16((M, w.H), 1.0, 7100 + 31 * rep + M, DEV))
+        if given:
+            lg_in.copy_(synth.normal_bf16((M, w.E), 1.0, 7200 + 31 * rep + M, DEV))
+
+    def layer():
+        moe.moe_forward_fp8(x_in, wt["w13"], wt["w13_scale"], wt["w2"], wt["w2_scale"], w.top_k,
+                            y, ws, w_router=wr, router_logits=lg_in, router_bias=wt["router_bias"],
+                            renormalize=w.renormalize, topk_ids_out=ids, router_logits_out=lg_out)
+
+    load(0)
+    layer()  # per-device set-up outside the capture
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status(ws) == 0
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        layer()
+    for rep in (1, 2, 3):
+        load(rep)
+        y.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert moe.moe_get_device_status(ws) == 0
+        if given:
+            lg = bits(lg_in)
+        else:
+            lg = bits(lg_out)
+            check_logits(lg, x_in, wt["w_router"], wt["router_bias"])
+        ref = oracle_fp8(bits(x_in), wt, w.top_k, lg, renorm=w.renormalize)
+        assert np.array_equal(ids.cpu().numpy(), ref["topk_ids"]), f"replay {rep}: routing"
+        assert_close_bf16(bits(y), ref["y"], f"y (replay {rep})")

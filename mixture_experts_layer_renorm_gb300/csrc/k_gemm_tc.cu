@@ -644,6 +644,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
   // along K.
   const int kspl = ksplit < 1 ? 1 : ksplit;
   const int nk = (K + kBKe - 1) / kBKe;
+  const int Mt = MODE == 2 ? (src_rows + N - 1) / N * N : 0;  // router: tokens of all tiles
   const int n_tiles = n_blocks * n_cunits * kspl;
   const TileSched sched = make_sched(n_cunits, kspl, nk, n_blocks, MODE == 1 ? n_pass : 1);
   const int n_work = t0 < n_tiles ? (n_tiles - 1 - t0) / tstride + 1 : 0;
@@ -1126,6 +1127,21 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
             }
             __syncwarp();  // the next item overwrites the staging rows
           } else {
+            if constexpr (MODE == 2) {
+              if (partial) {
+                // a K range of the router's tile: its fp32 sums go to this split's
+                // slice [Mt][a_rows] of h_acc, laid out like the logits (a warp's
+                // lanes are consecutive experts: each store one 128-byte line);
+                // the last split of the tile adds the slices in split order
+                if (n < a_rows) {
+                  const int sp = (tc.kb0 * kspl + nk - 1) / nk;  // this range's split (balanced ranges)
+                  float *dst = h_acc + ((size_t)sp * Mt + (size_t)b * N + j0) * a_rows + n;
+#pragma unroll
+                  for (int jj = 0; jj < 16; ++jj) dst[(size_t)jj * a_rows] = __uint_as_float(o[jj]);
+                }
+                return;
+              }
+            }
             const bool valid = n < (MODE == 1 ? H_out : a_rows);
             const float bias = (MODE == 2 && valid && vec != nullptr) ? vec[n] : 0.f;
 #pragma unroll
@@ -1189,6 +1205,56 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmap_w, const uint16_t *__restrict
             }
           }
           if (et == 0) tile_cnt[b * n_ctiles + c] = 0;
+        }
+      }
+      if constexpr (MODE == 2) {
+        if (partial) {
+          // The router's tile cut along K: the last part to finish (counted in K
+          // stages, as above) adds the splits' slices in split order -- the
+          // same sum whichever part comes last -- and writes the logits.
+          __threadfence();
+          epilogue_bar_sync();
+          if (et == 0) {
+            const int mine = tc.kb1 - tc.kb0;
+            *split_last = atomicAdd(&tile_cnt[b * n_ctiles + c], mine) + mine == nk;
+          }
+          epilogue_bar_sync();
+          if (*split_last) {
+            __threadfence();
+            const int n_h = c * 2 * kTileM + kTileM < a_rows ? 2 : 1;
+            for (int h = 0; h < n_h; ++h) {
+              const int n = c * 2 * kTileM + h * kTileM + q * 32 + lane;
+              if (n >= a_rows) continue;
+              const float bias = vec != nullptr ? vec[n] : 0.f;
+              for (int j0 = 16 * half; j0 < N; j0 += 32) {
+                // every slice's 16 values loaded before any is added (one L2
+                // round trip per chunk; the scratch holds kRouterMaxSplits
+                // slices, those past kspl are not added), then added in split
+                // order
+                float v[kRouterMaxSplits][16];
+#pragma unroll
+                for (int sp = 0; sp < kRouterMaxSplits; ++sp) {
+                  const float *src = h_acc + ((size_t)sp * Mt + (size_t)b * N + j0) * a_rows + n;
+#pragma unroll
+                  for (int jj = 0; jj < 16; ++jj) v[sp][jj] = __ldcg(src + (size_t)jj * a_rows);
+                }
+                float sum[16];
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) {
+                  sum[jj] = 0.f;
+#pragma unroll
+                  for (int sp = 0; sp < kRouterMaxSplits; ++sp)
+                    if (sp < kspl) sum[jj] += v[sp][jj];
+                }
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) {
+                  const int d = dst_row[j0 + jj];
+                  if (d >= 0) out16[(size_t)d * a_rows + n] = float_to_bf16_bits(sum[jj] + bias);
+                }
+              }
+            }
+            if (et == 0) tile_cnt[b * n_ctiles + c] = 0;
+          }
         }
       }
     }
@@ -1561,7 +1627,8 @@ cudaError_t launch_selftest_timeout(int *status, int limit_ms, cudaStream_t s) {
 }
 
 cudaError_t launch_tc_router(const uint16_t *x, const uint16_t *w_router, const float *bias, int M,
-                             int E, int H, uint16_t *logits, int *status, cudaStream_t s) {
+                             int E, int H, uint16_t *logits, int *status, float *split_scratch,
+                             int *tile_cnt, cudaStream_t s) {
   CUtensorMap map_w;
   cudaError_t err = make_weight_map(&map_w, w_router, H, E, 1);
   if (err != cudaSuccess) return err;
@@ -1578,7 +1645,19 @@ cudaError_t launch_tc_router(const uint16_t *x, const uint16_t *w_router, const 
   args.a_rows = E;
   args.B = N;
   args.n_ctiles = (E + 2 * kTileM - 1) / (2 * kTileM);
-  args.ksplit = 1;
+  // Each CTA streams the whole of W_r through its TMA unit (32 stages at
+  // H = 2048): with fewer tiles than SMs, the tile's K range is split over
+  // up to kRouterMaxSplits CTAs whose fp32 partial sums meet in split_scratch
+  // (Zipf prefill, routing 512 tokens 34.4 -> 29.4 us, 4096 tokens 36.0 ->
+  // 34.3; more than kRouterCtlCount tiles keep one CTA per tile).
+  int ks = 1;
+  const int units = ((M + N - 1) / N) * args.n_ctiles;
+  const int nk = (H + kBK - 1) / kBK;
+  if (split_scratch != nullptr && tile_cnt != nullptr && units <= kRouterCtlCount)
+    ks = std::max(1, std::min({kRouterMaxSplits, num_sms() / units, nk}));
+  args.ksplit = ks;
+  args.h_acc = split_scratch;
+  args.tile_cnt = tile_cnt;
   args.out16 = logits;
   args.status = status;
   args.max_blocks = (M + N - 1) / N;

@@ -49,8 +49,24 @@ long capacity(long P, int E, int B) {
 // offset 0 so that moe_get_device_status can find it from the pointer alone.
 struct WsLayout {
   size_t status, logits, ids, wts, sorted, eids, offsets, npost, hist, a, qx, sx, qa, sa, yacc,
-      hacc, tcnt, total;
+      hacc, tcnt, rscr, total;
 };
+
+// S0: the tensor-core router from 256 tokens up, the CUDA-core one below.
+constexpr int kTcRouterMinTokens = 256;
+
+// Batches whose tensor-core router may split its tiles' K range (routing of
+// more than 256 tokens, at most moe::kRouterCtlCount tiles of 128 tokens):
+// the split scratch holds kRouterMaxSplits fp32 slices of the logits.
+bool router_may_split(int M, int E) {
+  return M > kTcRouterMinTokens &&
+         ((M + 127) / 128) * ((E + 255) / 256) <= moe::kRouterCtlCount;
+}
+size_t router_scratch_bytes(int M, int E) {
+  return router_may_split(M, E)
+             ? sizeof(float) * moe::kRouterMaxSplits * static_cast<size_t>(E) * ((M + 127) / 128 * 128)
+             : 0;
+}
 
 // Decode-sized batches (those the fused routing kernel serves) may split
 // GEMM 1's K range; they reserve its fp32 partial sums and tile counters.
@@ -87,6 +103,7 @@ WsLayout ws_layout(int M, int E, int top_k, int H, int I, int B, bool fp8 = fals
   const bool split = M <= kSplitMaxTokens;
   w.hacc = take(split ? sizeof(float) * static_cast<size_t>(P) * 2 * I : 0);
   w.tcnt = take(split ? sizeof(int32_t) * static_cast<size_t>(cap / B) * ((I + 127) / 128) : 0);
+  w.rscr = take(router_scratch_bytes(M, E));
   w.total = o;
   return w;
 }
@@ -149,13 +166,16 @@ int *lib_status() {
   return g_lib_status_ptr[dev];
 }
 
-// S0: the tensor-core router from 256 tokens up, the CUDA-core one below.
-constexpr int kTcRouterMinTokens = 256;
-
+// split_scratch (nullable): the router's split scratch and the control block
+// holding its tile counters (the workspace's), for entry points that have one.
 moe_status_t run_router(const uint16_t *x, const uint16_t *w_router, const float *bias, int M,
-                        int E, int H, uint16_t *logits, int *status, cudaStream_t s) {
+                        int E, int H, uint16_t *logits, int *status, float *split_scratch,
+                        int *control, cudaStream_t s) {
   if (M >= kTcRouterMinTokens && forced_path() != 1)
-    return cuda_status(moe::launch_tc_router(x, w_router, bias, M, E, H, logits, status, s));
+    return cuda_status(moe::launch_tc_router(
+        x, w_router, bias, M, E, H, logits, status, split_scratch,
+        split_scratch != nullptr && control != nullptr ? control + moe::kRouterCtlOffset : nullptr,
+        s));
   return cuda_status(moe::launch_router_logits(x, w_router, bias, M, E, H, logits, s));
 }
 
@@ -171,7 +191,8 @@ moe_status_t run_route(const uint16_t *x, const uint16_t *w_router, const uint16
                        const float *bias, int M, int E, int top_k, int H, int renormalize, int B,
                        uint16_t *logits_ws, int32_t *ids, float *wts, int32_t *sorted,
                        int32_t *eids, int32_t *offs, int32_t *npost, int32_t *hist, int *control,
-                       float *zero_buf, long zero_n, bool *zeroed, bool skip_sort, cudaStream_t s) {
+                       float *router_scratch, float *zero_buf, long zero_n, bool *zeroed,
+                       bool skip_sort, cudaStream_t s) {
   const long P = static_cast<long>(M) * top_k;
   const int cap = static_cast<int>(capacity(P, E, B));
   *zeroed = false;
@@ -184,7 +205,8 @@ moe_status_t run_route(const uint16_t *x, const uint16_t *w_router, const uint16
   }
   const uint16_t *logits = router_logits;
   if (w_router) {
-    moe_status_t st = run_router(x, w_router, bias, M, E, H, logits_ws, control, s);
+    moe_status_t st =
+        run_router(x, w_router, bias, M, E, H, logits_ws, control, router_scratch, control, s);
     if (st != MOE_OK) return st;
     logits = logits_ws;
   }
@@ -318,11 +340,16 @@ moe_status_t run_gemm2_f8(const uint8_t *qa, const float *sa, const uint8_t *w2,
 size_t workspace_bytes(int M_max, int E, int top_k, int H, int I, int block_size_m, bool fp8) {
   if (check_shapes(M_max, E, top_k, H, I) != MOE_OK) return 0;
   if (block_size_m != 0 && !valid_block_size(block_size_m)) return 0;
-  // a smaller batch may reserve split-K scratch that M_max does not
+  // a smaller batch may reserve split scratch that M_max does not: the GEMMs'
+  // (up to kSplitMaxTokens tokens) or the router's (up to kRouterCtlCount
+  // tiles of 128 tokens)
   const int M_split = std::min(M_max, kSplitMaxTokens);
+  const int M_rsplit =
+      std::min(M_max, moe::kRouterCtlCount / ((E + 255) / 256) * 128);
   auto need = [&](int B) {
-    return std::max(ws_layout(M_max, E, top_k, H, I, B, fp8).total,
-                    ws_layout(M_split, E, top_k, H, I, B, fp8).total);
+    return std::max({ws_layout(M_max, E, top_k, H, I, B, fp8).total,
+                     ws_layout(M_split, E, top_k, H, I, B, fp8).total,
+                     ws_layout(M_rsplit, E, top_k, H, I, B, fp8).total});
   };
   if (block_size_m != 0) return need(block_size_m);
   size_t best = 0;
@@ -395,7 +422,8 @@ moe_status_t moe_router_logits(const moe_bf16_t *x, const moe_bf16_t *w_router,
   if (M == 0) return MOE_OK;
   if (!x || !w_router || !logits) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w_router)) return MOE_ERR_INVALID_ARG;
-  return run_router(x, w_router, router_bias, M, E, H, logits, lib_status(), stream);
+  return run_router(x, w_router, router_bias, M, E, H, logits, lib_status(), nullptr, nullptr,
+                    stream);
 }
 
 moe_status_t moe_topk_softmax(const moe_bf16_t *logits, int M, int E, int top_k, int renormalize,
@@ -530,7 +558,8 @@ moe_status_t moe_forward(const moe_bf16_t *x, const moe_bf16_t *w_router,
   bool zeroed = false;
   st = run_route(x, w_router, router_logits, router_bias, M, E, top_k, H, renormalize, B,
                  logits_ws, ids, wts, sorted, eids, offs, npost,
-                 at<int32_t>(ws, L.hist), status, yacc, zn, &zeroed,
+                 at<int32_t>(ws, L.hist), status,
+                 router_may_split(M, E) ? at<float>(ws, L.rscr) : nullptr, yacc, zn, &zeroed,
                  /*skip_sort=*/P * 4 <= E, stream);
   if (st != MOE_OK) return st;
   uint16_t *a = at<uint16_t>(ws, L.a);
@@ -576,7 +605,8 @@ moe_status_t moe_route(const moe_bf16_t *x, const moe_bf16_t *w_router,
   return run_route(x, w_router, router_logits, router_bias, M, E, top_k, H, renormalize,
                    block_size_m, logits_ws, topk_ids, topk_weights,
                    sorted_token_ids, expert_ids, expert_offsets, num_tokens_post_padded,
-                   at<int32_t>(ws, L.hist), at<int>(ws, 0), nullptr, 0, &zeroed,
+                   at<int32_t>(ws, L.hist), at<int>(ws, 0),
+                   router_may_split(M, E) ? at<float>(ws, L.rscr) : nullptr, nullptr, 0, &zeroed,
                    /*skip_sort=*/false, stream);
 }
 
@@ -686,7 +716,8 @@ moe_status_t moe_forward_fp8(const moe_bf16_t *x, const moe_bf16_t *w_router,
   bool zeroed = false;
   st = run_route(x, w_router, router_logits, router_bias, M, E, top_k, H, renormalize, B,
                  logits_ws, ids, wts, sorted, eids, offs, npost, at<int32_t>(ws, L.hist), status,
-                 yacc, zn, &zeroed, /*skip_sort=*/P * 4 <= E, stream);
+                 router_may_split(M, E) ? at<float>(ws, L.rscr) : nullptr, yacc, zn, &zeroed,
+                 /*skip_sort=*/P * 4 <= E, stream);
   if (st != MOE_OK) return st;
   st = cuda_status(moe::launch_quant_rows(x, M, H, qx, sx, stream));
   if (st != MOE_OK) return st;

@@ -16,6 +16,9 @@ constexpr int kStatusBytes = 1024;
 constexpr int kCountersOffset = 64;
 constexpr int kRouteFusedMaxGroups = 64;   // token groups (<= 8 tokens each); one more counter for the align
 constexpr int kDecodeCtlOffset = 192;     // the decode-layer kernel's grid-barrier counters (3 ints)
+constexpr int kRouterCtlOffset = 196;     // the tensor-core router's tile counters when it splits K
+constexpr int kRouterCtlCount = 60;       // (one per tile; it splits only up to this many tiles)
+constexpr int kRouterMaxSplits = 4;
 
 // Programmatic dependent launch.  Every kernel of the library is launched with
 // launch_pdl, so it may become resident while the kernel before it in the
@@ -199,8 +202,12 @@ cudaError_t launch_quant_rows(const uint16_t *src, int R, int K, uint8_t *q, flo
 // One CTA whose bounded wait on an mbarrier nothing completes gives up after
 // about limit_ms ms and records the timeout status (self-test of that path).
 cudaError_t launch_selftest_timeout(int *status, int limit_ms, cudaStream_t s);
+// With split_scratch (kRouterMaxSplits * E * roundup(M, 128) floats) and
+// tile_cnt (zero, kRouterCtlCount ints, left zero) the K range of each tile
+// is split over up to kRouterMaxSplits CTAs when the tiles leave SMs idle.
 cudaError_t launch_tc_router(const uint16_t *x, const uint16_t *w_router, const float *bias, int M,
-                             int E, int H, uint16_t *logits, int *status, cudaStream_t s);
+                             int E, int H, uint16_t *logits, int *status, float *split_scratch,
+                             int *tile_cnt, cudaStream_t s);
 
 // y = bf16(y_acc + residual)
 cudaError_t launch_finalize(const float *y_acc, const uint16_t *residual, int M, int H, uint16_t *y,

@@ -527,6 +527,50 @@ def test_route_with_router_weights(cfg, M):
     assert np.array_equal(out["o"], ro)
 
 
+@pytest.mark.parametrize("M,E,k,H", [(300, 128, 8, 2048), (512, 128, 8, 2048), (1000, 60, 4, 2048),
+                                     (4096, 128, 8, 2048), (7680, 128, 8, 2048),
+                                     (2000, 300, 8, 1024), (513, 256, 8, 192)])
+def test_route_splits_the_router_k_range(M, E, k, H):
+    """Above 256 tokens with a workspace, the tensor-core router splits each
+    tile's K range over up to four CTAs when its tiles leave SMs idle (fp32
+    partial sums in per-split slices, added in split order by the tile's last
+    part): the logits lie within the fp32 bound of the exact products, the
+    routing is the oracle's up to near-ties, ids and lists are the oracle's
+    top-k and align of the logits used, and a second call on the same
+    workspace (tile counters back at zero) gives the same logits bit for bit.
+    Four splits of 32 stages (300 to 4096 tokens), two at the 60-tile limit
+    (7680), 60 experts (rows past E), 300 experts (two weight tiles), three
+    stages over three splits (H = 192) with one token in the last tile."""
+    x = rand_bf16((M, H), 1.0, 8100 + M + E)
+    wr = rand_bf16((E, H), 0.02, 8200 + E + H)
+    bias = synth.zipf_router_bias(E, 1.1).to(DEV) if E % 2 == 0 else None
+    B = 64
+    ws = moe.Workspace(M, E, k, 16, 16, B)
+    first = None
+    for call in range(2):
+        g_lg = torch.empty((M, E), dtype=torch.bfloat16, device=DEV)
+        out, ws = run_route(M, E, k, B, x=x, wr=wr, bias=bias, ws=ws, lg_out=g_lg)
+        g_lg = bits(g_lg)
+        if first is None:
+            first = g_lg
+            check_logits(g_lg, x, wr, bias)
+            bias_np = None if bias is None else bias.cpu().numpy()
+            o_lg = oracle.router_logits(bits(x), bits(wr), bias_np)
+            o_ids, _ = oracle.topk_softmax(o_lg, k)
+            n = assert_routing_explained(g_lg, out["ids"], o_lg, o_ids, k)
+            assert n <= max(1, 0.02 * M), f"{n} of {M} tokens routed differently"
+        else:
+            assert np.array_equal(g_lg, first), f"call {call}: logits differ from the first call"
+        rid, rw = oracle.topk_softmax(g_lg, k)
+        assert np.array_equal(out["ids"], rid)
+        assert np.abs(out["w"].astype(np.float64) - rw).max() <= W_ABS
+        rs, re_, ro, rn = oracle.align_block_size(rid, E, B)
+        nn = int(out["n"][0])
+        assert nn == rn
+        assert np.array_equal(out["s"][:nn], rs[:nn])
+        assert np.array_equal(out["o"], ro)
+
+
 @pytest.mark.parametrize("M,E,k,H,B", [(1, 128, 8, 2048, 16), (8, 128, 8, 2048, 16),
                                        (5, 60, 4, 2048, 16), (2, 20, 3, 256, 16),
                                        (8, 256, 8, 2048, 16), (3, 200, 6, 2112, 32),

@@ -126,7 +126,10 @@ moe_status_t moe_align_block_size(const int32_t *topk_ids, int M, int top_k, int
  * issue page describes a kernel that fuses the router with softmax and top-k,
  * and the MoE execution analysis page ("Per-decode-step kernel launches")
  * counts one launch per step per layer; for batches of up to 256 tokens (with
- * M * top_k <= 16384) this runs as one launch, otherwise as three kernels.
+ * M * top_k <= 16384) this runs as one launch, otherwise as the router (its
+ * K range split over up to four CTAs per tile, through the workspace, when
+ * the tiles leave SMs idle), top-k and align kernels (count and scatter above
+ * 2048 pairs).
  * Exactly one of w_router [E, H] and router_logits [M, E] is non-NULL
  * (router_bias only with w_router; H is ignored with router_logits).
  * Outputs as for moe_topk_softmax and moe_align_block_size (block_size_m

@@ -64,6 +64,14 @@ def test_sizes_and_capacity(lib):
         assert moe.moe_workspace_size(3, 4, 2, 128, 64, B) > 0
     # a batch below M_max may need more (it reserves split-K scratch): the size covers it
     assert moe.moe_workspace_size(300, 128, 8, 2048, 768, 16) >= moe.moe_workspace_size(256, 128, 8, 2048, 768, 16)
+    # and the router's split scratch (up to 60 tiles of 128 tokens): sizes never
+    # shrink as M_max grows, across both limits (E = 128: 7680 tokens; E = 1024:
+    # 15 tiles of four weight tiles, 1920 tokens), for the bf16 and E4M3 layers
+    for E, edge in ((128, 7680), (1024, 1920)):
+        for size in (moe.moe_workspace_size, moe.moe_workspace_size_fp8):
+            Ms = [edge - 128, edge - 1, edge, edge + 1, edge + 128, 2 * edge]
+            sizes = [size(M, E, 8, 2048, 768, 0) for M in Ms]
+            assert all(b >= a for a, b in zip(sizes, sizes[1:])), (E, size.__name__, sizes)
     for M in (1, 8, 64, 512, 4096, 16384):
         assert moe.moe_pick_block_size(M, 128, 8, 2048, 768) in (16, 32, 64, 128, 256)
     # blocks a few times the mean group: 16 up to 6 pairs per expert, 32 up to

@@ -74,8 +74,12 @@ def special_rows(K, seed):
     return torch.stack(rows).to(torch.bfloat16)
 
 
+# Below 4096 rows the two-pass kernel; from 4096 rows the register-resident
+# one, with rows of 1, 2, 4 and 8 16-byte chunks per lane (ragged ones too)
+# and more rows than one resident wave; rows past 2048 take two passes.
 @pytest.mark.parametrize("R,K", [(1, 16), (37, 2048), (513, 768), (8, 1408), (300, 208),
-                                 (4096, 2048)])
+                                 (70, 496), (4095, 2048), (4096, 2048), (6000, 768),
+                                 (4099, 208), (5000, 496), (4100, 1408), (4096, 2064), (9, 4096)])
 def test_quantize_rows_matches_the_oracle_bit_for_bit(R, K):
     src = rand_bf16((R, K), 1.0, 100 + R + K)
     sp = special_rows(K, R).to(DEV)
